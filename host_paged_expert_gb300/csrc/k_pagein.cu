@@ -1,0 +1,102 @@
+// Page-in: copy the experts a wave planned from the host store into slots.
+//
+// "Paged Experts" (SGLang docs), "Captured decode": a kernel copies the
+// planned experts of every paged tensor from the pinned host store into
+// their slots, reading host memory directly through its unified address and
+// taking the count from device memory, so each graph replay moves exactly the
+// experts it decided on.  Here one expert row holds every paged tensor of the
+// expert (w13, w2 and, for FP8, both scale grids), so copying the row pages
+// all of them together: a slot can never hold one expert's weights with
+// another expert's scales.
+//
+// The grid is fixed from shapes (a few CTAs per SM); CTAs stride over
+// (planned expert, 16 KiB chunk) items and stop at the device-side count.
+
+#include "pe_internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr size_t kChunk = (size_t)kCopyThreads * 16 * kCopyUnroll;  // bytes per item
+
+__device__ __forceinline__ int4 load_stream(const int4* p) {
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Copy one chunk of up to kChunk bytes (a multiple of 16).
+__device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                           size_t bytes) {
+    const int4* s = reinterpret_cast<const int4*>(src);
+    int4* d = reinterpret_cast<int4*>(dst);
+    const int nvec = (int)(bytes >> 4);
+    int4 v[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int i = threadIdx.x + u * kCopyThreads;
+        if (i < nvec) v[u] = load_stream(s + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+        const int i = threadIdx.x + u * kCopyThreads;
+        if (i < nvec) d[i] = v[u];
+    }
+}
+
+__global__ void __launch_bounds__(kCopyThreads) pagein_kernel(
+    const uint8_t* __restrict__ host_layer, uint8_t* __restrict__ slots_layer, size_t stride,
+    size_t copy_bytes, const int32_t* __restrict__ plan_expert, const int32_t* __restrict__ plan_slot,
+    const int32_t* __restrict__ plan_count, int max_count) {
+    const int count = min(*plan_count, max_count);
+    const size_t nchunk = (copy_bytes + kChunk - 1) / kChunk;
+    const size_t items = (size_t)count * nchunk;
+    for (size_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int p = (int)(it / nchunk);
+        const size_t c = it - (size_t)p * nchunk;
+        const size_t off = c * kChunk;
+        const size_t e = (size_t)plan_expert[p];
+        const size_t slot = (size_t)plan_slot[p];
+        copy_chunk(host_layer + e * stride + off, slots_layer + slot * stride + off,
+                   min(kChunk, copy_bytes - off));
+    }
+}
+
+__global__ void __launch_bounds__(kCopyThreads) copy_kernel(const uint8_t* __restrict__ src,
+                                                            uint8_t* __restrict__ dst, size_t bytes) {
+    const size_t nchunk = (bytes + kChunk - 1) / kChunk;
+    for (size_t c = blockIdx.x; c < nchunk; c += gridDim.x) {
+        const size_t off = c * kChunk;
+        copy_chunk(src + off, dst + off, min(kChunk, bytes - off));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pagein(const LayerDev& L, const Shape& s, const uint8_t* host_layer,
+                          uint8_t* slots_layer, int wave, int max_count, int num_sms,
+                          cudaStream_t st) {
+    const size_t nchunk = (s.copy_bytes + kChunk - 1) / kChunk;
+    const size_t want = (size_t)max_count * nchunk;
+    const int grid = (int)min(want, (size_t)num_sms * 4);
+    if (grid <= 0) return cudaSuccess;
+    pagein_kernel<<<grid, kCopyThreads, 0, st>>>(host_layer, slots_layer, s.stride, s.copy_bytes,
+                                                 L.plan_expert + (size_t)wave * s.K,
+                                                 L.plan_slot + (size_t)wave * s.K,
+                                                 L.plan_count + wave, max_count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st) {
+    const size_t nchunk = (bytes + kChunk - 1) / kChunk;
+    const int grid = (int)min(nchunk, (size_t)num_sms * 4);
+    if (grid <= 0) return cudaSuccess;
+    copy_kernel<<<grid, kCopyThreads, 0, st>>>((const uint8_t*)src, (uint8_t*)dst, bytes);
+    return cudaGetLastError();
+}
+
+}  // namespace pe

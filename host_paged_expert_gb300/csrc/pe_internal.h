@@ -1,0 +1,74 @@
+// Internal declarations shared by the libpe translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pe.h"
+
+namespace pe {
+
+constexpr int kMaxExperts = 1024;  // plan kernel keeps per-expert flags in shared memory
+constexpr int kMaxSlots = 1024;
+constexpr int kMaxTopK = 32;       // one warp lane per chosen expert
+constexpr int kPlanThreads = 1024;
+constexpr int kFp8Block = 128;
+
+enum Counter { C_STEPS = 0, C_WAVES, C_ENTRIES, C_DISTINCT, C_HITS, C_PAGE_INS, C_COLD, C_NUM };
+
+// Device pointers of one layer's residency state and last plan.
+struct LayerDev {
+    int32_t* slot_expert;   // [K]   expert held by each slot, -1 = empty
+    uint32_t* slot_tick;    // [K]   clock value of the slot's last use
+    int32_t* expert_slot;   // [E]   slot holding each expert, -1 = not resident
+    uint32_t* clock;        // [1]
+    unsigned long long* counters;  // [C_NUM]
+    int32_t* plan_expert;   // [Wmax][K]
+    int32_t* plan_slot;     // [Wmax][K]
+    int32_t* plan_count;    // [Wmax]
+    int32_t* num_waves;     // [1]
+    int32_t* topk_id;       // [maxT*k]
+    float* topk_w;          // [maxT*k]
+    int32_t* entry_slot;    // [maxT*k]
+    int32_t* entry_wave;    // [maxT*k]
+    const uint8_t* loaded;  // [E]   1 once the expert's host row was written
+};
+
+struct Shape {
+    int E, k, K, H, I, Wmax;
+    int dtype;
+    size_t stride;       // bytes between expert rows (slot or host store)
+    size_t copy_bytes;   // bytes a page-in moves (payload rounded up to 16)
+    size_t w13_off, s13_off, w2_off, s2_off;
+};
+
+// ---- launchers (each returns the launch status) ----
+
+// Routing of T tokens by one warp per token into topk_id / topk_w.
+cudaError_t launch_route(const LayerDev& L, const Shape& s, const float* logits, int T,
+                         uint32_t* err, cudaStream_t st);
+// LRU planning of all waves of one step (one CTA); routes inline when
+// route_inline is set (small T), else reads topk_id / topk_w.
+cudaError_t launch_plan(const LayerDev& L, const Shape& s, const float* logits, int T,
+                        int route_inline, uint32_t* err, cudaStream_t st);
+// Copy the experts planned for wave `wave` from the host store into slots.
+cudaError_t launch_pagein(const LayerDev& L, const Shape& s, const uint8_t* host_layer,
+                          uint8_t* slots_layer, int wave, int max_count, int num_sms,
+                          cudaStream_t st);
+// Plain device-side copy used by the host-link probe.
+cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
+// Decode expert MLP, part 1: h = SiLU(gate x) * (up x) for the wave's entries.
+cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                          const uint8_t* slots_layer, int wave, int T, float* hbuf,
+                          int num_sms, cudaStream_t st);
+// Decode expert MLP, part 2: w * (down h).  fused: sum the top-k in place
+// and write out (single wave); else write merged[entry] for the wave.
+cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
+                        int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
+                        int num_sms, cudaStream_t st);
+// out[t] = sum_j merged[t, j] in entry order, rounded to bf16.
+cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
+                            cudaStream_t st);
+
+}  // namespace pe

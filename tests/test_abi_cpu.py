@@ -1,0 +1,112 @@
+"""The C ABI library builds, loads and exports every declared entry point;
+pure entry points and argument validation work without a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from host_paged_expert_gb300 import _lib, synth
+from host_paged_expert_gb300.synth import MoEShape
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pe.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_lib.LIB_PATH):
+        from host_paged_expert_gb300 import build
+
+        build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pe_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for want in ("pe_create", "pe_load_host_expert", "pe_forward", "pe_stats", "pe_destroy",
+                 "pe_last_error", "pe_required_device_bytes", "pe_reset_residency"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in pe.h but not exported"
+    assert sorted(_lib.EXPORTS) == names
+
+
+def test_row_layout_matches_expert_sizes(L):
+    bf = _lib.row_layout(synth.STACK48)
+    assert bf["payload_bytes"] == 9_437_184 == synth.STACK48.expert_bytes
+    assert bf["row_stride"] == 9_437_184
+    assert bf["w2_offset"] == 6_291_456
+    f8 = _lib.row_layout(synth.STACK48_FP8)
+    assert f8["payload_bytes"] == 4_719_744 == synth.STACK48_FP8.expert_bytes
+    assert f8["s13_bytes"] == 4 * 12 * 16 and f8["s2_bytes"] == 4 * 16 * 6
+    for k in ("w13_offset", "s13_offset", "w2_offset", "s2_offset"):
+        assert f8[k] % 128 == 0
+    assert f8["row_stride"] % 256 == 0 and f8["row_stride"] >= f8["s2_offset"] + f8["s2_bytes"]
+    tiny = _lib.row_layout(synth.TINY)
+    assert tiny["payload_bytes"] == 3 * 256 * 128 * 2
+
+
+def test_max_waves_from_shapes(L):
+    s = synth.STACK48
+    assert _lib.max_waves(s, 1) == 1
+    assert _lib.max_waves(s, 4) == 1           # 32 entries fit K=32
+    assert _lib.max_waves(s, 5) == 2           # 40 entries, 40 distinct at most
+    assert _lib.max_waves(s, 2048) == 4        # at most E=128 distinct
+    assert _lib.max_waves(s.with_slots(128), 2048) == 1
+    assert _lib.max_waves(synth.TINY, 64) == 3  # 16 experts over K=6
+
+
+def test_required_bytes_cover_slot_table(L):
+    s = synth.STACK48
+    n = _lib.required_device_bytes(s, 8)
+    table = s.num_layers * s.num_slots * 9_437_184
+    assert table <= n < table + 64 * 2**20
+    assert _lib.required_device_bytes(s.with_slots(64), 8) > n
+
+
+@pytest.mark.parametrize("bad", [
+    dict(num_slots=1),            # K < top_k
+    dict(num_slots=200),          # K > E
+    dict(top_k=0),
+    dict(hidden=100),             # not a multiple of 8
+    dict(num_experts=2000),
+])
+def test_invalid_configs_rejected(L, bad):
+    base = dict(num_layers=2, num_experts=16, top_k=2, num_slots=6, hidden=256, intermediate=128)
+    base.update(bad)
+    s = MoEShape(**base)
+    cfg = _lib.make_config(s, 4)
+    assert L.pe_required_device_bytes(ctypes.byref(cfg)) == 0
+    h = ctypes.c_void_p()
+    st = L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h))
+    assert st == _lib.PE_ERR_INVALID
+    assert L.pe_last_error(None)
+
+
+def test_unsupported_dtype_and_fp8_shape(L):
+    cfg = _lib.make_config(synth.TINY, 4)
+    cfg.dtype = 7
+    h = ctypes.c_void_p()
+    assert L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == _lib.PE_ERR_UNSUPPORTED_DTYPE
+    s = MoEShape(1, 16, 2, 6, 200, 128, "fp8")  # H not a multiple of 128
+    cfg = _lib.make_config(s, 4)
+    assert L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == _lib.PE_ERR_INVALID
+
+
+def test_null_handle_calls_are_errors(L):
+    assert L.pe_forward(None, 0, None, None, None, 1, None) == _lib.PE_ERR_INVALID
+    assert L.pe_stats(None, -1, None) == _lib.PE_ERR_INVALID
+    assert L.pe_load_host_expert(None, 0, 0, None, None, None, None) == _lib.PE_ERR_INVALID
+    L.pe_destroy(None)
