@@ -1,0 +1,534 @@
+#!/usr/bin/env python
+"""Paged-MoE decode benchmark on one GB300 (one JSON line on stdout).
+
+A step is one decode token through the whole 48-layer paged MoE stack: per
+layer, routing + device LRU planning, page-in of the missing experts from the
+pinned host store, the SiLU-gated expert MLP of the token's top-8 entries and
+the top-k sum.  The default workload is the 48-layer bf16 stack (H=2048,
+I=768, E=128, top-8) with K=32 resident experts per layer at batch 1; router
+logits follow the drifting-bias recipe, so consecutive tokens reuse experts.
+
+Timed passes (each starts from empty slots and replays the same W+K tokens):
+  value  graph-replayed decode with inputs already in HBM (CUDA events);
+  e2e    the same through host buffers: the token's hidden states and logits
+         are copied in from pinned memory and the 48 outputs copied back,
+         inside the timed region;
+  trace  eager decode with per-kernel CUDA events (libpe's profiler) and
+         per-layer counters, used for the roofline figures.
+The oracle leg times the CPU reference on the host cores on a bounded sample.
+
+``--impl reference`` times the CPU reference as the reference arm.
+Multi-GPU: replicas only (one independent stack per GPU, no collective on
+the data path); launch with torchrun, value = sum over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from host_paged_expert_gb300 import synth  # noqa: E402
+
+METRIC = "paged-MoE decode tok/s (48 layers, K resident)"
+_T0 = time.time()
+
+
+def log(msg: str) -> None:
+    print(f"[bench {time.time() - _T0:7.1f}s] {msg}", file=sys.stderr, flush=True)
+HBM_NOMINAL_GBS = 7900.0
+
+
+def workload(name: str):
+    base = synth.STACK48
+    if name == "decode48":
+        return base.with_slots(32), 1, "48 layers, H=2048, I=768, E=128, top-8, K=32, bf16 experts, batch 1"
+    if name.startswith("graphed48_b"):
+        b = int(name[len("graphed48_b"):])
+        return base.with_slots(64), b, f"48 layers, H=2048, I=768, E=128, top-8, K=64, bf16, batch {b}"
+    if name.startswith("fp8_48_b"):
+        b = int(name[len("fp8_48_b"):])
+        return synth.STACK48_FP8, b, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, batch {b}"
+    raise SystemExit(f"unknown workload {name}")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=256)
+    p.add_argument("--warmup", type=int, default=8)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="decode48")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-trace", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--probe-bytes", type=int, default=2 << 30)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ inputs
+
+
+def make_inputs(shape, batch, n_tokens, seed=0):
+    zipf = 1.1 if shape.dtype == "fp8" else None
+    lg = synth.decode_logits(shape.num_layers, shape.num_experts, n_tokens, batch=batch, seed=seed, zipf_s=zipf)
+    lg = np.ascontiguousarray(lg.transpose(1, 0, 2, 3))  # [S, L, B, E]
+    hs = synth.hidden_states((n_tokens, shape.num_layers, batch), shape.hidden, seed=seed)  # [S, L, B, H]
+    return lg, hs
+
+
+def load_weights(model, weights):
+    s = weights.shape
+    for l in range(s.num_layers):
+        for e in range(s.num_experts):
+            model.load_expert(l, e, weights.row(l, e))
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.device = device
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if not self.proc or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks / traffic
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "host_paged_expert_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".h")):
+            h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload_name: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload_name, {}).get(kernel)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+# ------------------------------------------------------------------ our arm
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from host_paged_expert_gb300 import _lib
+
+    dev = local_rank
+    torch.cuda.set_device(dev)
+    shape, B, desc = workload(args.workload)
+    L, E, H, k = shape.num_layers, shape.num_experts, shape.hidden, shape.top_k
+    W, K = args.warmup, args.steps
+    S = W + K
+
+    t0 = time.time()
+    weights = synth.ExpertWeights(shape, seed=0)
+    log("weights pool ready")
+    model = _lib.PagedMoE(shape, max_tokens=B, device=dev)
+    log(f"handle created: arena {model.arena.numel() / 1e9:.2f} GB, host store "
+        f"{shape.num_layers * shape.num_experts * model.layout['row_stride'] / 1e9:.2f} GB pinned")
+    load_weights(model, weights)
+    t_load = time.time() - t0
+    log("experts loaded into the host store")
+    payload = model.layout["payload_bytes"]
+
+    lg_h, hs_h = make_inputs(shape, B, S)
+    stream = torch.cuda.Stream(device=dev)
+    sp = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        lg_d = torch.from_numpy(lg_h).to(dev)
+        hs_d = torch.from_numpy(hs_h.view(np.int16)).view(torch.bfloat16).to(dev)
+        x_st = torch.zeros((L, B, H), dtype=torch.bfloat16, device=dev)
+        l_st = torch.zeros((L, B, E), dtype=torch.float32, device=dev)
+        y_st = torch.zeros((L, B, H), dtype=torch.bfloat16, device=dev)
+    stream.synchronize()
+
+    # host-link probe: pinned host store -> HBM, copy engine and device-side loads
+    ce_gbs, kn_gbs = model.probe_host_link(min(args.probe_bytes, L * E * model.layout["row_stride"]), 3, stream)
+    link_gbs = max(ce_gbs, kn_gbs)
+    log(f"host link probe: copy engine {ce_gbs:.1f} GB/s, device loads {kn_gbs:.1f} GB/s")
+
+    xp, lp, yp = x_st.data_ptr(), l_st.data_ptr(), y_st.data_ptr()
+    xs, ls, ys = B * H * 2, B * E * 4, B * H * 2
+
+    def launch_token():
+        for l in range(L):
+            model.forward_ptr(l, xp + l * xs, lp + l * ls, yp + l * ys, B, sp)
+
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            launch_token()
+
+    def step(t):
+        x_st.copy_(hs_d[t], non_blocking=True)
+        l_st.copy_(lg_d[t], non_blocking=True)
+        if graph is not None:
+            graph.replay()
+        else:
+            launch_token()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- value pass
+    with torch.cuda.stream(stream):
+        model.reset_residency(stream)
+        for t in range(W):
+            step(t)
+        s0 = model.stats(-1)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(dev) as clk:
+            ev0.record(stream)
+            for t in range(W, S):
+                step(t)
+            ev1.record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        s1 = model.stats(-1)
+    clocks = clk.summary()
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    tok_s = world * K * B / (ms * 1e-3)
+    log(f"value pass: {ms:.1f} ms for {K} steps -> {tok_s:.1f} tok/s")
+    d = {n: s1[n] - s0[n] for n in ("steps", "waves", "entries", "distinct", "hits", "page_ins")}
+
+    # ---- e2e pass: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hs_pin = torch.from_numpy(hs_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+        lg_pin = torch.from_numpy(lg_h).pin_memory()
+        y_pin = torch.empty((S, L, B, H), dtype=torch.bfloat16).pin_memory()
+        with torch.cuda.stream(stream):
+            model.reset_residency(stream)
+
+            def step_host(t):
+                x_st.copy_(hs_pin[t], non_blocking=True)
+                l_st.copy_(lg_pin[t], non_blocking=True)
+                if graph is not None:
+                    graph.replay()
+                else:
+                    launch_token()
+                y_pin[t].copy_(y_st, non_blocking=True)
+
+            for t in range(W):
+                step_host(t)
+            stream.synchronize()
+            barrier()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for t in range(W, S):
+                step_host(t)
+            b.record(stream)
+            stream.synchronize()
+            e_ms = a.elapsed_time(b)
+        if world > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": round(world * K * B / (e_ms * 1e-3), 2), "unit": "tok/s",
+               "h2d_bytes_per_step": L * B * (H * 2 + E * 4), "d2h_bytes_per_step": L * B * H * 2}
+
+    # ---- trace pass: per-kernel events, per-layer counters, layer-step latency
+    trace = None
+    if not args.no_trace:
+        peaks = measured_peaks()
+        with torch.cuda.stream(stream):
+            model.reset_residency(stream)
+            for t in range(W):
+                step(t)
+            stream.synchronize()
+            model.profile_enable(True)
+            prev = [model.stats(l) for l in range(L)]
+            roof_s = 0.0
+            lat = []
+            for t in range(W, S):
+                x_st.copy_(hs_d[t], non_blocking=True)
+                l_st.copy_(lg_d[t], non_blocking=True)
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)]
+                evs[0].record(stream)
+                for l in range(L):
+                    model.forward_ptr(l, xp + l * xs, lp + l * ls, yp + l * ys, B, sp)
+                    evs[l + 1].record(stream)
+                stream.synchronize()
+                lat += [evs[l].elapsed_time(evs[l + 1]) * 1e3 for l in range(L)]
+                cur = [model.stats(l) for l in range(L)]
+                for l in range(L):
+                    dist = cur[l]["distinct"] - prev[l]["distinct"]
+                    pin = cur[l]["page_ins"] - prev[l]["page_ins"]
+                    roof_s += max(dist * payload / (peaks["hbm_gbs"] * 1e9), pin * payload / (link_gbs * 1e9))
+                prev = cur
+            prof = model.profile_read()
+            model.profile_enable(False)
+        trace = {"prof": prof, "roof_s": roof_s, "lat_us": lat, "peaks": peaks}
+
+    out = {"tok_s": tok_s, "ms": ms, "clocks": clocks, "d": d, "e2e": e2e, "trace": trace,
+           "link": {"copy_engine_gbs": round(ce_gbs, 1), "kernel_gbs": round(kn_gbs, 1)},
+           "t_load": t_load, "shape": shape, "B": B, "desc": desc, "payload": payload,
+           "layout": model.layout, "lg_h": lg_h, "hs_h": hs_h, "weights": weights}
+    model.close()
+    return out
+
+
+def launches_per_layer_step(shape, B):
+    from host_paged_expert_gb300 import _lib
+
+    Wm = _lib.max_waves(shape, B)
+    n = 1 + 3 * Wm + (1 if Wm > 1 else 0)
+    if B > 32:
+        n += 1
+    return n
+
+
+# ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
+
+
+def oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=None, n_steps=None, warm=0):
+    """Run the CPU oracle over layer-steps in token order (token t, layer l),
+    converting each routed expert's weights from storage every time, until
+    ``budget_s`` seconds or ``n_steps`` layer-steps.  Returns (steps, seconds)."""
+    from oracle import mlp as omlp
+
+    L = shape.num_layers
+    layers = [omlp.PagedLayer(shape.num_experts, shape.num_slots, shape.top_k,
+                              (lambda l: (lambda e: omlp.expert_weights(weights.row(l, e), shape.dtype)))(l))
+              for l in range(L)]
+    done, t0 = 0, None
+    total = lg_h.shape[0] * L
+    i = 0
+    while i < total:
+        if i == warm:
+            t0 = time.perf_counter()
+        t, l = divmod(i, L)
+        layers[l].step(hs_h[t, l], lg_h[t, l])
+        i += 1
+        if i > warm:
+            done += 1
+            el = time.perf_counter() - t0
+            if (budget_s is not None and el >= budget_s) or (n_steps is not None and done >= n_steps):
+                return done, el
+    return done, time.perf_counter() - t0 if t0 else 0.0
+
+
+def blas_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    shape, B, desc = workload(args.workload)
+    weights = synth.ExpertWeights(shape, seed=0)
+    n_tok = max(1, -(-(args.warmup + args.steps) // shape.num_layers)) + 1
+    lg_h, hs_h = make_inputs(shape, B, n_tok)
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, n_steps=args.steps, warm=args.warmup)
+    tok_s = steps / shape.num_layers * B / sec
+    line = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tok/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": f"{args.workload}: {desc}",
+                                            "step": "one layer-step of the CPU oracle; tok/s = layer-steps / 48 / s"},
+            "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"{steps} layer-steps after {args.warmup} warm-up layer-steps, "
+                                       "token-major over the 48 layers"},
+            "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    import torch
+
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    r = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    shape, B = r["shape"], r["B"]
+    L = shape.num_layers
+    lay = r["layout"]
+    d = r["d"]
+    line = {
+        "metric": METRIC, "value": round(r["tok_s"], 2), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype,
+        "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {r['desc']}", "global_batch": B * world,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "graph": not args.no_graph,
+                   "l2": "inputs larger than L2: each step streams ~%.1f GB of expert weights"
+                         % (d["distinct"] / args.steps * r["payload"] / 1e9)},
+        "clocks": r["clocks"],
+        "gpu_launches": args.steps * L * launches_per_layer_step(shape, B),
+        "page_in": {"per_token": round(d["page_ins"] / args.steps, 3),
+                    "miss_rate_per_entry": round(d["page_ins"] / max(1, d["entries"]), 4),
+                    "miss_rate_per_distinct": round(d["page_ins"] / max(1, d["distinct"]), 4),
+                    "bytes_per_token": int(d["page_ins"] / args.steps * r["payload"]),
+                    "link_probe_gbs": r["link"]},
+        "setup_s": round(r["t_load"], 1),
+    }
+    if r["e2e"]:
+        line["e2e"] = r["e2e"]
+    tr = r["trace"]
+    if tr:
+        peaks = tr["peaks"]
+        prof = tr["prof"]
+        link = max(r["link"]["copy_engine_gbs"], r["link"]["kernel_gbs"])
+        alg = {"pagein": d["page_ins"] * r["payload"],
+               "gateup": d["distinct"] * (lay["w13_bytes"] + lay["s13_bytes"]),
+               "down": d["distinct"] * (lay["w2_bytes"] + lay["s2_bytes"])}
+        kernels = {}
+        for name, v in prof.items():
+            if not v["launches"]:
+                continue
+            ent = {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
+                   "avg_us": round(v["total_ms"] / v["launches"] * 1e3, 2)}
+            if name in alg:
+                bound = "host_link" if name == "pagein" else "hbm"
+                peak = link if name == "pagein" else peaks["hbm_gbs"]
+                ach = alg[name] / (v["total_ms"] * 1e-3) / 1e9 if v["total_ms"] > 0 else 0.0
+                ent.update({"bound": bound, "achieved_gbs": round(ach, 1), "peak_gbs": round(peak, 1),
+                            "frac": round(ach / peak, 4),
+                            "bytes_per_launch": round(alg[name] / v["launches"])})
+            kernels[name] = ent
+        dom = max((n for n in kernels if n in alg), key=lambda n: kernels[n]["total_ms"])
+        kd = kernels[dom]
+        line["roofline"] = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved_gbs"],
+                            "peak": kd["peak_gbs"], "unit": "GB/s", "frac": kd["frac"],
+                            "traffic": ncu_traffic(dom, args.workload),
+                            "peak_src": ("same-run host-link probe (best of copy engine and device loads)"
+                                         if dom == "pagein" else f"MEASURED_PEAKS.json hbm_gbs ({peaks['src']})"),
+                            "bytes_per_launch": kd["bytes_per_launch"]}
+        line["kernels"] = kernels
+        lat = sorted(tr["lat_us"])
+        line["layer_step_us"] = {"p50": round(lat[len(lat) // 2], 1), "p99": round(lat[int(len(lat) * 0.99)], 1),
+                                 "mean": round(sum(lat) / len(lat), 1), "source": "eager trace pass"}
+        line["layer_roofline"] = {
+            "frac": round(tr["roof_s"] * 1e3 / r["ms"], 4),
+            "roofline_ms_per_step": round(tr["roof_s"] * 1e3 / args.steps, 4),
+            "definition": "sum over layer-steps of max(distinct*expert_bytes/HBM, page_ins*expert_bytes/link) "
+                          "divided by the graph-timed value pass",
+            "hbm_gbs": peaks["hbm_gbs"], "link_gbs": link}
+    if world == 1 and not args.no_cpu_baseline:
+        steps, sec = oracle_layer_steps(shape, r["weights"], r["lg_h"], r["hs_h"], budget_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(steps / L * B / sec, 4), "unit": "tok/s", "cores": blas_threads(),
+                                "kind": "oracle",
+                                "sample": f"first {steps} layer-steps (token-major) of this workload, "
+                                          f"{sec:.1f} s, fp64 numpy"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
