@@ -15,6 +15,7 @@
 // projection gives the same bits.  That is what makes the paged output equal
 // the unpaged (K = E) output bit for bit.
 
+#include "pe_device.cuh"
 #include "pe_internal.h"
 
 namespace pe {
@@ -22,8 +23,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-
-__device__ __forceinline__ int4 ldg16(const void* p) { return __ldg(reinterpret_cast<const int4*>(p)); }
+constexpr int kCopyLoads = 8;                               // 16-byte loads per lane per copy item
+constexpr size_t kWarpCopy = (size_t)32 * 16 * kCopyLoads;  // 4 KiB per copy item
+constexpr int kStageXBytes = 48 * 1024;                     // tokens' x staged in shared memory up to this
 
 // acc += sum of the 8 bf16 products of w and x, in element order.
 __device__ __forceinline__ float dot8_bf16(int4 w, int4 x, float acc) {
@@ -49,13 +51,28 @@ __device__ __forceinline__ float dot8_bf16_f32(int4 w, float4 h0, float4 h1, flo
     return acc;
 }
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
-
 __device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.f, expf(-g))); }
+
+// h = SiLU(gate . x) * (up . x) for one gate/up row pair held by the warp
+// (chunk c of lane l covers elements 8*(l + 32c) .. +7).  Every path that
+// computes an h value goes through this function, so h does not depend on
+// where the weights were read from.
+// xr is a generic pointer to the token's bf16 row (shared or global memory).
+template <int CPL>
+__device__ __forceinline__ float row_pair_h(const int4 (&gv)[CPL], const int4 (&uv)[CPL], const uint8_t* xr,
+                                            int lane, int nchunk) {
+    float ag = 0.f, au = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        const int4 xv = idx < nchunk ? *reinterpret_cast<const int4*>(xr + 16 * (size_t)idx) : make_int4(0, 0, 0, 0);
+        ag = dot8_bf16(gv[c], xv, ag);
+        au = dot8_bf16(uv[c], xv, au);
+    }
+    ag = warp_sum(ag);
+    au = warp_sum(au);
+    return __fmul_rn(silu(ag), au);
+}
 
 // h[i, n] = SiLU(gate_n . x_t) * (up_n . x_t) for entries i of `wave`.
 // CPL = 16-byte chunks of an H-long row per lane.
@@ -77,27 +94,129 @@ __global__ void __launch_bounds__(kThreads) gateup_bf16_kernel(LayerDev L, Shape
         const uint8_t* g = w13 + (size_t)n * row_bytes;
         const uint8_t* u = w13 + (size_t)(s.I + n) * row_bytes;
         const uint8_t* xr = reinterpret_cast<const uint8_t*>(x + (size_t)(i / s.k) * s.H);
-        int4 gv[CPL], uv[CPL], xv[CPL];
+        int4 gv[CPL], uv[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
             const int idx = lane + 32 * c;
             if (idx < nchunk) {
                 gv[c] = ldg16(g + 16 * (size_t)idx);
                 uv[c] = ldg16(u + 16 * (size_t)idx);
-                xv[c] = ldg16(xr + 16 * (size_t)idx);
             } else {
-                gv[c] = uv[c] = xv[c] = make_int4(0, 0, 0, 0);
+                gv[c] = uv[c] = make_int4(0, 0, 0, 0);
             }
         }
-        float ag = 0.f, au = 0.f;
+        const float h = row_pair_h<CPL>(gv, uv, xr, lane, nchunk);
+        if (lane == 0) hbuf[(size_t)i * s.I + n] = h;
+    }
+}
+
+// Gate/up of one wave fused with its page-in (decode sizes: at most
+// kFusedMaxEntries entries).  Warp work items, in this order:
+//   1. gate/up row pairs of the members paged in this wave: read from the
+//      host store, written to the member's slot, and used for h right away;
+//   2. the rest of each paged row (w2 and scales) copied host -> slot in
+//      8 KiB pieces;
+//   3. gate/up row pairs of the members that were already resident (HBM).
+// Link-bound items come first so the host link is busy from the start while
+// the HBM-bound items fill the remaining warps.  For each row pair the warp
+// computes h for every entry of the wave routed to that member.
+template <int CPL>
+__global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
+    LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ host,
+    uint8_t* __restrict__ slots, int wave, int T, float* __restrict__ hbuf, int stage_x) {
+    extern __shared__ int4 sh_x[];
+    const int lane = threadIdx.x & 31;
+    const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
+    if (stage_x) {  // the wave's tokens, once per CTA
+        const int nvec = T * s.H / 8;
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) sh_x[i] = ldg16(xbase + 16 * (size_t)i);
+        __syncthreads();
+        xbase = reinterpret_cast<const uint8_t*>(sh_x);
+    }
+    const int nchunk = s.H >> 3;
+    const size_t row_bytes = (size_t)s.H * 2;
+    const int size = L.member_count[wave];
+    const int count = L.plan_count[wave];
+    const int nent = T * s.k;
+    const long long miss_rows = (long long)count * s.I;
+    const size_t tail_bytes = s.copy_bytes - s.tail_off;
+    const long long copies_per = (long long)((tail_bytes + kWarpCopy - 1) / kWarpCopy);
+    const long long copies = (long long)count * copies_per;
+    const long long total = miss_rows + copies + (long long)(size - count) * s.I;
+    const int32_t* mexp = L.member_expert + (size_t)wave * s.K;
+    const int32_t* mslot = L.member_slot + (size_t)wave * s.K;
+    for (long long item = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); item < total;
+         item += (long long)gridDim.x * kWarps) {
+        if (item >= miss_rows && item < miss_rows + copies) {
+            const long long c = item - miss_rows;
+            const int q = (int)(c / copies_per);
+            const size_t off = s.tail_off + (size_t)(c - (long long)q * copies_per) * kWarpCopy;
+            const uint8_t* src = host + (size_t)mexp[q] * s.stride + off;
+            uint8_t* dst = slots + (size_t)mslot[q] * s.stride + off;
+            const size_t nbytes = min(kWarpCopy, s.copy_bytes - off);
+            int4 v[kCopyLoads];
+#pragma unroll
+            for (int u = 0; u < kCopyLoads; ++u) {
+                const size_t o = ((size_t)u * 32 + lane) * 16;
+                if (o < nbytes) v[u] = ld_nc_na(src + o);
+            }
+#pragma unroll
+            for (int u = 0; u < kCopyLoads; ++u) {
+                const size_t o = ((size_t)u * 32 + lane) * 16;
+                if (o < nbytes) *reinterpret_cast<int4*>(dst + o) = v[u];
+            }
+            continue;
+        }
+        int q, n;
+        if (item < miss_rows) {
+            q = (int)(item / s.I);
+            n = (int)(item - (long long)q * s.I);
+        } else {
+            const long long r = item - miss_rows - copies;
+            q = count + (int)(r / s.I);
+            n = (int)(r - (long long)(q - count) * s.I);
+        }
+        const bool from_host = q < count;
+        const int slot = mslot[q];
+        uint8_t* slot_row = slots + (size_t)slot * s.stride + s.w13_off;
+        const uint8_t* g = (from_host ? host + (size_t)mexp[q] * s.stride + s.w13_off : slot_row) +
+                           (size_t)n * row_bytes;
+        const uint8_t* u = g + (size_t)s.I * row_bytes;
+        int4 gv[CPL], uv[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-            ag = dot8_bf16(gv[c], xv[c], ag);
-            au = dot8_bf16(uv[c], xv[c], au);
+            const int idx = lane + 32 * c;
+            if (idx < nchunk) {
+                gv[c] = from_host ? ld_nc_na(g + 16 * (size_t)idx) : ldg16(g + 16 * (size_t)idx);
+                uv[c] = from_host ? ld_nc_na(u + 16 * (size_t)idx) : ldg16(u + 16 * (size_t)idx);
+            } else {
+                gv[c] = uv[c] = make_int4(0, 0, 0, 0);
+            }
         }
-        ag = warp_sum(ag);
-        au = warp_sum(au);
-        if (lane == 0) hbuf[(size_t)i * s.I + n] = __fmul_rn(silu(ag), au);
+        if (from_host) {
+            uint8_t* gd = slot_row + (size_t)n * row_bytes;
+            uint8_t* ud = gd + (size_t)s.I * row_bytes;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                const int idx = lane + 32 * c;
+                if (idx < nchunk) {
+                    *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[c];
+                    *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[c];
+                }
+            }
+        }
+        for (int b0 = 0; b0 < nent; b0 += 32) {
+            const int i = b0 + lane;
+            const bool mine = i < nent && L.entry_wave[i] == wave && L.entry_slot[i] == slot;
+            unsigned mask = __ballot_sync(0xffffffffu, mine);
+            while (mask) {
+                const int ei = b0 + __ffs(mask) - 1;
+                mask &= mask - 1;
+                const uint8_t* xr = xbase + (size_t)(ei / s.k) * row_bytes;
+                const float h = row_pair_h<CPL>(gv, uv, xr, lane, nchunk);
+                if (lane == 0) hbuf[(size_t)ei * s.I + n] = h;
+            }
+        }
     }
 }
 
@@ -200,6 +319,24 @@ cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16
     else if (cpl <= 16) PE_GATEUP(16);
     else return cudaErrorInvalidValue;
 #undef PE_GATEUP
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gateup_pagein(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                 const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
+                                 float* hbuf, int num_sms, cudaStream_t st) {
+    const int grid = num_sms * 2;
+    const int cpl = (s.H / 8 + 31) / 32;
+    const size_t xbytes = (size_t)T * s.H * 2;
+    const int stage = xbytes <= (size_t)kStageXBytes;
+    const size_t smem = stage ? xbytes : 0;
+#define PE_GUP(C) gateup_pagein_bf16_kernel<C><<<grid, kThreads, smem, st>>>(L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)
+    if (cpl <= 1) PE_GUP(1);
+    else if (cpl <= 2) PE_GUP(2);
+    else if (cpl <= 4) PE_GUP(4);
+    else if (cpl <= 8) PE_GUP(8);
+    else return cudaErrorInvalidValue;
+#undef PE_GUP
     return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@
 // The grid is fixed from shapes (a few CTAs per SM); CTAs stride over
 // (planned expert, 16 KiB chunk) items and stop at the device-side count.
 
+#include "pe_device.cuh"
 #include "pe_internal.h"
 
 namespace pe {
@@ -20,14 +21,6 @@ namespace {
 constexpr int kCopyThreads = 256;
 constexpr int kCopyUnroll = 4;
 constexpr size_t kChunk = (size_t)kCopyThreads * 16 * kCopyUnroll;  // bytes per item
-
-__device__ __forceinline__ int4 load_stream(const int4* p) {
-    int4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
 
 // Copy one chunk of up to kChunk bytes (a multiple of 16).
 __device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
@@ -39,7 +32,7 @@ __device__ __forceinline__ void copy_chunk(const uint8_t* __restrict__ src, uint
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
         const int i = threadIdx.x + u * kCopyThreads;
-        if (i < nvec) v[u] = load_stream(s + i);
+        if (i < nvec) v[u] = ld_nc_na(s + i);
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {

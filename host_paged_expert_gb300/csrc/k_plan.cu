@@ -90,22 +90,23 @@ __global__ void __launch_bounds__(256) route_kernel(LayerDev L, int E, int k, co
                      L.topk_w + (size_t)warp * k, err);
 }
 
-// Exclusive block-wide prefix count of a per-thread flag (blockDim.x == 1024).
+// Exclusive block-wide prefix count of a per-thread flag; every thread of the
+// block calls it.  warp_tot needs 32 ints.
 __device__ __forceinline__ int block_prefix(bool flag, int* warp_tot, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const unsigned b = __ballot_sync(0xffffffffu, flag);
     const int in_warp = __popc(b & ((1u << lane) - 1u));
     if (lane == 0) warp_tot[warp] = __popc(b);
     __syncthreads();
     if (warp == 0) {
-        const int v = warp_tot[lane];
+        const int v = lane < nwarps ? warp_tot[lane] : 0;
         int incl = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int n = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += n;
         }
-        warp_tot[lane] = incl - v;
+        if (lane < nwarps) warp_tot[lane] = incl - v;
         if (lane == 31) *total = incl;
     }
     __syncthreads();
@@ -114,34 +115,34 @@ __device__ __forceinline__ int block_prefix(bool flag, int* warp_tot, int* total
     return r;
 }
 
-__global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev L, Shape s,
-                                                            const float* logits, int T,
-                                                            int route_inline, uint32_t* err) {
+// One CTA plans every wave of a step.  blockDim.x is a multiple of 32 and at
+// least E (thread e owns expert e in the scans) and K (thread s owns slot s).
+__global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape s,
+                                                               const float* logits, int T,
+                                                               int route_inline, uint32_t* err) {
     __shared__ int32_t sh_slot_expert[kMaxSlots];
     __shared__ uint32_t sh_tick[kMaxSlots];
     __shared__ int32_t sh_expert_slot[kMaxExperts];
     __shared__ int32_t sh_order[kMaxExperts];
     __shared__ int32_t sh_wave_of[kMaxExperts];
     __shared__ int32_t sh_slot_in_wave[kMaxExperts];
+    __shared__ int32_t sh_ids[kMaxExperts];  // routed ids of an inline-routed step (T*k <= 1024)
     __shared__ uint8_t sh_used[kMaxExperts];
     __shared__ uint8_t sh_inwave[kMaxExperts];
     __shared__ int sh_warp[32];
     __shared__ int sh_nR, sh_nM, sh_cold, sh_bad;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nthr = blockDim.x;
     const int E = s.E, K = s.K, k = s.k;
     const int nent = T * k;
+    const bool ids_in_smem = route_inline && nent <= kMaxExperts;
 
-    if (route_inline) {
-        for (int t = tid >> 5; t < T; t += kPlanThreads / 32)
-            route_token_warp(logits + (size_t)t * E, E, k, L.topk_id + (size_t)t * k,
-                             L.topk_w + (size_t)t * k, err);
-    }
-    for (int i = tid; i < K; i += kPlanThreads) {
+    // state loads first: they do not depend on routing
+    for (int i = tid; i < K; i += nthr) {
         sh_slot_expert[i] = L.slot_expert[i];
         sh_tick[i] = L.slot_tick[i];
     }
-    for (int e = tid; e < E; e += kPlanThreads) {
+    for (int e = tid; e < E; e += nthr) {
         sh_expert_slot[e] = L.expert_slot[e];
         sh_used[e] = 0;
         sh_inwave[e] = 0;
@@ -153,10 +154,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev L, Shape s,
         sh_bad = 0;
     }
     uint32_t clock = *L.clock;
-    __syncthreads();  // also publishes the inline routing's global writes
+    if (route_inline) {
+        for (int t = tid >> 5; t < T; t += nthr >> 5) {
+            route_token_warp(logits + (size_t)t * E, E, k, L.topk_id + (size_t)t * k,
+                             L.topk_w + (size_t)t * k, err);
+            if (ids_in_smem && (tid & 31) < k) sh_ids[t * k + (tid & 31)] = L.topk_id[(size_t)t * k + (tid & 31)];
+        }
+    }
+    __syncthreads();  // publishes the routing (shared and global) to the block
 
-    for (int i = tid; i < nent; i += kPlanThreads) {
-        const int e = L.topk_id[i];
+    for (int i = tid; i < nent; i += nthr) {
+        const int e = ids_in_smem ? sh_ids[i] : L.topk_id[i];
         if (e >= 0 && e < E)
             sh_used[e] = 1;
         else
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev L, Shape s,
     __syncthreads();
 
     // order = R ++ M, both ascending id
-    const int e = tid;  // E <= blockDim
+    const int e = tid;
     const bool used = e < E && sh_used[e];
     const bool isR = used && sh_expert_slot[e] >= 0;
     const bool isM = used && sh_expert_slot[e] < 0;
@@ -189,10 +197,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev L, Shape s,
         const int nres = (w == 0) ? nR : 0;  // only R can be resident, and R fits in wave 0
         const int nmiss = size - nres;
         ++clock;
-        for (int i = tid; i < size; i += kPlanThreads) {
+        for (int i = tid; i < size; i += nthr) {
             const int m = sh_order[base + i];
             sh_inwave[m] = 1;
-            if (i < nres) sh_tick[sh_expert_slot[m]] = clock;
+            if (i < nres) {
+                const int slot = sh_expert_slot[m];
+                sh_tick[slot] = clock;
+                // hits follow the page-ins in the member list
+                L.member_expert[(size_t)w * K + nmiss + i] = m;
+                L.member_slot[(size_t)w * K + nmiss + i] = slot;
+            }
         }
         __syncthreads();
         // rank of each victim slot in (tick, slot) order
@@ -224,44 +238,53 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(LayerDev L, Shape s,
             sh_slot_expert[slot] = m;
             sh_expert_slot[m] = slot;
             sh_tick[slot] = clock;
-            L.plan_expert[(size_t)w * K + my_rank] = m;
-            L.plan_slot[(size_t)w * K + my_rank] = slot;
+            const size_t q = (size_t)w * K + my_rank;
+            L.plan_expert[q] = m;
+            L.plan_slot[q] = slot;
+            L.member_expert[q] = m;
+            L.member_slot[q] = slot;
             if (!L.loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
         }
         __syncthreads();
-        for (int i = tid; i < size; i += kPlanThreads) {
+        for (int i = tid; i < size; i += nthr) {
             const int m = sh_order[base + i];
             sh_wave_of[m] = w;
             sh_slot_in_wave[m] = sh_expert_slot[m];
             sh_inwave[m] = 0;
         }
-        if (tid == 0) L.plan_count[w] = nmiss;
+        if (tid == 0) {
+            L.plan_count[w] = nmiss;
+            L.member_count[w] = size;
+        }
         total_miss += nmiss;
         __syncthreads();
     }
-    for (int w = nW + tid; w < s.Wmax; w += kPlanThreads) L.plan_count[w] = 0;
+    for (int w = nW + tid; w < s.Wmax; w += nthr) {
+        L.plan_count[w] = 0;
+        L.member_count[w] = 0;
+    }
 
-    for (int i = tid; i < nent; i += kPlanThreads) {
-        const int m = L.topk_id[i];
+    for (int i = tid; i < nent; i += nthr) {
+        const int m = ids_in_smem ? sh_ids[i] : L.topk_id[i];
         const bool ok = m >= 0 && m < E;
         L.entry_wave[i] = ok ? sh_wave_of[m] : -1;
         L.entry_slot[i] = ok ? sh_slot_in_wave[m] : 0;
     }
-    for (int i = tid; i < K; i += kPlanThreads) {
+    for (int i = tid; i < K; i += nthr) {
         L.slot_expert[i] = sh_slot_expert[i];
         L.slot_tick[i] = sh_tick[i];
     }
-    for (int m = tid; m < E; m += kPlanThreads) L.expert_slot[m] = sh_expert_slot[m];
+    for (int m = tid; m < E; m += nthr) L.expert_slot[m] = sh_expert_slot[m];
     if (tid == 0) {
         *L.clock = clock;
         *L.num_waves = nW;
-        L.counters[C_STEPS] += 1;
-        L.counters[C_WAVES] += nW;
-        L.counters[C_ENTRIES] += nent;
-        L.counters[C_DISTINCT] += nD;
-        L.counters[C_HITS] += nR;
-        L.counters[C_PAGE_INS] += total_miss;
-        L.counters[C_COLD] += sh_cold;
+        atomicAdd(&L.counters[C_STEPS], 1ull);
+        atomicAdd(&L.counters[C_WAVES], (unsigned long long)nW);
+        atomicAdd(&L.counters[C_ENTRIES], (unsigned long long)nent);
+        atomicAdd(&L.counters[C_DISTINCT], (unsigned long long)nD);
+        atomicAdd(&L.counters[C_HITS], (unsigned long long)nR);
+        atomicAdd(&L.counters[C_PAGE_INS], (unsigned long long)total_miss);
+        atomicAdd(&L.counters[C_COLD], (unsigned long long)sh_cold);
         if (sh_bad) atomicOr(err, PE_DEVERR_PLAN);
     }
 }
@@ -277,7 +300,11 @@ cudaError_t launch_route(const LayerDev& L, const Shape& s, const float* logits,
 
 cudaError_t launch_plan(const LayerDev& L, const Shape& s, const float* logits, int T,
                         int route_inline, uint32_t* err, cudaStream_t st) {
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(L, s, logits, T, route_inline, err);
+    int threads = s.E > s.K ? s.E : s.K;
+    if (route_inline && threads < 32 * T) threads = 32 * T;  // one warp per token
+    threads = (threads + 31) / 32 * 32;
+    if (threads > kPlanMaxThreads) threads = kPlanMaxThreads;
+    plan_kernel<<<1, threads, 0, st>>>(L, s, logits, T, route_inline, err);
     return cudaGetLastError();
 }
 

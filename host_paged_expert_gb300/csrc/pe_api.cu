@@ -81,8 +81,8 @@ struct Carver {
     }
 };
 
-enum ProfKind { P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_DOWN, P_SUM, P_NUM };
-const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "down", "topk_sum"};
+enum ProfKind { P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_NUM };
+const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "gateup_pagein", "down", "topk_sum"};
 
 }  // namespace
 
@@ -148,6 +148,9 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         d.plan_expert = cv.take<int32_t>((size_t)W * K);
         d.plan_slot = cv.take<int32_t>((size_t)W * K);
         d.plan_count = cv.take<int32_t>(W);
+        d.member_expert = cv.take<int32_t>((size_t)W * K);
+        d.member_slot = cv.take<int32_t>((size_t)W * K);
+        d.member_count = cv.take<int32_t>(W);
         d.num_waves = cv.take<int32_t>(1);
         d.topk_id = cv.take<int32_t>(maxTk);
         d.topk_w = cv.take<float>(maxTk);
@@ -234,6 +237,7 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
     s.s13_off = r.s13_offset;
     s.w2_off = r.w2_offset;
     s.s2_off = r.s2_offset;
+    s.tail_off = r.s13_offset;
     ce = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
     if (ce) {
         delete h;
@@ -411,6 +415,7 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
         reinterpret_cast<uintptr_t>(router_logits) % 4)
         return fail(h, PE_ERR_INVALID, "hidden/out must be 16-byte aligned, logits 4-byte aligned");
     if (hidden == out) return fail(h, PE_ERR_INVALID, "out may not alias hidden");
+    if (c.dtype != PE_BF16) return fail(h, PE_ERR_UNSUPPORTED_DTYPE, "block-FP8 forward is not available in this build");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int T = num_tokens;
@@ -436,16 +441,25 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
         if (e) return cuda_fail(h, e, "plan kernel");
     }
     const int fused = s.Wmax == 1;
+    // decode sizes page in inside the gate/up kernel; the choice depends on T
+    // only, and both routes compute every h with the same code
+    const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
     for (int w = 0; w < s.Wmax; ++w) {
-        {
-            ProfScope p(h, P_PAGEIN, st);
-            e = launch_pagein(L, s, host_layer, slots_layer, w, max_count, h->num_sms, st);
-            if (e) return cuda_fail(h, e, "page-in kernel");
-        }
-        {
-            ProfScope p(h, P_GATEUP, st);
-            e = launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
-            if (e) return cuda_fail(h, e, "gate/up kernel");
+        if (pagein_fused) {
+            ProfScope p(h, P_GATEUP_PAGEIN, st);
+            e = launch_gateup_pagein(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st);
+            if (e) return cuda_fail(h, e, "gate/up + page-in kernel");
+        } else {
+            {
+                ProfScope p(h, P_PAGEIN, st);
+                e = launch_pagein(L, s, host_layer, slots_layer, w, max_count, h->num_sms, st);
+                if (e) return cuda_fail(h, e, "page-in kernel");
+            }
+            {
+                ProfScope p(h, P_GATEUP, st);
+                e = launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
+                if (e) return cuda_fail(h, e, "gate/up kernel");
+            }
         }
         {
             ProfScope p(h, P_DOWN, st);

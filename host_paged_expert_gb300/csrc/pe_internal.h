@@ -12,7 +12,8 @@ namespace pe {
 constexpr int kMaxExperts = 1024;  // plan kernel keeps per-expert flags in shared memory
 constexpr int kMaxSlots = 1024;
 constexpr int kMaxTopK = 32;       // one warp lane per chosen expert
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanMaxThreads = 1024;
+constexpr int kFusedMaxEntries = 64;  // decode: one warp scans a wave's entries per weight row
 constexpr int kFp8Block = 128;
 
 enum Counter { C_STEPS = 0, C_WAVES, C_ENTRIES, C_DISTINCT, C_HITS, C_PAGE_INS, C_COLD, C_NUM };
@@ -27,6 +28,9 @@ struct LayerDev {
     int32_t* plan_expert;   // [Wmax][K]
     int32_t* plan_slot;     // [Wmax][K]
     int32_t* plan_count;    // [Wmax]
+    int32_t* member_expert; // [Wmax][K] wave members: the page-ins (plan order), then the hits
+    int32_t* member_slot;   // [Wmax][K] slot of each member while its wave runs
+    int32_t* member_count;  // [Wmax]
     int32_t* num_waves;     // [1]
     int32_t* topk_id;       // [maxT*k]
     float* topk_w;          // [maxT*k]
@@ -41,6 +45,7 @@ struct Shape {
     size_t stride;       // bytes between expert rows (slot or host store)
     size_t copy_bytes;   // bytes a page-in moves (payload rounded up to 16)
     size_t w13_off, s13_off, w2_off, s2_off;
+    size_t tail_off;     // start of everything after w13 (scales, w2): copied as one block
 };
 
 // ---- launchers (each returns the launch status) ----
@@ -58,6 +63,13 @@ cudaError_t launch_pagein(const LayerDev& L, const Shape& s, const uint8_t* host
                           cudaStream_t st);
 // Plain device-side copy used by the host-link probe.
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st);
+// Decode expert MLP, part 1 fused with page-in: for every member of the wave,
+// stream its gate/up rows (from the host store for page-ins, which are also
+// written to their slot; from the slot for hits) and compute h for every
+// entry routed to it; the rest of each paged row is copied alongside.
+cudaError_t launch_gateup_pagein(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                 const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
+                                 float* hbuf, int num_sms, cudaStream_t st);
 // Decode expert MLP, part 1: h = SiLU(gate x) * (up x) for the wave's entries.
 cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
                           const uint8_t* slots_layer, int wave, int T, float* hbuf,
