@@ -25,7 +25,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCopyLoads = 8;                               // 16-byte loads per lane per copy item
 constexpr size_t kWarpCopy = (size_t)32 * 16 * kCopyLoads;  // 4 KiB per copy item
-constexpr int kStageXBytes = 48 * 1024;                     // tokens' x staged in shared memory up to this
+constexpr int kStageXBytes = 48 * 1024;                     // dynamic shared memory budget of the fused kernel
 
 // acc += sum of the 8 bf16 products of w and x, in element order.
 __device__ __forceinline__ float dot8_bf16(int4 w, int4 x, float acc) {
@@ -81,6 +81,8 @@ __global__ void __launch_bounds__(kThreads) gateup_bf16_kernel(LayerDev L, Shape
                                                               const __nv_bfloat16* __restrict__ x,
                                                               const uint8_t* __restrict__ slots,
                                                               int wave, int T, float* __restrict__ hbuf) {
+    pdl_wait();
+    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int nchunk = s.H >> 3;
     const size_t row_bytes = (size_t)s.H * 2;
@@ -111,48 +113,67 @@ __global__ void __launch_bounds__(kThreads) gateup_bf16_kernel(LayerDev L, Shape
 }
 
 // Gate/up of one wave fused with its page-in (decode sizes: at most
-// kFusedMaxEntries entries).  Warp work items, in this order:
-//   1. gate/up row pairs of the members paged in this wave: read from the
-//      host store, written to the member's slot, and used for h right away;
-//   2. the rest of each paged row (w2 and scales) copied host -> slot in
-//      8 KiB pieces;
-//   3. gate/up row pairs of the members that were already resident (HBM).
-// Link-bound items come first so the host link is busy from the start while
-// the HBM-bound items fill the remaining warps.  For each row pair the warp
-// computes h for every entry of the wave routed to that member.
+// kFusedMaxEntries entries).  Two groups of CTAs run side by side:
+//   link CTAs  - gate/up row pairs of the members paged in this wave, read
+//                from the host store, written to the member's slot and used
+//                for h right away; then the rest of each paged row (w2 and
+//                scales) copied host -> slot in 4 KiB pieces;
+//   HBM CTAs   - gate/up row pairs of the members that were already resident.
+// The host link stays busy for the whole kernel while the resident experts
+// stream from HBM underneath it.  For each row pair the warp computes h for
+// every entry of the wave routed to that member.
+//
+// Dynamic shared memory: [member experts K][member slots K][entry keys nent]
+// then, when it fits, the wave's token rows of x.
 template <int CPL>
 __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
     LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ host,
     uint8_t* __restrict__ slots, int wave, int T, float* __restrict__ hbuf, int stage_x) {
-    extern __shared__ int4 sh_x[];
-    const int lane = threadIdx.x & 31;
-    const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
-    if (stage_x) {  // the wave's tokens, once per CTA
-        const int nvec = T * s.H / 8;
-        for (int i = threadIdx.x; i < nvec; i += blockDim.x) sh_x[i] = ldg16(xbase + 16 * (size_t)i);
-        __syncthreads();
-        xbase = reinterpret_cast<const uint8_t*>(sh_x);
-    }
-    const int nchunk = s.H >> 3;
-    const size_t row_bytes = (size_t)s.H * 2;
+    extern __shared__ int4 sh_dyn[];
+    int32_t* sh_mexp = reinterpret_cast<int32_t*>(sh_dyn);
+    int32_t* sh_mslot = sh_mexp + s.K;
+    int32_t* sh_ekey = sh_mslot + s.K;  // entry's slot if it belongs to this wave, else -1
+    const int nent = T * s.k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();
+    pdl_trigger();
     const int size = L.member_count[wave];
     const int count = L.plan_count[wave];
-    const int nent = T * s.k;
+    for (int i = threadIdx.x; i < size; i += blockDim.x) {
+        sh_mexp[i] = L.member_expert[(size_t)wave * s.K + i];
+        sh_mslot[i] = L.member_slot[(size_t)wave * s.K + i];
+    }
+    for (int i = threadIdx.x; i < nent; i += blockDim.x)
+        sh_ekey[i] = L.entry_wave[i] == wave ? L.entry_slot[i] : -1;
+    const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
+    if (stage_x) {  // the wave's tokens, once per CTA
+        int4* sx = reinterpret_cast<int4*>(sh_ekey + ((nent + 3) & ~3));
+        const int nvec = T * s.H / 8;
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) sx[i] = ldg16(xbase + 16 * (size_t)i);
+        xbase = reinterpret_cast<const uint8_t*>(sx);
+    }
+    __syncthreads();
+
+    const int nchunk = s.H >> 3;
+    const size_t row_bytes = (size_t)s.H * 2;
     const long long miss_rows = (long long)count * s.I;
     const size_t tail_bytes = s.copy_bytes - s.tail_off;
     const long long copies_per = (long long)((tail_bytes + kWarpCopy - 1) / kWarpCopy);
-    const long long copies = (long long)count * copies_per;
-    const long long total = miss_rows + copies + (long long)(size - count) * s.I;
-    const int32_t* mexp = L.member_expert + (size_t)wave * s.K;
-    const int32_t* mslot = L.member_slot + (size_t)wave * s.K;
-    for (long long item = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); item < total;
-         item += (long long)gridDim.x * kWarps) {
-        if (item >= miss_rows && item < miss_rows + copies) {
+    const long long link_items = miss_rows + (long long)count * copies_per;
+    const long long hbm_items = (long long)(size - count) * s.I;
+    const int G = gridDim.x;
+    const int Gl = link_items == 0 ? 0 : hbm_items == 0 ? G : max(1, G / 2);
+    const bool link_cta = (int)blockIdx.x < Gl;
+    const long long first = (long long)(link_cta ? blockIdx.x : blockIdx.x - Gl) * kWarps + warp;
+    const long long stride = (long long)(link_cta ? Gl : G - Gl) * kWarps;
+    const long long total = link_cta ? link_items : hbm_items;
+    for (long long item = first; item < total; item += stride) {
+        if (link_cta && item >= miss_rows) {
             const long long c = item - miss_rows;
             const int q = (int)(c / copies_per);
             const size_t off = s.tail_off + (size_t)(c - (long long)q * copies_per) * kWarpCopy;
-            const uint8_t* src = host + (size_t)mexp[q] * s.stride + off;
-            uint8_t* dst = slots + (size_t)mslot[q] * s.stride + off;
+            const uint8_t* src = host + (size_t)sh_mexp[q] * s.stride + off;
+            uint8_t* dst = slots + (size_t)sh_mslot[q] * s.stride + off;
             const size_t nbytes = min(kWarpCopy, s.copy_bytes - off);
             int4 v[kCopyLoads];
 #pragma unroll
@@ -167,19 +188,11 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
             }
             continue;
         }
-        int q, n;
-        if (item < miss_rows) {
-            q = (int)(item / s.I);
-            n = (int)(item - (long long)q * s.I);
-        } else {
-            const long long r = item - miss_rows - copies;
-            q = count + (int)(r / s.I);
-            n = (int)(r - (long long)(q - count) * s.I);
-        }
-        const bool from_host = q < count;
-        const int slot = mslot[q];
+        const int q = link_cta ? (int)(item / s.I) : count + (int)(item / s.I);
+        const int n = (int)(item % s.I);
+        const int slot = sh_mslot[q];
         uint8_t* slot_row = slots + (size_t)slot * s.stride + s.w13_off;
-        const uint8_t* g = (from_host ? host + (size_t)mexp[q] * s.stride + s.w13_off : slot_row) +
+        const uint8_t* g = (link_cta ? host + (size_t)sh_mexp[q] * s.stride + s.w13_off : slot_row) +
                            (size_t)n * row_bytes;
         const uint8_t* u = g + (size_t)s.I * row_bytes;
         int4 gv[CPL], uv[CPL];
@@ -187,13 +200,13 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
         for (int c = 0; c < CPL; ++c) {
             const int idx = lane + 32 * c;
             if (idx < nchunk) {
-                gv[c] = from_host ? ld_nc_na(g + 16 * (size_t)idx) : ldg16(g + 16 * (size_t)idx);
-                uv[c] = from_host ? ld_nc_na(u + 16 * (size_t)idx) : ldg16(u + 16 * (size_t)idx);
+                gv[c] = link_cta ? ld_nc_na(g + 16 * (size_t)idx) : ldg16(g + 16 * (size_t)idx);
+                uv[c] = link_cta ? ld_nc_na(u + 16 * (size_t)idx) : ldg16(u + 16 * (size_t)idx);
             } else {
                 gv[c] = uv[c] = make_int4(0, 0, 0, 0);
             }
         }
-        if (from_host) {
+        if (link_cta) {
             uint8_t* gd = slot_row + (size_t)n * row_bytes;
             uint8_t* ud = gd + (size_t)s.I * row_bytes;
 #pragma unroll
@@ -207,8 +220,7 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
         }
         for (int b0 = 0; b0 < nent; b0 += 32) {
             const int i = b0 + lane;
-            const bool mine = i < nent && L.entry_wave[i] == wave && L.entry_slot[i] == slot;
-            unsigned mask = __ballot_sync(0xffffffffu, mine);
+            unsigned mask = __ballot_sync(0xffffffffu, i < nent && sh_ekey[i] == slot);
             while (mask) {
                 const int ei = b0 + __ffs(mask) - 1;
                 mask &= mask - 1;
@@ -220,73 +232,94 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
     }
 }
 
-// One warp per (token t, output row m).  For each entry j of t in `wave`:
-// p_j = w_tj * (down_m . h_tj).  fused: out[t, m] = bf16(sum_j p_j) (all
-// entries in this wave); else merged[t*k + j, m] = p_j.
-// CPL = 16-byte chunks of an I-long row per lane; entries go 8 at a time.
+// Down projection of one wave.  A CTA owns token t and kDownRows output
+// rows; warp w handles entries j = w, w + 8, ... of t that belong to the
+// wave.  The warp keeps its entry's h in registers and streams the entry's
+// down rows (all kDownRows loads issued before the dot products), giving
+// p_j[m] = w_tj * (down_m . h_tj) per row.  Then:
+//   fused (all of t's entries are in this wave): out[t, m] = bf16(sum_j p_j[m])
+//     in entry order j = 0..k-1, from shared memory;
+//   else merged[t*k + j, m] = p_j[m] for the wave's entries.
+// CPL = 16-byte chunks of an I-long row per lane.
+constexpr int kDownRows = 8;
+
 template <int CPL>
 __global__ void __launch_bounds__(kThreads) down_bf16_kernel(LayerDev L, Shape s,
                                                             const uint8_t* __restrict__ slots, int wave,
                                                             int T, const float* __restrict__ hbuf,
                                                             float* __restrict__ merged,
                                                             __nv_bfloat16* __restrict__ out, int fused) {
-    constexpr int JB = 8;
-    const int lane = threadIdx.x & 31;
+    __shared__ float sh_p[kMaxTopK][kDownRows];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nchunk = s.I >> 3;
     const size_t row_bytes = (size_t)s.I * 2;
-    const long long total = (long long)T * s.H;
-    for (long long item = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); item < total;
-         item += (long long)gridDim.x * kWarps) {
-        const int t = (int)(item / s.H);
-        const int m = (int)(item - (long long)t * s.H);
-        float acc = 0.f;
-        for (int j0 = 0; j0 < s.k; j0 += JB) {
-            int4 wv[JB][CPL];
-            bool act[JB];
+    const int blocks_per_t = (s.H + kDownRows - 1) / kDownRows;
+    const int t = blockIdx.x / blocks_per_t;
+    const int m0 = (blockIdx.x - t * blocks_per_t) * kDownRows;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= T) return;
+    for (int j = warp; j < s.k; j += kWarps) {
+        const int i = t * s.k + j;
+        if (L.entry_wave[i] != wave) {
+            if (fused && lane < kDownRows) sh_p[j][lane] = 0.f;  // only after a routing error
+            continue;
+        }
+        const int slot = L.entry_slot[i];
+        const float wj = L.topk_w[i];
+        const uint8_t* rows = slots + (size_t)slot * s.stride + s.w2_off + (size_t)m0 * row_bytes;
+        const float* h = hbuf + (size_t)i * s.I;
+        int4 wv[kDownRows][CPL];
 #pragma unroll
-            for (int jj = 0; jj < JB; ++jj) {
-                const int j = j0 + jj;
-                const int i = t * s.k + j;
-                act[jj] = j < s.k && L.entry_wave[i] == wave;
-                if (act[jj]) {
-                    const uint8_t* row = slots + (size_t)L.entry_slot[i] * s.stride + s.w2_off +
-                                         (size_t)m * row_bytes;
+        for (int r = 0; r < kDownRows; ++r) {
 #pragma unroll
-                    for (int c = 0; c < CPL; ++c) {
-                        const int idx = lane + 32 * c;
-                        wv[jj][c] = idx < nchunk ? ldg16(row + 16 * (size_t)idx) : make_int4(0, 0, 0, 0);
-                    }
-                }
-            }
-#pragma unroll
-            for (int jj = 0; jj < JB; ++jj) {
-                if (!act[jj]) continue;
-                const int i = t * s.k + j0 + jj;
-                const float* h = hbuf + (size_t)i * s.I;
-                float d = 0.f;
-#pragma unroll
-                for (int c = 0; c < CPL; ++c) {
-                    const int idx = lane + 32 * c;
-                    if (idx < nchunk) {
-                        const float4 h0 = __ldg(reinterpret_cast<const float4*>(h + 8 * idx));
-                        const float4 h1 = __ldg(reinterpret_cast<const float4*>(h + 8 * idx + 4));
-                        d = dot8_bf16_f32(wv[jj][c], h0, h1, d);
-                    }
-                }
-                d = warp_sum(d);
-                const float p = __fmul_rn(L.topk_w[i], d);
-                if (fused)
-                    acc = __fadd_rn(acc, p);
-                else if (lane == 0)
-                    merged[(size_t)i * s.H + m] = p;
+            for (int c = 0; c < CPL; ++c) {
+                const int idx = lane + 32 * c;
+                wv[r][c] = (m0 + r < s.H && idx < nchunk) ? ldg16(rows + (size_t)r * row_bytes + 16 * (size_t)idx)
+                                                          : make_int4(0, 0, 0, 0);
             }
         }
-        if (fused && lane == 0) out[(size_t)t * s.H + m] = __float2bfloat16_rn(acc);
+        float4 hv[CPL][2];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int idx = lane + 32 * c;
+            if (idx < nchunk) {
+                hv[c][0] = __ldg(reinterpret_cast<const float4*>(h + 8 * idx));
+                hv[c][1] = __ldg(reinterpret_cast<const float4*>(h + 8 * idx + 4));
+            } else {
+                hv[c][0] = hv[c][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kDownRows; ++r) {
+            float d = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                if (lane + 32 * c < nchunk) d = dot8_bf16_f32(wv[r][c], hv[c][0], hv[c][1], d);
+            d = warp_sum(d);
+            const float p = __fmul_rn(wj, d);
+            if (lane == 0) {
+                if (fused)
+                    sh_p[j][r] = p;
+                else if (m0 + r < s.H)
+                    merged[(size_t)i * s.H + m0 + r] = p;
+            }
+        }
+    }
+    if (!fused) return;
+    __syncthreads();
+    if ((int)threadIdx.x < kDownRows && m0 + (int)threadIdx.x < s.H) {
+        const int r = threadIdx.x;
+        float acc = 0.f;
+        for (int j = 0; j < s.k; ++j) acc = __fadd_rn(acc, sh_p[j][r]);
+        out[(size_t)t * s.H + m0 + r] = __float2bfloat16_rn(acc);
     }
 }
 
 __global__ void topk_sum_kernel(const float* __restrict__ merged, __nv_bfloat16* __restrict__ out,
                                 int T, int k, int H) {
+    pdl_wait();
+    pdl_trigger();
     const long long total = (long long)T * H;
     for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total;
          q += (long long)gridDim.x * blockDim.x) {
@@ -311,15 +344,14 @@ cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16
     const int grid = grid_for((long long)T * s.k * s.I, num_sms);
     if (grid <= 0) return cudaSuccess;
     const int cpl = (s.H / 8 + 31) / 32;
-#define PE_GATEUP(C) gateup_bf16_kernel<C><<<grid, kThreads, 0, st>>>(L, s, x, slots_layer, wave, T, hbuf)
+#define PE_GATEUP(C) return launch_pdl(gateup_bf16_kernel<C>, grid, kThreads, 0, st, L, s, x, slots_layer, wave, T, hbuf)
     if (cpl <= 1) PE_GATEUP(1);
-    else if (cpl <= 2) PE_GATEUP(2);
-    else if (cpl <= 4) PE_GATEUP(4);
-    else if (cpl <= 8) PE_GATEUP(8);
-    else if (cpl <= 16) PE_GATEUP(16);
-    else return cudaErrorInvalidValue;
+    if (cpl <= 2) PE_GATEUP(2);
+    if (cpl <= 4) PE_GATEUP(4);
+    if (cpl <= 8) PE_GATEUP(8);
+    if (cpl <= 16) PE_GATEUP(16);
 #undef PE_GATEUP
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gateup_pagein(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
@@ -328,33 +360,34 @@ cudaError_t launch_gateup_pagein(const LayerDev& L, const Shape& s, const __nv_b
     const int grid = num_sms * 2;
     const int cpl = (s.H / 8 + 31) / 32;
     const size_t xbytes = (size_t)T * s.H * 2;
-    const int stage = xbytes <= (size_t)kStageXBytes;
-    const size_t smem = stage ? xbytes : 0;
-#define PE_GUP(C) gateup_pagein_bf16_kernel<C><<<grid, kThreads, smem, st>>>(L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)
+    const size_t meta = (size_t)4 * (2 * s.K + ((T * s.k + 3) & ~3));
+    const int stage = meta + xbytes <= (size_t)kStageXBytes;
+    const size_t smem = meta + (stage ? xbytes : 0);
+#define PE_GUP(C) return launch_pdl(gateup_pagein_bf16_kernel<C>, grid, kThreads, smem, st, L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)
     if (cpl <= 1) PE_GUP(1);
-    else if (cpl <= 2) PE_GUP(2);
-    else if (cpl <= 4) PE_GUP(4);
-    else if (cpl <= 8) PE_GUP(8);
-    else return cudaErrorInvalidValue;
+    if (cpl <= 2) PE_GUP(2);
+    if (cpl <= 4) PE_GUP(4);
+    if (cpl <= 8) PE_GUP(8);
 #undef PE_GUP
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
                         int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
                         int num_sms, cudaStream_t st) {
-    const int grid = grid_for((long long)T * s.H, num_sms);
-    if (grid <= 0) return cudaSuccess;
+    const long long blocks = (long long)T * ((s.H + kDownRows - 1) / kDownRows);
+    if (blocks <= 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const int grid = (int)blocks;
     const int cpl = (s.I / 8 + 31) / 32;
-#define PE_DOWN(C) down_bf16_kernel<C><<<grid, kThreads, 0, st>>>(L, s, slots_layer, wave, T, hbuf, merged, out, fused)
+#define PE_DOWN(C) return launch_pdl(down_bf16_kernel<C>, grid, kThreads, 0, st, L, s, slots_layer, wave, T, hbuf, merged, out, fused)
     if (cpl <= 1) PE_DOWN(1);
-    else if (cpl <= 2) PE_DOWN(2);
-    else if (cpl <= 3) PE_DOWN(3);
-    else if (cpl <= 4) PE_DOWN(4);
-    else if (cpl <= 8) PE_DOWN(8);
-    else return cudaErrorInvalidValue;
+    if (cpl <= 2) PE_DOWN(2);
+    if (cpl <= 3) PE_DOWN(3);
+    if (cpl <= 4) PE_DOWN(4);
+    if (cpl <= 8) PE_DOWN(8);
 #undef PE_DOWN
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
@@ -362,8 +395,7 @@ cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* 
     const long long total = (long long)T * s.H;
     const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     if (grid <= 0) return cudaSuccess;
-    topk_sum_kernel<<<grid, 256, 0, st>>>(merged, out, T, s.k, s.H);
-    return cudaGetLastError();
+    return launch_pdl(topk_sum_kernel, grid, 256, 0, st, merged, out, T, s.k, s.H);
 }
 
 }  // namespace pe

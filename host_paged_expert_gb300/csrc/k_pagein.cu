@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(kCopyThreads) pagein_kernel(
     const uint8_t* __restrict__ host_layer, uint8_t* __restrict__ slots_layer, size_t stride,
     size_t copy_bytes, const int32_t* __restrict__ plan_expert, const int32_t* __restrict__ plan_slot,
     const int32_t* __restrict__ plan_count, int max_count) {
+    pdl_wait();
+    pdl_trigger();
     const int count = min(*plan_count, max_count);
     const size_t nchunk = (copy_bytes + kChunk - 1) / kChunk;
     const size_t items = (size_t)count * nchunk;
@@ -77,11 +79,10 @@ cudaError_t launch_pagein(const LayerDev& L, const Shape& s, const uint8_t* host
     const size_t want = (size_t)max_count * nchunk;
     const int grid = (int)min(want, (size_t)num_sms * 4);
     if (grid <= 0) return cudaSuccess;
-    pagein_kernel<<<grid, kCopyThreads, 0, st>>>(host_layer, slots_layer, s.stride, s.copy_bytes,
-                                                 L.plan_expert + (size_t)wave * s.K,
-                                                 L.plan_slot + (size_t)wave * s.K,
-                                                 L.plan_count + wave, max_count);
-    return cudaGetLastError();
+    return launch_pdl(pagein_kernel, grid, kCopyThreads, 0, st, host_layer, slots_layer, s.stride, s.copy_bytes,
+                      (const int32_t*)(L.plan_expert + (size_t)wave * s.K),
+                      (const int32_t*)(L.plan_slot + (size_t)wave * s.K), (const int32_t*)(L.plan_count + wave),
+                      max_count);
 }
 
 cudaError_t launch_copy(const void* src, void* dst, size_t bytes, int num_sms, cudaStream_t st) {

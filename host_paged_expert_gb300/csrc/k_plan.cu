@@ -14,9 +14,15 @@
 //   slots whose expert is outside the wave, by (tick, slot) ascending; the
 //   missing members in ascending id take the victims in that order and get
 //   tick = clock.
+//
+// The planner is one CTA and sits on the critical path of every decode
+// step, so it is written for latency: all of its global loads are issued
+// up front, routing works on logits held in registers, and everything after
+// routing runs in shared memory until the final stores.
 
 #include <math.h>
 
+#include "pe_device.cuh"
 #include "pe_internal.h"
 
 namespace pe {
@@ -29,27 +35,35 @@ __device__ __forceinline__ bool ranks_before(float v, int id, float bv, int bid)
 
 // One warp routes one token: top-k ids in selection order and the softmax
 // over the chosen logits (equal to the E-wide softmax renormalised on them).
-__device__ void route_token_warp(const float* __restrict__ row, int E, int k, int32_t* ids,
-                                 float* ws, uint32_t* err) {
+// EPL = logits per lane (ceil(E / 32)), held in registers.  Lane j < k
+// returns pick j in (id, w); other lanes return id = -1.
+template <int EPL>
+__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int& out_id,
+                                                 float& out_w, bool& nan_seen) {
     const int lane = threadIdx.x & 31;
-    float prev_v = 0.f;
-    int prev_id = -1;
-    float my_v = -INFINITY;
-    int my_id = 0;
-    bool nan_seen = false;
+    float v[EPL];
+#pragma unroll
+    for (int q = 0; q < EPL; ++q) {
+        const int e = lane + 32 * q;
+        float x = e < E ? row[e] : -INFINITY;
+        if (isnan(x)) {
+            x = -INFINITY;
+            nan_seen = true;
+        }
+        v[q] = x;
+    }
+    float prev_v = 0.f, my_v = -INFINITY;
+    int prev_id = -1, my_id = -1;
     for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
         int bid = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            float v = row[e];
-            if (isnan(v)) {
-                v = -INFINITY;
-                nan_seen = true;
-            }
-            // only candidates strictly after the previous pick qualify
-            const bool after = (j == 0) || ranks_before(prev_v, prev_id, v, e);
-            if (after && ranks_before(v, e, bv, bid)) {
-                bv = v;
+#pragma unroll
+        for (int q = 0; q < EPL; ++q) {
+            const int e = lane + 32 * q;
+            // only experts that exist and come strictly after the previous pick
+            const bool ok = e < E && (j == 0 || ranks_before(prev_v, prev_id, v[q], e));
+            if (ok && ranks_before(v[q], e, bv, bid)) {
+                bv = v[q];
                 bid = e;
             }
         }
@@ -75,48 +89,32 @@ __device__ void route_token_warp(const float* __restrict__ row, int E, int k, in
     float sum = ex;
 #pragma unroll
     for (int o = 16; o; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
+    out_id = lane < k ? my_id : -1;
+    out_w = lane < k ? __fdiv_rn(ex, sum) : 0.f;
+}
+
+template <int EPL>
+__global__ void __launch_bounds__(256) route_kernel(LayerDev L, int E, int k, const float* logits,
+                                                    int T, uint32_t* err) {
+    pdl_wait();
+    pdl_trigger();
+    const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int id;
+    float w;
+    bool nan_seen = false;
+    route_token_warp<EPL>(logits + (size_t)t * E, E, k, id, w, nan_seen);
+    const int lane = threadIdx.x & 31;
     if (lane < k) {
-        ids[lane] = my_id;
-        ws[lane] = __fdiv_rn(ex, sum);
+        L.topk_id[(size_t)t * k + lane] = id;
+        L.topk_w[(size_t)t * k + lane] = w;
     }
     if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, PE_DEVERR_NAN_LOGIT);
 }
 
-__global__ void __launch_bounds__(256) route_kernel(LayerDev L, int E, int k, const float* logits,
-                                                    int T, uint32_t* err) {
-    const int warp = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (warp >= T) return;
-    route_token_warp(logits + (size_t)warp * E, E, k, L.topk_id + (size_t)warp * k,
-                     L.topk_w + (size_t)warp * k, err);
-}
-
-// Exclusive block-wide prefix count of a per-thread flag; every thread of the
-// block calls it.  warp_tot needs 32 ints.
-__device__ __forceinline__ int block_prefix(bool flag, int* warp_tot, int* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const unsigned b = __ballot_sync(0xffffffffu, flag);
-    const int in_warp = __popc(b & ((1u << lane) - 1u));
-    if (lane == 0) warp_tot[warp] = __popc(b);
-    __syncthreads();
-    if (warp == 0) {
-        const int v = lane < nwarps ? warp_tot[lane] : 0;
-        int incl = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        if (lane < nwarps) warp_tot[lane] = incl - v;
-        if (lane == 31) *total = incl;
-    }
-    __syncthreads();
-    const int r = warp_tot[warp] + in_warp;
-    __syncthreads();
-    return r;
-}
-
 // One CTA plans every wave of a step.  blockDim.x is a multiple of 32 and at
 // least E (thread e owns expert e in the scans) and K (thread s owns slot s).
+template <int EPL>
 __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape s,
                                                                const float* logits, int T,
                                                                int route_inline, uint32_t* err) {
@@ -129,21 +127,27 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
     __shared__ int32_t sh_ids[kMaxExperts];  // routed ids of an inline-routed step (T*k <= 1024)
     __shared__ uint8_t sh_used[kMaxExperts];
     __shared__ uint8_t sh_inwave[kMaxExperts];
-    __shared__ int sh_warp[32];
-    __shared__ int sh_nR, sh_nM, sh_cold, sh_bad;
+    __shared__ uint8_t sh_loaded[kMaxExperts];
+    __shared__ unsigned long long sh_vkey[kMaxSlots];  // (tick, slot) of victim slots, ~0 otherwise
+    __shared__ int sh_wr[32], sh_wm[32];
+    __shared__ int sh_nR, sh_nM, sh_cold, sh_bad, sh_nan;
 
     const int tid = threadIdx.x, nthr = blockDim.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int E = s.E, K = s.K, k = s.k;
     const int nent = T * k;
     const bool ids_in_smem = route_inline && nent <= kMaxExperts;
 
-    // state loads first: they do not depend on routing
+    pdl_wait();
+    pdl_trigger();
+    // every global load of the planner is issued here, before routing
     for (int i = tid; i < K; i += nthr) {
         sh_slot_expert[i] = L.slot_expert[i];
         sh_tick[i] = L.slot_tick[i];
     }
     for (int e = tid; e < E; e += nthr) {
         sh_expert_slot[e] = L.expert_slot[e];
+        sh_loaded[e] = L.loaded[e];
         sh_used[e] = 0;
         sh_inwave[e] = 0;
         sh_wave_of[e] = -1;
@@ -152,16 +156,24 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
     if (tid == 0) {
         sh_cold = 0;
         sh_bad = 0;
+        sh_nan = 0;
     }
     uint32_t clock = *L.clock;
     if (route_inline) {
-        for (int t = tid >> 5; t < T; t += nthr >> 5) {
-            route_token_warp(logits + (size_t)t * E, E, k, L.topk_id + (size_t)t * k,
-                             L.topk_w + (size_t)t * k, err);
-            if (ids_in_smem && (tid & 31) < k) sh_ids[t * k + (tid & 31)] = L.topk_id[(size_t)t * k + (tid & 31)];
+        for (int t = warp; t < T; t += nwarps) {
+            int id;
+            float w;
+            bool nan_seen = false;
+            route_token_warp<EPL>(logits + (size_t)t * E, E, k, id, w, nan_seen);
+            if (lane < k) {
+                L.topk_id[(size_t)t * k + lane] = id;
+                L.topk_w[(size_t)t * k + lane] = w;
+                if (ids_in_smem) sh_ids[t * k + lane] = id;
+            }
+            if (nan_seen) sh_nan = 1;
         }
     }
-    __syncthreads();  // publishes the routing (shared and global) to the block
+    __syncthreads();  // routing, state and flags are in shared memory from here on
 
     for (int i = tid; i < nent; i += nthr) {
         const int e = ids_in_smem ? sh_ids[i] : L.topk_id[i];
@@ -172,16 +184,42 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
     }
     __syncthreads();
 
-    // order = R ++ M, both ascending id
+    // order = R ++ M, both ascending id (one scan for both lists)
     const int e = tid;
     const bool used = e < E && sh_used[e];
     const bool isR = used && sh_expert_slot[e] >= 0;
     const bool isM = used && sh_expert_slot[e] < 0;
-    const int posR = block_prefix(isR, sh_warp, &sh_nR);
-    const int posM = block_prefix(isM, sh_warp, &sh_nM);
+    const unsigned bR = __ballot_sync(0xffffffffu, isR), bM = __ballot_sync(0xffffffffu, isM);
+    const unsigned below = (1u << lane) - 1u;
+    if (lane == 0) {
+        sh_wr[warp] = __popc(bR);
+        sh_wm[warp] = __popc(bM);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int vr = lane < nwarps ? sh_wr[lane] : 0, vm = lane < nwarps ? sh_wm[lane] : 0;
+        int ir = vr, im = vm;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int nr = __shfl_up_sync(0xffffffffu, ir, o), nm = __shfl_up_sync(0xffffffffu, im, o);
+            if (lane >= o) {
+                ir += nr;
+                im += nm;
+            }
+        }
+        if (lane < nwarps) {
+            sh_wr[lane] = ir - vr;
+            sh_wm[lane] = im - vm;
+        }
+        if (lane == 31) {
+            sh_nR = ir;
+            sh_nM = im;
+        }
+    }
+    __syncthreads();
     const int nR = sh_nR, nM = sh_nM;
-    if (isR) sh_order[posR] = e;
-    if (isM) sh_order[nR + posM] = e;
+    if (isR) sh_order[sh_wr[warp] + __popc(bR & below)] = e;
+    if (isM) sh_order[nR + sh_wm[warp] + __popc(bM & below)] = e;
     __syncthreads();
 
     const int nD = nR + nM;
@@ -210,21 +248,19 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
         }
         __syncthreads();
         // rank of each victim slot in (tick, slot) order
-        int my_rank = -1;
+        unsigned long long my_key = ~0ull;
         if (tid < K) {
             const int ex = sh_slot_expert[tid];
-            if (ex < 0 || !sh_inwave[ex]) {
-                const unsigned long long key = ((unsigned long long)sh_tick[tid] << 32) | (unsigned)tid;
-                int r = 0;
-                for (int o = 0; o < K; ++o) {
-                    const int ox = sh_slot_expert[o];
-                    if (ox < 0 || !sh_inwave[ox]) {
-                        const unsigned long long ok = ((unsigned long long)sh_tick[o] << 32) | (unsigned)o;
-                        r += ok < key;
-                    }
-                }
-                my_rank = r;
-            }
+            if (ex < 0 || !sh_inwave[ex]) my_key = ((unsigned long long)sh_tick[tid] << 32) | (unsigned)tid;
+            sh_vkey[tid] = my_key;
+        }
+        __syncthreads();
+        int my_rank = -1;
+        if (tid < K && my_key != ~0ull && nmiss > 0) {
+            int r = 0;
+#pragma unroll 8
+            for (int o = 0; o < K; ++o) r += sh_vkey[o] < my_key;
+            my_rank = r;
         }
         __syncthreads();
         if (my_rank >= 0 && my_rank < nmiss) {
@@ -243,7 +279,7 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
             L.plan_slot[q] = slot;
             L.member_expert[q] = m;
             L.member_slot[q] = slot;
-            if (!L.loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
+            if (!sh_loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
         }
         __syncthreads();
         for (int i = tid; i < size; i += nthr) {
@@ -286,7 +322,13 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
         atomicAdd(&L.counters[C_PAGE_INS], (unsigned long long)total_miss);
         atomicAdd(&L.counters[C_COLD], (unsigned long long)sh_cold);
         if (sh_bad) atomicOr(err, PE_DEVERR_PLAN);
+        if (sh_nan) atomicOr(err, PE_DEVERR_NAN_LOGIT);
     }
+}
+
+inline int epl_for(int E) {
+    const int epl = (E + 31) / 32;
+    return epl <= 1 ? 1 : epl <= 2 ? 2 : epl <= 4 ? 4 : epl <= 8 ? 8 : epl <= 16 ? 16 : 32;
 }
 
 }  // namespace
@@ -294,7 +336,12 @@ __global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape
 cudaError_t launch_route(const LayerDev& L, const Shape& s, const float* logits, int T,
                          uint32_t* err, cudaStream_t st) {
     const int warps = 8;
-    route_kernel<<<(T + warps - 1) / warps, warps * 32, 0, st>>>(L, s.E, s.k, logits, T, err);
+    const int grid = (T + warps - 1) / warps;
+    switch (epl_for(s.E)) {
+#define PE_ROUTE(N) case N: return launch_pdl(route_kernel<N>, grid, warps * 32, 0, st, L, s.E, s.k, logits, T, err);
+        PE_ROUTE(1) PE_ROUTE(2) PE_ROUTE(4) PE_ROUTE(8) PE_ROUTE(16) PE_ROUTE(32)
+#undef PE_ROUTE
+    }
     return cudaGetLastError();
 }
 
@@ -304,7 +351,11 @@ cudaError_t launch_plan(const LayerDev& L, const Shape& s, const float* logits, 
     if (route_inline && threads < 32 * T) threads = 32 * T;  // one warp per token
     threads = (threads + 31) / 32 * 32;
     if (threads > kPlanMaxThreads) threads = kPlanMaxThreads;
-    plan_kernel<<<1, threads, 0, st>>>(L, s, logits, T, route_inline, err);
+    switch (epl_for(s.E)) {
+#define PE_PLAN(N) case N: return launch_pdl(plan_kernel<N>, 1, threads, 0, st, L, s, logits, T, route_inline, err);
+        PE_PLAN(1) PE_PLAN(2) PE_PLAN(4) PE_PLAN(8) PE_PLAN(16) PE_PLAN(32)
+#undef PE_PLAN
+    }
     return cudaGetLastError();
 }
 
