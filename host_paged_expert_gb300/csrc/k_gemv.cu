@@ -27,53 +27,6 @@ constexpr int kCopyLoads = 8;                               // 16-byte loads per
 constexpr size_t kWarpCopy = (size_t)32 * 16 * kCopyLoads;  // 4 KiB per copy item
 constexpr int kStageXBytes = 48 * 1024;                     // dynamic shared memory budget of the fused kernel
 
-// acc += sum of the 8 bf16 products of w and x, in element order.
-__device__ __forceinline__ float dot8_bf16(int4 w, int4 x, float acc) {
-    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
-    const uint32_t xv[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(xv[q] << 16), acc);
-        acc = fmaf(__uint_as_float(wv[q] & 0xffff0000u), __uint_as_float(xv[q] & 0xffff0000u), acc);
-    }
-    return acc;
-}
-
-// acc += sum of the 8 products of bf16 weights and fp32 activations h[0..7].
-__device__ __forceinline__ float dot8_bf16_f32(int4 w, float4 h0, float4 h1, float acc) {
-    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
-    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc = fmaf(__uint_as_float(wv[q] << 16), hv[2 * q], acc);
-        acc = fmaf(__uint_as_float(wv[q] & 0xffff0000u), hv[2 * q + 1], acc);
-    }
-    return acc;
-}
-
-__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.f, expf(-g))); }
-
-// h = SiLU(gate . x) * (up . x) for one gate/up row pair held by the warp
-// (chunk c of lane l covers elements 8*(l + 32c) .. +7).  Every path that
-// computes an h value goes through this function, so h does not depend on
-// where the weights were read from.
-// xr is a generic pointer to the token's bf16 row (shared or global memory).
-template <int CPL>
-__device__ __forceinline__ float row_pair_h(const int4 (&gv)[CPL], const int4 (&uv)[CPL], const uint8_t* xr,
-                                            int lane, int nchunk) {
-    float ag = 0.f, au = 0.f;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-        const int idx = lane + 32 * c;
-        const int4 xv = idx < nchunk ? *reinterpret_cast<const int4*>(xr + 16 * (size_t)idx) : make_int4(0, 0, 0, 0);
-        ag = dot8_bf16(gv[c], xv, ag);
-        au = dot8_bf16(uv[c], xv, au);
-    }
-    ag = warp_sum(ag);
-    au = warp_sum(au);
-    return __fmul_rn(silu(ag), au);
-}
-
 // h[i, n] = SiLU(gate_n . x_t) * (up_n . x_t) for entries i of `wave`.
 // CPL = 16-byte chunks of an H-long row per lane.
 template <int CPL>
@@ -124,7 +77,8 @@ __global__ void __launch_bounds__(kThreads) gateup_bf16_kernel(LayerDev L, Shape
 // every entry of the wave routed to that member.
 //
 // Dynamic shared memory: [member experts K][member slots K][entry keys nent]
-// then, when it fits, the wave's token rows of x.
+// padded to a multiple of 4 ints, then, when it fits, the wave's token rows
+// of x (16-byte aligned).
 template <int CPL>
 __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
     LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ host,
@@ -147,7 +101,8 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_pagein_bf16_kernel(
         sh_ekey[i] = L.entry_wave[i] == wave ? L.entry_slot[i] : -1;
     const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
     if (stage_x) {  // the wave's tokens, once per CTA
-        int4* sx = reinterpret_cast<int4*>(sh_ekey + ((nent + 3) & ~3));
+        // 16-byte aligned: the metadata block is padded to a multiple of 4 ints
+        int4* sx = reinterpret_cast<int4*>(sh_mexp + ((2 * s.K + nent + 3) & ~3));
         const int nvec = T * s.H / 8;
         for (int i = threadIdx.x; i < nvec; i += blockDim.x) sx[i] = ldg16(xbase + 16 * (size_t)i);
         xbase = reinterpret_cast<const uint8_t*>(sx);
@@ -360,7 +315,7 @@ cudaError_t launch_gateup_pagein(const LayerDev& L, const Shape& s, const __nv_b
     const int grid = num_sms * 2;
     const int cpl = (s.H / 8 + 31) / 32;
     const size_t xbytes = (size_t)T * s.H * 2;
-    const size_t meta = (size_t)4 * (2 * s.K + ((T * s.k + 3) & ~3));
+    const size_t meta = (size_t)4 * ((2 * s.K + T * s.k + 3) & ~3);  // same padding as the kernel
     const int stage = meta + xbytes <= (size_t)kStageXBytes;
     const size_t smem = meta + (stage ? xbytes : 0);
 #define PE_GUP(C) return launch_pdl(gateup_pagein_bf16_kernel<C>, grid, kThreads, smem, st, L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)

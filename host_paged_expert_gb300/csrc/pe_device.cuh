@@ -24,6 +24,53 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+// acc += sum of the 8 bf16 products of w and x, in element order.
+__device__ __forceinline__ float dot8_bf16(int4 w, int4 x, float acc) {
+    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+    const uint32_t xv[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(xv[q] << 16), acc);
+        acc = fmaf(__uint_as_float(wv[q] & 0xffff0000u), __uint_as_float(xv[q] & 0xffff0000u), acc);
+    }
+    return acc;
+}
+
+// acc += sum of the 8 products of bf16 weights and fp32 activations h[0..7].
+__device__ __forceinline__ float dot8_bf16_f32(int4 w, float4 h0, float4 h1, float acc) {
+    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+    const float hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        acc = fmaf(__uint_as_float(wv[q] << 16), hv[2 * q], acc);
+        acc = fmaf(__uint_as_float(wv[q] & 0xffff0000u), hv[2 * q + 1], acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdiv_rn(g, __fadd_rn(1.f, expf(-g))); }
+
+// h = SiLU(gate . x) * (up . x) for one gate/up row pair held by the warp
+// (chunk c of lane l covers elements 8*(l + 32c) .. +7).  Every path that
+// computes an h value goes through this function, so h does not depend on
+// where the weights were read from.
+// xr is a generic pointer to the token's bf16 row (shared or global memory).
+template <int CPL>
+__device__ __forceinline__ float row_pair_h(const int4 (&gv)[CPL], const int4 (&uv)[CPL], const uint8_t* xr,
+                                            int lane, int nchunk) {
+    float ag = 0.f, au = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        const int4 xv = idx < nchunk ? *reinterpret_cast<const int4*>(xr + 16 * (size_t)idx) : make_int4(0, 0, 0, 0);
+        ag = dot8_bf16(gv[c], xv, ag);
+        au = dot8_bf16(uv[c], xv, au);
+    }
+    ag = warp_sum(ag);
+    au = warp_sum(au);
+    return __fmul_rn(silu(ag), au);
+}
+
 }  // namespace pe
 
 namespace pe {

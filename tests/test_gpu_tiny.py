@@ -237,3 +237,28 @@ def test_graph_captured_decode_matches_eager(tiny):
     assert graphed.stats(0)["page_ins"] == eager.stats(0)["page_ins"]
     eager.close()
     graphed.close()
+
+
+@pytest.mark.parametrize("E,k,K", [(1, 1, 1), (8, 1, 3), (8, 2, 5), (9, 3, 7), (16, 2, 16)])
+def test_odd_slot_and_entry_counts(E, k, K):
+    """Slot and entry counts that make the fused kernel's shared-memory
+    metadata block an odd number of ints; outputs still match the oracle and
+    the K = E call."""
+    _lib = _need_gpu()
+    s = synth.MoEShape(1, E, k, K, 256, 128, "bf16")
+    w = synth.ExpertWeights(s, seed=E + 10 * K)
+    a = _lib.PagedMoE(s, max_tokens=7)
+    gu.load_stack(a, w)
+    b = _lib.PagedMoE(s.with_slots(E), max_tokens=7, store_owner=a)
+    o = omlp.PagedLayer(E, K, k, gu.expert_fn(w, 0))
+    for T in (1, 3, 5, 7):
+        xb = synth.hidden_states((T,), s.hidden, seed=T, tag=E)
+        lg = synth.prefill_logits(1, E, T, seed=T + K)[0]
+        x, l = gu.to_dev_bf16(xb), gu.to_dev_f32(lg)
+        ya, yb = a.forward(0, x, l), b.forward(0, x, l)
+        out, _, plan, ids, wts = o.step(xb, lg)
+        gu.check_plan(a.read_plan(0, T), plan, ids, wts)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb))
+        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
+    b.close()
+    a.close()
