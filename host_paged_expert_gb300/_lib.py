@@ -27,7 +27,7 @@ EXPORTS = [
     "pe_required_device_bytes", "pe_get_row_layout", "pe_max_waves", "pe_create", "pe_create_shared",
     "pe_load_host_expert", "pe_host_row", "pe_forward", "pe_stats", "pe_read_plan", "pe_read_residency",
     "pe_read_slot", "pe_reset_residency", "pe_probe_host_link", "pe_profile_enable", "pe_profile_read",
-    "pe_destroy", "pe_last_error",
+    "pe_destroy", "pe_last_error", "pe_expert_mlp_noalloc",
 ]
 
 
@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
     L.pe_profile_read.argtypes = [c_void_p, POINTER(PEProfile)]
     L.pe_destroy.argtypes = [c_void_p]
     L.pe_destroy.restype = None
+    L.pe_expert_mlp_noalloc.argtypes = [c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32,
+                                         c_void_p]
     L.pe_last_error.argtypes = [c_void_p]
     L.pe_last_error.restype = ctypes.c_char_p
     for name in EXPORTS:

@@ -86,6 +86,10 @@ const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "gateup_pa
 
 }  // namespace
 
+namespace pe {
+void set_thread_error(const char* msg) { g_create_error = msg ? msg : ""; }
+}  // namespace pe
+
 struct pe_handle {
     pe_config cfg;
     pe_row_layout row;

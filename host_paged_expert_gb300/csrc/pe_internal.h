@@ -48,6 +48,9 @@ struct Shape {
     size_t tail_off;     // start of everything after w13 (scales, w2): copied as one block
 };
 
+// Records the message pe_last_error(NULL) returns in this thread.
+void set_thread_error(const char* msg);
+
 // ---- launchers (each returns the launch status) ----
 
 // Routing of T tokens by one warp per token into topk_id / topk_w.

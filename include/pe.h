@@ -226,11 +226,38 @@ pe_status pe_probe_host_link(pe_handle* h, void* dev_dst, size_t bytes, int32_t 
 pe_status pe_profile_enable(pe_handle* h, int32_t on);
 pe_status pe_profile_read(pe_handle* h, pe_profile_t* out);
 
+/* Scratch held by pe_expert_mlp_noalloc in every GPU that loads libpe. */
+#define PE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* One bf16 expert's SiLU-gated MLP that allocates nothing, for callers that
+ * cannot allocate device memory where they need it (for example code that
+ * may only use the buffers a framework hands it, or a path that must not
+ * synchronise the device by calling cudaMalloc).  The pages describe no such
+ * call; it has no counterpart there.
+ *   out[t] = w2 . (SiLU(w13[0:I] . x[t]) * (w13[I:2I] . x[t]))  for t < num_tokens
+ *   w13: device, bf16 [2I, H] (gate rows, then up rows); w2: device, bf16 [H, I];
+ *   x, out: device, bf16 [num_tokens, H]; all 16-byte aligned; out may not
+ *   alias x.  H <= 2048 and I <= 1024, both multiples of 8.
+ * The intermediate h (num_tokens * I fp32) lives in a static device array of
+ * PE_NOALLOC_SCRATCH_BYTES; larger requests return PE_ERR_RANGE before any
+ * launch.  The result equals pe_forward on a one-expert layer (E = K =
+ * top_k = 1) with the same weights, bit for bit.
+ * The first call on a device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  Every
+ * call shares the one array per device: calls whose kernels overlap on the
+ * GPU (other streams, other host threads) race on it; order them on one
+ * stream.  Asynchronous on `stream`; no host synchronisation.
+ * Errors: PE_ERR_INVALID (NULL, misaligned, bad sizes), PE_ERR_RANGE (above
+ *   the limits), PE_ERR_CUDA; the message is in pe_last_error(NULL). */
+pe_status pe_expert_mlp_noalloc(const void* w13, const void* w2, const void* x, void* out,
+                                int32_t num_tokens, int32_t hidden, int32_t intermediate, void* stream);
+
 /* Frees the host store (if owned) and the handle; never the arena. */
 void pe_destroy(pe_handle* h);
 
 /* Message of the handle's last error ("" if none); pe_last_error(NULL)
- * returns the last error of a failed pe_create in this thread. */
+ * returns the last error of a failed pe_create, or of a failed call that
+ * takes no handle, in this thread. */
 const char* pe_last_error(pe_handle* h);
 
 #ifdef __cplusplus
