@@ -12,7 +12,9 @@ Readings where the pages are silent:
     largest logits are the k largest probabilities); entries are ordered by
     descending logit and equal logits go to the lower expert id first;
   * a NaN logit is treated as -inf for selection and reported through the
-    returned flag.
+    returned flag;
+  * a token whose logits are all NaN (all -inf) gets equal weights 1/k on the
+    experts chosen by the tie rule (ids 0..k-1): the softmax is undefined there.
 """
 
 from __future__ import annotations
@@ -53,7 +55,8 @@ def route(logits: np.ndarray, top_k: int) -> tuple[np.ndarray, np.ndarray, bool]
         # primary key: descending logit; secondary: ascending id
         order = np.lexsort((expert, -sel[t]))
         ids[t] = order[:top_k]
-    p = softmax(sel)
+    dead = np.all(np.isneginf(sel), axis=1)
+    p = softmax(np.where(dead[:, None], 0.0, sel))
     kept = np.take_along_axis(p, ids.astype(np.int64), axis=1)
     weights = kept / np.sum(kept, axis=1, keepdims=True)
     return ids, weights, had_nan

@@ -90,7 +90,11 @@ def check_route_nan(route):
     ids, w, nan = route(logits, 2)
     assert nan
     assert ids.tolist() == [[2, 0]]
-    assert np.isfinite(w).all()
+    assert np.allclose(w[0], scipy.special.softmax([2.0, 0.5]), rtol=1e-12)
+    # every logit NaN: tie rule picks ids 0..k-1 with equal weights
+    ids, w, nan = route(np.full((1, 5), np.nan, np.float32), 3)
+    assert nan and ids.tolist() == [[0, 1, 2]]
+    assert np.all(w == 1.0 / 3.0)
 
 
 # ---------------------------------------------------------------- fp8
