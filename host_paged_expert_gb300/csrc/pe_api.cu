@@ -419,7 +419,6 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
         reinterpret_cast<uintptr_t>(router_logits) % 4)
         return fail(h, PE_ERR_INVALID, "hidden/out must be 16-byte aligned, logits 4-byte aligned");
     if (hidden == out) return fail(h, PE_ERR_INVALID, "out may not alias hidden");
-    if (c.dtype != PE_BF16) return fail(h, PE_ERR_UNSUPPORTED_DTYPE, "block-FP8 forward is not available in this build");
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int T = num_tokens;
@@ -448,10 +447,12 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // decode sizes page in inside the gate/up kernel; the choice depends on T
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
+    const bool fp8 = c.dtype == PE_FP8_BLOCK128;
     for (int w = 0; w < s.Wmax; ++w) {
         if (pagein_fused) {
             ProfScope p(h, P_GATEUP_PAGEIN, st);
-            e = launch_gateup_pagein(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st);
+            e = fp8 ? launch_gateup_pagein_fp8(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                    : launch_gateup_pagein(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st);
             if (e) return cuda_fail(h, e, "gate/up + page-in kernel");
         } else {
             {
@@ -461,13 +462,15 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             }
             {
                 ProfScope p(h, P_GATEUP, st);
-                e = launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
+                e = fp8 ? launch_gateup_fp8(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                        : launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
                 if (e) return cuda_fail(h, e, "gate/up kernel");
             }
         }
         {
             ProfScope p(h, P_DOWN, st);
-            e = launch_down(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st);
+            e = fp8 ? launch_down_fp8(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
+                    : launch_down(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st);
             if (e) return cuda_fail(h, e, "down kernel");
         }
     }

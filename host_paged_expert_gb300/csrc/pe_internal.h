@@ -82,6 +82,16 @@ cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16
 cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
                         int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
                         int num_sms, cudaStream_t st);
+// Block-FP8 counterparts of the three decode kernels above.
+cudaError_t launch_gateup_pagein_fp8(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                     const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
+                                     float* hbuf, int num_sms, cudaStream_t st);
+cudaError_t launch_gateup_fp8(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                              const uint8_t* slots_layer, int wave, int T, float* hbuf, int num_sms,
+                              cudaStream_t st);
+cudaError_t launch_down_fp8(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
+                            int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
+                            int num_sms, cudaStream_t st);
 // out[t] = sum_j merged[t, j] in entry order, rounded to bf16.
 cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
                             cudaStream_t st);
