@@ -9,8 +9,11 @@
 // stream whose sizes depend only on shapes, which keeps it capturable in a
 // CUDA graph ("Captured decode").
 
+#include <cudaTypedefs.h>
+
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -61,6 +64,31 @@ void row_layout(const pe_config& c, pe_row_layout* r) {
     r->row_stride = align_up(r->s2_offset + r->s2_bytes, 256);
 }
 
+Shape make_shape(const pe_config& c, const pe_row_layout& r) {
+    Shape s;
+    s.E = c.num_experts;
+    s.k = c.top_k;
+    s.K = c.num_slots;
+    s.H = c.hidden;
+    s.I = c.intermediate;
+    s.Wmax = 1;
+    s.dtype = c.dtype;
+    s.stride = r.row_stride;
+    s.copy_bytes = align_up(r.s2_offset + r.s2_bytes, 16);
+    s.w13_off = r.w13_offset;
+    s.s13_off = r.s13_offset;
+    s.w2_off = r.w2_offset;
+    s.s2_off = r.s2_offset;
+    s.tail_off = r.s13_offset;
+    return s;
+}
+
+// The tensor-core prefill path serves calls with more than kFusedMaxEntries
+// entries when the shapes tile evenly.
+bool tc_enabled(const pe_config& c, const pe_row_layout& r) {
+    return (long long)c.max_tokens * c.top_k > kFusedMaxEntries && prefill_tc_supported(make_shape(c, r));
+}
+
 int32_t max_waves(const pe_config& c, int32_t T) {
     const long long ent = (long long)T * c.top_k;
     if (ent <= c.num_slots) return 1;
@@ -81,8 +109,9 @@ struct Carver {
     }
 };
 
-enum ProfKind { P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_NUM };
-const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "gateup_pagein", "down", "topk_sum"};
+enum ProfKind { P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_GEMM, P_NUM };
+const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "gateup_pagein", "down", "topk_sum",
+                                 "prefill_gemm"};
 
 }  // namespace
 
@@ -105,6 +134,9 @@ struct pe_handle {
     uint32_t* err = nullptr;
     float* hbuf = nullptr;
     float* merged = nullptr;
+    bool tc_ok = false;      // tensor-core prefill path available
+    PrefillDev pre = {};
+    PrefillMaps maps;
     int num_sms = 0;
     std::string last_error;
     // per-kernel timing
@@ -141,6 +173,18 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
     uint32_t* err = cv.take<uint32_t>(1);
     float* hbuf = cv.take<float>(maxTk * c.intermediate);
     float* merged = cv.take<float>(maxTk * c.hidden);
+    PrefillDev pre = {};
+    const bool tc = tc_enabled(c, r);
+    if (tc) {
+        const size_t rows = prefill_max_rows((int)maxTk, K);
+        pre.x_perm = cv.take<__nv_bfloat16>(rows * c.hidden);
+        pre.h_perm = cv.take<__nv_bfloat16>(rows * c.intermediate);
+        pre.perm = cv.take<int32_t>(rows);
+        pre.tiles = cv.take<int4>(rows / 128);
+        pre.counts = cv.take<int32_t>(4);
+        pre.max_rows = (int)rows;
+        pre.max_tiles = (int)(rows / 128);
+    }
     std::vector<LayerDev> layers(L);
     for (int l = 0; l < L; ++l) {
         LayerDev& d = layers[l];
@@ -171,6 +215,8 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         h->layers = layers;
         h->Wmax = W;
         h->maxTk = (int)maxTk;
+        h->tc_ok = tc;
+        h->pre = pre;
     }
     return align_up(cv.off, 256);
 }
@@ -184,6 +230,64 @@ pe_status reset_state(pe_handle* h, cudaStream_t st) {
         if (!e) e = cudaMemsetAsync(d.clock, 0, sizeof(uint32_t), st);
         if (e) return cuda_fail(h, e, "reset residency");
     }
+    return PE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor map with 128-byte swizzled boxes (inner box = 64 elements).
+bool encode_bf16(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor maps over the prefill workspace and the whole slot table.
+pe_status setup_prefill(pe_handle* h) {
+    const pe_config& c = h->cfg;
+    const PrefillDev& P = h->pre;
+    const cuuint64_t H = (cuuint64_t)c.hidden, I = (cuuint64_t)c.intermediate, rows = (cuuint64_t)P.max_rows;
+    const cuuint64_t nslots = (cuuint64_t)c.num_layers * c.num_slots, stride = h->row.row_stride;
+    bool ok = true;
+    {
+        const cuuint64_t d[2] = {H, rows}, st[1] = {H * 2};
+        const cuuint32_t b[2] = {64, 128};
+        ok = ok && encode_bf16(&h->maps.x_perm, P.x_perm, 2, d, st, b);
+    }
+    {
+        const cuuint64_t d[2] = {I, rows}, st[1] = {I * 2};
+        const cuuint32_t b[2] = {64, 128};
+        ok = ok && encode_bf16(&h->maps.h_perm, P.h_perm, 2, d, st, b);
+    }
+    {
+        const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H * 2, stride};
+        const cuuint32_t b[3] = {64, 64, 1};
+        ok = ok && encode_bf16(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b);
+    }
+    {
+        const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I * 2, stride};
+        const cuuint32_t b[3] = {64, 128, 1};
+        ok = ok && encode_bf16(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b);
+    }
+    if (!ok) return fail(h, PE_ERR_CUDA, "could not encode the prefill tensor maps");
+    cudaError_t e = prefill_setup_kernels();
+    if (e) return cuda_fail(h, e, "prefill kernel attributes");
     return PE_OK;
 }
 
@@ -227,25 +331,17 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
     h->cfg = *cfg;
     h->row = r;
     carve(h, *cfg, r, static_cast<uint8_t*>(arena));
-    Shape& s = h->shape;
-    s.E = cfg->num_experts;
-    s.k = cfg->top_k;
-    s.K = cfg->num_slots;
-    s.H = cfg->hidden;
-    s.I = cfg->intermediate;
-    s.Wmax = h->Wmax;
-    s.dtype = cfg->dtype;
-    s.stride = r.row_stride;
-    s.copy_bytes = align_up(r.s2_offset + r.s2_bytes, 16);
-    s.w13_off = r.w13_offset;
-    s.s13_off = r.s13_offset;
-    s.w2_off = r.w2_offset;
-    s.s2_off = r.s2_offset;
-    s.tail_off = r.s13_offset;
+    h->shape = make_shape(*cfg, r);
+    h->shape.Wmax = h->Wmax;
     ce = cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, cfg->device);
     if (ce) {
         delete h;
         return fail(nullptr, PE_ERR_CUDA, std::string("device attribute: ") + cudaGetErrorString(ce));
+    }
+    if (h->tc_ok && setup_prefill(h) != PE_OK) {
+        const std::string msg = h->last_error;
+        delete h;
+        return fail(nullptr, PE_ERR_CUDA, msg);
     }
 
     const size_t store_bytes = (size_t)cfg->num_layers * cfg->num_experts * r.row_stride;
@@ -448,6 +544,25 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
     const bool fp8 = c.dtype == PE_FP8_BLOCK128;
+    if (!pagein_fused && h->tc_ok) {
+        // prefill sizes: per wave, page-in then the two tensor-core GEMMs;
+        // every entry lands in the merged buffer, summed after the last wave
+        for (int w = 0; w < s.Wmax; ++w) {
+            {
+                ProfScope p(h, P_PAGEIN, st);
+                e = launch_pagein(L, s, host_layer, slots_layer, w, max_count, h->num_sms, st);
+                if (e) return cuda_fail(h, e, "page-in kernel");
+            }
+            ProfScope p(h, P_GEMM, st);
+            e = launch_prefill_wave(L, s, h->pre, h->maps, x, layer * c.num_slots, w, T, h->merged, h->err,
+                                    h->num_sms, st);
+            if (e) return cuda_fail(h, e, "prefill GEMM kernels");
+        }
+        ProfScope p(h, P_SUM, st);
+        e = launch_topk_sum(s, h->merged, y, T, st);
+        if (e) return cuda_fail(h, e, "top-k sum kernel");
+        return PE_OK;
+    }
     for (int w = 0; w < s.Wmax; ++w) {
         if (pagein_fused) {
             ProfScope p(h, P_GATEUP_PAGEIN, st);

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libpe translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -47,6 +48,34 @@ struct Shape {
     size_t w13_off, s13_off, w2_off, s2_off;
     size_t tail_off;     // start of everything after w13 (scales, w2): copied as one block
 };
+
+// Workspace of the tensor-core prefill path (rows grouped by expert, each
+// expert padded to a multiple of 128 rows).
+struct PrefillDev {
+    __nv_bfloat16* x_perm;  // [max_rows][H]  A operand of the gate/up GEMM
+    __nv_bfloat16* h_perm;  // [max_rows][I]  A operand of the down GEMM
+    int32_t* perm;          // [max_rows]     entry of each row, -1 = padding
+    int4* tiles;            // [max_tiles]    (row0, slot in the whole table, valid rows, member)
+    int32_t* counts;        // [4]            tiles, rows of the current wave
+    int max_rows, max_tiles;
+};
+
+// TMA descriptors of the prefill path, encoded once at creation.
+struct PrefillMaps {
+    CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
+    CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
+    CUtensorMap w13;     // 3-D bf16 [L*K slots][2I][H], 64 x 64 x 1 boxes
+    CUtensorMap w2;      // 3-D bf16 [L*K slots][H][I], 64 x 128 x 1 boxes
+};
+
+bool prefill_tc_supported(const Shape& s);
+size_t prefill_max_rows(int max_entries, int K);
+cudaError_t prefill_setup_kernels();
+// align + gather + gate/up GEMM + down GEMM of one wave; merged entries are
+// written for the wave's entries (the top-k sum runs after the last wave).
+cudaError_t launch_prefill_wave(const LayerDev& L, const Shape& s, const PrefillDev& P, const PrefillMaps& M,
+                                const __nv_bfloat16* x, int slot_base, int wave, int T, float* merged,
+                                uint32_t* err, int num_sms, cudaStream_t st);
 
 // Records the message pe_last_error(NULL) returns in this thread.
 void set_thread_error(const char* msg);

@@ -61,6 +61,7 @@ typedef enum pe_dtype {
 #define PE_DEVERR_NAN_LOGIT  0x1u /* a router logit was NaN (routed as -inf) */
 #define PE_DEVERR_NOT_LOADED 0x2u /* a planned expert was never loaded       */
 #define PE_DEVERR_PLAN       0x4u /* internal plan check failed              */
+#define PE_DEVERR_TIMEOUT    0x8u /* a bounded wait inside a kernel gave up   */
 
 typedef struct pe_config {
     int32_t num_layers;   /* L, MoE layers sharing one host store         */
