@@ -57,6 +57,9 @@ def workload(name: str):
     if name.startswith("graphed48_b"):
         b = int(name[len("graphed48_b"):])
         return base.with_slots(64), b, f"48 layers, H=2048, I=768, E=128, top-8, K=64, bf16, batch {b}"
+    if name.startswith("prefill48_T"):
+        t = int(name[len("prefill48_T"):])
+        return base.with_slots(32), t, f"48 layers, H=2048, I=768, E=128, top-8, K=32, bf16, prefill chunks of {t} tokens"
     if name.startswith("fp8_48_b"):
         b = int(name[len("fp8_48_b"):])
         return synth.STACK48_FP8, b, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, batch {b}"
@@ -380,6 +383,119 @@ def launches_per_layer_step(shape, B):
     return n
 
 
+# ------------------------------------------------------------------ prefill workload
+
+
+def run_prefill(args):
+    """Prefill chunks through the 48-layer stack (one chunk per step, a few
+    distinct chunks cycled).  Eager launches; per-kernel events in a second
+    pass give the GEMM tensor-core throughput."""
+    import torch
+
+    from host_paged_expert_gb300 import _lib
+
+    shape, T, desc = workload(args.workload)
+    if args.layers:
+        import dataclasses
+
+        shape = dataclasses.replace(shape, num_layers=args.layers)
+        desc = desc.replace("48 layers", f"{args.layers} layers (profiling subset)")
+    L, E, H, I, k = shape.num_layers, shape.num_experts, shape.hidden, shape.intermediate, shape.top_k
+    W, K = args.warmup, args.steps
+    weights = synth.ExpertWeights(shape, seed=0)
+    model = _lib.PagedMoE(shape, max_tokens=T)
+    load_weights(model, weights)
+    log("experts loaded")
+    payload = model.layout["payload_bytes"]
+    nchunk = 2
+    stream = torch.cuda.Stream()
+    sp = stream.cuda_stream
+    lgs, hss = [], []
+    for c in range(nchunk):
+        lgs.append(torch.from_numpy(synth.prefill_logits(L, E, T, seed=c)).cuda())
+        hss.append(torch.from_numpy(synth.hidden_states((L, T), H, seed=c, tag=5).view(np.int16)).view(torch.bfloat16).cuda())
+    out = torch.empty((L, T, H), dtype=torch.bfloat16, device="cuda")
+    ce_gbs, kn_gbs = model.probe_host_link(min(args.probe_bytes, L * E * model.layout["row_stride"]), 3, stream)
+    link = max(ce_gbs, kn_gbs)
+    log(f"link {ce_gbs:.1f} / {kn_gbs:.1f} GB/s")
+    torch.cuda.synchronize()
+
+    def step(t):
+        lg, hs = lgs[t % nchunk], hss[t % nchunk]
+        for l in range(L):
+            model.forward_ptr(l, hs[l].data_ptr(), lg[l].data_ptr(), out[l].data_ptr(), T, sp)
+
+    with torch.cuda.stream(stream):
+        model.reset_residency(stream)
+        for t in range(W):
+            step(t)
+        s0 = model.stats(-1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        with ClockSampler(0) as clk:
+            a.record(stream)
+            for t in range(W, W + K):
+                step(t)
+            b.record(stream)
+            stream.synchronize()
+        ms = a.elapsed_time(b)
+        s1 = model.stats(-1)
+        # trace pass: per-kernel events and per-layer counters
+        model.reset_residency(stream)
+        for t in range(W):
+            step(t)
+        stream.synchronize()
+        model.profile_enable(True)
+        prev = [model.stats(l) for l in range(L)]
+        roof_s = 0.0
+        peaks = measured_peaks()
+        for t in range(W, W + K):
+            step(t)
+            stream.synchronize()
+            cur = [model.stats(l) for l in range(L)]
+            for l in range(L):
+                dist = cur[l]["distinct"] - prev[l]["distinct"]
+                pin = cur[l]["page_ins"] - prev[l]["page_ins"]
+                roof_s += max(dist * payload / (peaks["hbm_gbs"] * 1e9), pin * payload / (link * 1e9))
+            prev = cur
+        prof = model.profile_read()
+        model.profile_enable(False)
+    d = {n: s1[n] - s0[n] for n in ("steps", "waves", "entries", "distinct", "hits", "page_ins")}
+    tok_s = K * T / (ms * 1e-3)
+    log(f"prefill value pass: {ms:.1f} ms for {K} chunks -> {tok_s:.0f} tok/s")
+    ent = d["entries"]
+    flops = {"gemm_gateup": 2.0 * ent * H * 2 * I, "gemm_down": 2.0 * ent * I * H}
+    kernels = {}
+    for name, v in prof.items():
+        if not v["launches"]:
+            continue
+        e = {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
+             "avg_us": round(v["total_ms"] / v["launches"] * 1e3, 2)}
+        if name in flops:
+            tf = flops[name] / (v["total_ms"] * 1e-3) / 1e12
+            e.update({"bound": "tensor", "achieved_tflops": round(tf, 1), "peak_tflops": peaks["bf16_tflops"],
+                      "frac": round(tf / peaks["bf16_tflops"], 4)})
+        if name == "pagein":
+            gbs = d["page_ins"] * payload / (v["total_ms"] * 1e-3) / 1e9
+            e.update({"bound": "host_link", "achieved_gbs": round(gbs, 1), "peak_gbs": round(link, 1),
+                      "frac": round(gbs / link, 4)})
+        kernels[name] = e
+    line = {"metric": "paged-MoE prefill tok/s (48 layers, K resident)", "value": round(tok_s, 1), "unit": "tok/s",
+            "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms / K, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: {desc}", "chunks_cycled": nchunk},
+            "clocks": clk.summary(),
+            "page_in": {"per_layer_step": round(d["page_ins"] / (K * L), 2), "link_probe_gbs": [round(ce_gbs, 1), round(kn_gbs, 1)],
+                        "waves_per_layer_step": round(d["waves"] / (K * L), 2),
+                        "distinct_per_layer_step": round(d["distinct"] / (K * L), 2)},
+            "layer_roofline": {"frac": round(roof_s * 1e3 / (sum(v["total_ms"] for v in prof.values())), 4),
+                               "definition": "sum over layer-steps of max(distinct*expert_bytes/HBM, page_ins*expert_bytes/link) "
+                                             "divided by the summed kernel time of the trace pass"},
+            "kernels": kernels}
+    print(json.dumps(line), flush=True)
+    model.close()
+
+
 # ------------------------------------------------------------------ oracle (CPU baseline / reference arm)
 
 
@@ -456,6 +572,9 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.workload.startswith("prefill48_T"):
+        run_prefill(args)
+        return
     r = run_ours(args, rank, world, local_rank)
     if rank != 0:
         if world > 1:

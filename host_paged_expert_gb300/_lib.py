@@ -53,7 +53,7 @@ class PEPlanView(ctypes.Structure):
                 ("entry_slot", POINTER(c_int32)), ("entry_wave", POINTER(c_int32)), ("num_waves", c_int32)]
 
 
-PROF_KINDS = 8
+PROF_KINDS = 12
 
 
 class PEProfile(ctypes.Structure):

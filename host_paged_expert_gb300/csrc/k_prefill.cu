@@ -250,18 +250,22 @@ cudaError_t prefill_setup_kernels() {
     return e;
 }
 
-cudaError_t launch_prefill_wave(const LayerDev& L, const Shape& s, const PrefillDev& P, const PrefillMaps& M,
-                                const __nv_bfloat16* x, int slot_base, int wave, int T, float* merged, uint32_t* err,
-                                int num_sms, cudaStream_t st) {
+cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const PrefillDev& P, const __nv_bfloat16* x,
+                                 int slot_base, int wave, int T, int num_sms, cudaStream_t st) {
     cudaError_t e = launch_pdl(prefill_align_kernel, 1, 1024, 0, st, L, s, P, slot_base, wave, T);
     if (e) return e;
-    e = launch_pdl(prefill_gather_kernel, num_sms * 4, 256, 0, st, x, P, s.H, s.k);
-    if (e) return e;
+    return launch_pdl(prefill_gather_kernel, num_sms * 4, 256, 0, st, x, P, s.H, s.k);
+}
+
+cudaError_t launch_prefill_gemm(int which, const LayerDev& L, const Shape& s, const PrefillDev& P,
+                                const PrefillMaps& M, float* merged, uint32_t* err, cudaStream_t st) {
     const int m_tiles = P.max_tiles;
-    const int n1 = s.I / 64, n2 = s.H / BN;
-    e = launch_pdl(prefill_gemm_kernel<0>, m_tiles * n1, 128, (size_t)GEMM_SMEM, st, M.x_perm, M.w13, P, L, s, n1,
-                   s.H / BK, merged, err);
-    if (e) return e;
+    if (which == 0) {
+        const int n1 = s.I / 64;
+        return launch_pdl(prefill_gemm_kernel<0>, m_tiles * n1, 128, (size_t)GEMM_SMEM, st, M.x_perm, M.w13, P, L, s,
+                          n1, s.H / BK, merged, err);
+    }
+    const int n2 = s.H / BN;
     return launch_pdl(prefill_gemm_kernel<1>, m_tiles * n2, 128, (size_t)GEMM_SMEM, st, M.h_perm, M.w2, P, L, s, n2,
                       s.I / BK, merged, err);
 }

@@ -109,9 +109,12 @@ struct Carver {
     }
 };
 
-enum ProfKind { P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_GEMM, P_NUM };
-const char* kProfNames[P_NUM] = {"route", "plan", "pagein", "gateup", "gateup_pagein", "down", "topk_sum",
-                                 "prefill_gemm"};
+enum ProfKind {
+    P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_ALIGN, P_GEMM1, P_GEMM2, P_NUM
+};
+const char* kProfNames[P_NUM] = {"route",    "plan",         "pagein",       "gateup",
+                                 "gateup_pagein", "down",    "topk_sum",     "prefill_align",
+                                 "gemm_gateup",   "gemm_down"};
 
 }  // namespace
 
@@ -553,10 +556,19 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
                 e = launch_pagein(L, s, host_layer, slots_layer, w, max_count, h->num_sms, st);
                 if (e) return cuda_fail(h, e, "page-in kernel");
             }
-            ProfScope p(h, P_GEMM, st);
-            e = launch_prefill_wave(L, s, h->pre, h->maps, x, layer * c.num_slots, w, T, h->merged, h->err,
-                                    h->num_sms, st);
-            if (e) return cuda_fail(h, e, "prefill GEMM kernels");
+            {
+                ProfScope p(h, P_ALIGN, st);
+                e = launch_prefill_align(L, s, h->pre, x, layer * c.num_slots, w, T, h->num_sms, st);
+                if (e) return cuda_fail(h, e, "prefill align kernels");
+            }
+            {
+                ProfScope p(h, P_GEMM1, st);
+                e = launch_prefill_gemm(0, L, s, h->pre, h->maps, h->merged, h->err, st);
+                if (e) return cuda_fail(h, e, "gate/up GEMM kernel");
+            }
+            ProfScope p(h, P_GEMM2, st);
+            e = launch_prefill_gemm(1, L, s, h->pre, h->maps, h->merged, h->err, st);
+            if (e) return cuda_fail(h, e, "down GEMM kernel");
         }
         ProfScope p(h, P_SUM, st);
         e = launch_topk_sum(s, h->merged, y, T, st);

@@ -71,11 +71,14 @@ struct PrefillMaps {
 bool prefill_tc_supported(const Shape& s);
 size_t prefill_max_rows(int max_entries, int K);
 cudaError_t prefill_setup_kernels();
-// align + gather + gate/up GEMM + down GEMM of one wave; merged entries are
-// written for the wave's entries (the top-k sum runs after the last wave).
-cudaError_t launch_prefill_wave(const LayerDev& L, const Shape& s, const PrefillDev& P, const PrefillMaps& M,
-                                const __nv_bfloat16* x, int slot_base, int wave, int T, float* merged,
-                                uint32_t* err, int num_sms, cudaStream_t st);
+// Prefill wave, part 1: group the wave's entries by expert into 128-row
+// tiles and gather their token rows (align + gather kernels).
+cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const PrefillDev& P, const __nv_bfloat16* x,
+                                 int slot_base, int wave, int T, int num_sms, cudaStream_t st);
+// Prefill wave, part 2: which = 0 the gate/up GEMM (h), 1 the down GEMM
+// (merged entries of the wave; the top-k sum runs after the last wave).
+cudaError_t launch_prefill_gemm(int which, const LayerDev& L, const Shape& s, const PrefillDev& P,
+                                const PrefillMaps& M, float* merged, uint32_t* err, cudaStream_t st);
 
 // Records the message pe_last_error(NULL) returns in this thread.
 void set_thread_error(const char* msg);

@@ -118,7 +118,7 @@ typedef struct pe_plan_view {
 } pe_plan_view;
 
 /* Per-kernel device time recorded while profiling is on. */
-#define PE_PROF_KINDS 8
+#define PE_PROF_KINDS 12
 typedef struct pe_profile_t {
     const char* name[PE_PROF_KINDS]; /* kernel family; NULL if unused        */
     uint64_t launches[PE_PROF_KINDS];

@@ -262,3 +262,22 @@ def test_odd_slot_and_entry_counts(E, k, K):
         assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
     b.close()
     a.close()
+
+
+def test_prefill_runs_on_the_tensor_core_path(tiny):
+    """A 64-token chunk (128 entries) takes the tcgen05 GEMM path; a decode
+    step takes the fused page-in GEMV path."""
+    s, w, paged, _ = tiny
+    _lib = _need_gpu()
+    m = _lib.PagedMoE(s, max_tokens=64, store_owner=paged)
+    m.profile_enable(True)
+    xb = synth.hidden_states((64,), s.hidden, seed=31)
+    lg = synth.prefill_logits(1, s.num_experts, 64, seed=31)[0]
+    m.forward(0, gu.to_dev_bf16(xb), gu.to_dev_f32(lg))
+    prof = m.profile_read()
+    assert prof["gemm_gateup"]["launches"] >= 2 and prof["gemm_down"]["launches"] >= 2 and prof["gateup_pagein"]["launches"] == 0
+    m.profile_enable(True)
+    m.forward(0, gu.to_dev_bf16(xb[:1]), gu.to_dev_f32(lg[:1]))
+    prof = m.profile_read()
+    assert prof["gateup_pagein"]["launches"] == 1 and prof["gemm_gateup"]["launches"] == 0
+    m.close()
