@@ -612,6 +612,7 @@ def main():
         link = max(r["link"]["copy_engine_gbs"], r["link"]["kernel_gbs"])
         alg = {"pagein": d["page_ins"] * r["payload"],
                "gateup_pagein": d["page_ins"] * r["payload"],
+               "decode_step": d["page_ins"] * r["payload"],
                "gateup": d["distinct"] * (lay["w13_bytes"] + lay["s13_bytes"]),
                "down": d["distinct"] * (lay["w2_bytes"] + lay["s2_bytes"])}
         kernels = {}
@@ -621,7 +622,7 @@ def main():
             ent = {"launches": v["launches"], "total_ms": round(v["total_ms"], 3),
                    "avg_us": round(v["total_ms"] / v["launches"] * 1e3, 2)}
             if name in alg:
-                on_link = name in ("pagein", "gateup_pagein")
+                on_link = name in ("pagein", "gateup_pagein", "decode_step")
                 bound = "host_link" if on_link else "hbm"
                 peak = link if on_link else peaks["hbm_gbs"]
                 ach = alg[name] / (v["total_ms"] * 1e-3) / 1e9 if v["total_ms"] > 0 else 0.0

@@ -1,0 +1,386 @@
+// Single-wave decode step of the expert MLP in one kernel: page-in, gate/up,
+// down projection and top-k sum.
+//
+// "Paged Experts" (SGLang docs), "Captured decode": a decode step whose
+// entries fit the K slots (tokens * top_k <= K) is one wave decided and paged
+// on the GPU.  Once the plan is written, what bounds that step is the host
+// link: the missing experts' bytes must cross it.  This kernel keeps every
+// other part of the step underneath that transfer.
+//   link SMs   stream the page-ins' gate/up rows from the host store (writing
+//              them to their slots and computing h from them on the way) and
+//              copy the rest of each paged row;
+//   HBM SMs    compute h of the resident experts, then - as soon as those are
+//              all done - their down projections into the merged buffer;
+//   all SMs    once the link is drained: the down projections of the paged
+//              experts, then the fixed-order top-k sum.
+// A CTA's role follows the SM it runs on (every third SM streams the link):
+// outstanding host reads hold an SM's memory pipeline for tens of
+// microseconds, and HBM loads issued on the same SM would queue behind them.
+// Work inside a role is taken from atomic queues.  Phases are ordered by
+// counters in global memory (bounded waits; the grid is sized so that every
+// CTA is resident at once).  The last CTA to leave resets the counters for the
+// layer's next step.
+//
+// Every value is computed by the same device code, in the same order, as in
+// the multi-kernel path (row_pair_h for h, the lane-chunked dot product and
+// warp sum for a down row, p = w * d, the sum over j = 0..k-1 from zero), so
+// the two paths give the same bits and the output still equals K = E.
+
+#include "pe_device.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+namespace {
+
+constexpr int kThr = 256;
+constexpr int kWp = kThr / 32;
+constexpr int kRowsD = 4;                                 // down rows per warp item
+constexpr int kCopyLd = 8;                                // 16-byte loads per lane per copy item
+constexpr size_t kCopyItem = (size_t)32 * 16 * kCopyLd;  // 4 KiB
+constexpr int kDynBudget = 48 * 1024;
+constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a second
+
+// Per-layer counters: work queues (next item), completion counts and barriers.
+enum SyncSlot { Q_LINK = 0, Q_HBM, Q_HDOWN, D_LINK, D_HITS, S_DOWN, S_EXIT, S_NUM };
+constexpr int kGrab = 2;        // items a warp takes from a queue at a time
+constexpr int kLinkSmEvery = 3;  // SMs with %smid % 3 == 0 stream the host link
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bypass L1: data written by other CTAs of this grid.
+__device__ __forceinline__ int4 ldcg16(const void* p) { return __ldcg(reinterpret_cast<const int4*>(p)); }
+
+// All threads of the CTA have finished their writes; publish them and count.
+__device__ __forceinline__ void cta_arrive(unsigned* ctr) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+    }
+}
+
+// Wait (thread 0 polls, the CTA waits at the barrier) until *ctr >= target.
+// Gives up after kSpinLimit polls, records PE_DEVERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool cta_wait(const unsigned* ctr, unsigned target, uint32_t* err, int* flag_sh) {
+    if (threadIdx.x == 0) {
+        int ok = 0;
+        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+            if (ld_acquire_u32(ctr) >= target) {
+                ok = 1;
+                break;
+            }
+            __nanosleep(128);
+        }
+        if (!ok) atomicOr(err, PE_DEVERR_TIMEOUT);
+        *flag_sh = ok;
+    }
+    __syncthreads();
+    return *flag_sh != 0;
+}
+
+// p = w * (down_m . h) for kRowsD rows m0.. of one entry, written to merged.
+// CPL = 16-byte chunks of an I-long row per lane.
+template <int CPL>
+__device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, float wj, int m0, int H, int I,
+                                          float* merged_row, int lane) {
+    const int nchunk = I >> 3;
+    const size_t row_bytes = (size_t)I * 2;
+    int4 wv[kRowsD][CPL];
+#pragma unroll
+    for (int r = 0; r < kRowsD; ++r)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int idx = lane + 32 * c;
+            wv[r][c] = (m0 + r < H && idx < nchunk) ? ldcg16(w2 + (size_t)(m0 + r) * row_bytes + 16 * (size_t)idx)
+                                                    : make_int4(0, 0, 0, 0);
+        }
+    float4 hv[CPL][2];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        if (idx < nchunk) {
+            hv[c][0] = __ldcg(reinterpret_cast<const float4*>(h + 8 * idx));
+            hv[c][1] = __ldcg(reinterpret_cast<const float4*>(h + 8 * idx + 4));
+        } else {
+            hv[c][0] = hv[c][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsD; ++r) {
+        float d = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (lane + 32 * c < nchunk) d = dot8_bf16_f32(wv[r][c], hv[c][0], hv[c][1], d);
+        d = warp_sum(d);
+        if (lane == 0 && m0 + r < H) merged_row[m0 + r] = __fmul_rn(wj, d);
+    }
+}
+
+// Dynamic shared memory: [member experts K][member slots K][entry keys nent]
+// [entry member nent] padded to 4 ints, then the tokens' x when it fits.
+template <int CPLH, int CPLI>
+__global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Shape s,
+                                                                 const __nv_bfloat16* __restrict__ x,
+                                                                 const uint8_t* __restrict__ host,
+                                                                 uint8_t* __restrict__ slots, int T,
+                                                                 float* __restrict__ hbuf, float* __restrict__ merged,
+                                                                 __nv_bfloat16* __restrict__ out, unsigned* sync,
+                                                                 uint32_t* err, int stage_x) {
+    extern __shared__ int4 sh_dyn[];
+    __shared__ int sh_flag;
+    __shared__ int sh_nhit, sh_nmiss;
+    __shared__ int sh_hit_list[kFusedMaxEntries], sh_miss_list[kFusedMaxEntries];
+    int32_t* sh_mexp = reinterpret_cast<int32_t*>(sh_dyn);
+    int32_t* sh_mslot = sh_mexp + s.K;
+    int32_t* sh_ekey = sh_mslot + s.K;  // entry's slot (-1 if not in the wave)
+    int32_t* sh_eq = sh_ekey + kFusedMaxEntries;  // entry's member index
+    const int nent = T * s.k;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    pdl_wait();
+
+    const int size = L.member_count[0];
+    const int count = L.plan_count[0];
+    for (int i = threadIdx.x; i < size; i += blockDim.x) {
+        sh_mexp[i] = L.member_expert[i];
+        sh_mslot[i] = L.member_slot[i];
+    }
+    for (int i = threadIdx.x; i < nent; i += blockDim.x) sh_ekey[i] = L.entry_wave[i] == 0 ? L.entry_slot[i] : -1;
+    const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
+    if (stage_x) {
+        int4* sx = reinterpret_cast<int4*>(sh_mexp + ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3));
+        const int nvec = T * s.H / 8;
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) sx[i] = ldg16(xbase + 16 * (size_t)i);
+        xbase = reinterpret_cast<const uint8_t*>(sx);
+    }
+    __syncthreads();
+    if (threadIdx.x < nent) {  // member of each entry (nent <= kFusedMaxEntries <= kThr)
+        int q = -1;
+        for (int j = 0; j < size; ++j)
+            if (sh_mslot[j] == sh_ekey[threadIdx.x]) q = j;
+        sh_eq[threadIdx.x] = q;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {  // entries of hit members / of paged members, ascending
+        int nh = 0, nm = 0;
+        for (int i = 0; i < nent; ++i) {
+            const int q = sh_eq[i];
+            if (q < 0) continue;
+            if (q < count)
+                sh_miss_list[nm++] = i;
+            else
+                sh_hit_list[nh++] = i;
+        }
+        sh_nhit = nh;
+        sh_nmiss = nm;
+    }
+    __syncthreads();
+
+    const int nchunk = s.H >> 3;
+    const size_t row_bytes = (size_t)s.H * 2;
+    const long long miss_rows = (long long)count * s.I;
+    const size_t tail_bytes = s.copy_bytes - s.tail_off;
+    const long long copies_per = (long long)((tail_bytes + kCopyItem - 1) / kCopyItem);
+    const long long link_items = miss_rows + (long long)count * copies_per;
+    const long long hbm_items = (long long)(size - count) * s.I;
+    const int G = gridDim.x;
+    unsigned smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    const bool link_cta = hbm_items == 0 ? true : link_items == 0 ? false : (smid % kLinkSmEvery) == 0;
+    const int row_blocks = (s.H + kRowsD - 1) / kRowsD;
+
+    // Gate/up (and page-in) items from one role's queue: the link queue (page-in
+    // rows from the host store, then the rest of each paged row) or the HBM
+    // queue (resident members' rows).
+    auto run_queue = [&](const bool as_link) {
+        unsigned* q = &sync[as_link ? Q_LINK : Q_HBM];
+        unsigned* done = &sync[as_link ? D_LINK : D_HITS];
+        const long long total = as_link ? link_items : hbm_items;
+        for (;;) {
+            long long base = 0;
+            if (lane == 0) base = atomicAdd(q, (unsigned)kGrab);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (base >= total) break;
+            const long long end = min(base + kGrab, total);
+            for (long long item = base; item < end; ++item) {
+                if (as_link && item >= miss_rows) {
+                    const long long c = item - miss_rows;
+                    const int m = (int)(c / copies_per);
+                    const size_t off = s.tail_off + (size_t)(c - (long long)m * copies_per) * kCopyItem;
+                    const uint8_t* src = host + (size_t)sh_mexp[m] * s.stride + off;
+                    uint8_t* dst = slots + (size_t)sh_mslot[m] * s.stride + off;
+                    const size_t nbytes = min(kCopyItem, s.copy_bytes - off);
+                    int4 v[kCopyLd];
+#pragma unroll
+                    for (int u = 0; u < kCopyLd; ++u) {
+                        const size_t o = ((size_t)u * 32 + lane) * 16;
+                        if (o < nbytes) v[u] = ld_nc_na(src + o);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kCopyLd; ++u) {
+                        const size_t o = ((size_t)u * 32 + lane) * 16;
+                        if (o < nbytes) *reinterpret_cast<int4*>(dst + o) = v[u];
+                    }
+                    continue;
+                }
+                const int mq = as_link ? (int)(item / s.I) : count + (int)(item / s.I);
+                const int n = (int)(item % s.I);
+                const int slot = sh_mslot[mq];
+                uint8_t* slot_row = slots + (size_t)slot * s.stride + s.w13_off;
+                const uint8_t* g = (as_link ? host + (size_t)sh_mexp[mq] * s.stride + s.w13_off : slot_row) +
+                                   (size_t)n * row_bytes;
+                const uint8_t* u = g + (size_t)s.I * row_bytes;
+                int4 gv[CPLH], uv[CPLH];
+#pragma unroll
+                for (int c = 0; c < CPLH; ++c) {
+                    const int idx = lane + 32 * c;
+                    if (idx < nchunk) {
+                        gv[c] = as_link ? ld_nc_na(g + 16 * (size_t)idx) : ldg16(g + 16 * (size_t)idx);
+                        uv[c] = as_link ? ld_nc_na(u + 16 * (size_t)idx) : ldg16(u + 16 * (size_t)idx);
+                    } else {
+                        gv[c] = uv[c] = make_int4(0, 0, 0, 0);
+                    }
+                }
+                if (as_link) {
+                    uint8_t* gd = slot_row + (size_t)n * row_bytes;
+                    uint8_t* ud = gd + (size_t)s.I * row_bytes;
+#pragma unroll
+                    for (int c = 0; c < CPLH; ++c) {
+                        const int idx = lane + 32 * c;
+                        if (idx < nchunk) {
+                            *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[c];
+                            *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[c];
+                        }
+                    }
+                }
+                for (int b0 = 0; b0 < nent; b0 += 32) {
+                    const int i = b0 + lane;
+                    unsigned mask = __ballot_sync(0xffffffffu, i < nent && sh_ekey[i] == slot);
+                    while (mask) {
+                        const int ei = b0 + __ffs(mask) - 1;
+                        mask &= mask - 1;
+                        const float hval =
+                            row_pair_h<CPLH>(gv, uv, xbase + (size_t)(ei / s.k) * row_bytes, lane, nchunk);
+                        if (lane == 0) hbuf[(size_t)ei * s.I + n] = hval;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence();
+                atomicAdd(done, (unsigned)(end - base));
+            }
+        }
+    };
+
+    // ---- phase 1 ----
+    run_queue(link_cta);
+
+    // ---- phase 2: down projections ----
+    if (!link_cta) {
+        // resident experts: as soon as every resident expert's h is done
+        cta_wait(&sync[D_HITS], (unsigned)hbm_items, err, &sh_flag);
+        const long long items = (long long)sh_nhit * row_blocks;
+        for (;;) {
+            long long base = 0;
+            if (lane == 0) base = atomicAdd(&sync[Q_HDOWN], (unsigned)kGrab);
+            base = __shfl_sync(0xffffffffu, base, 0);
+            if (base >= items) break;
+            for (long long it = base; it < min(base + kGrab, items); ++it) {
+                const int e = sh_hit_list[it / row_blocks];
+                const int m0 = (int)(it % row_blocks) * kRowsD;
+                const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
+                down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, L.topk_w[e], m0, s.H, s.I, merged + (size_t)e * s.H,
+                                lane);
+            }
+        }
+        // then help drain the link queue (nothing of ours is queued on this SM any more)
+        if (link_items > 0) run_queue(true);
+    }
+    // paged experts: once the link is drained (their h and their w2 rows)
+    cta_wait(&sync[D_LINK], (unsigned)link_items, err, &sh_flag);
+    {
+        const long long items = (long long)sh_nmiss * row_blocks;
+        for (long long it = (long long)blockIdx.x * kWp + warp; it < items; it += (long long)G * kWp) {
+            const int e = sh_miss_list[it / row_blocks];
+            const int m0 = (int)(it % row_blocks) * kRowsD;
+            const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
+            down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, L.topk_w[e], m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+        }
+    }
+    cta_arrive(&sync[S_DOWN]);
+    cta_wait(&sync[S_DOWN], (unsigned)G, err, &sh_flag);
+    pdl_trigger();
+
+    // ---- phase 3: top-k sum in entry order ----
+    const long long total = (long long)T * s.H;
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total; q += (long long)G * blockDim.x) {
+        const int t = (int)(q / s.H);
+        const int m = (int)(q - (long long)t * s.H);
+        float acc = 0.f;
+        for (int j = 0; j < s.k; ++j) acc = __fadd_rn(acc, __ldcg(merged + ((size_t)t * s.k + j) * s.H + m));
+        out[q] = __float2bfloat16_rn(acc);
+    }
+
+    // the last CTA out resets the counters for this layer's next step
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&sync[S_EXIT], 1u) == (unsigned)G - 1) {
+            for (int i = 0; i < S_EXIT; ++i) sync[i] = 0;
+            __threadfence();
+            sync[S_EXIT] = 0;
+        }
+    }
+}
+
+}  // namespace
+
+int decode_fused_sync_words() { return S_NUM; }
+
+bool decode_fused_supported(const Shape& s, int T) {
+    const int cplh = (s.H / 8 + 31) / 32, cpli = (s.I / 8 + 31) / 32;
+    return s.dtype == PE_BF16 && (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K &&
+           cplh <= 8 && cpli <= 4 && (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
+}
+
+cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* host_layer,
+                                uint8_t* slots_layer, int T, float* hbuf, float* merged, __nv_bfloat16* out,
+                                unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st) {
+    const int grid = num_sms * 2;  // two CTAs per SM: every CTA is resident at once
+    const size_t meta = (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3);
+    const size_t xbytes = (size_t)T * s.H * 2;
+    const int stage = meta + xbytes <= (size_t)kDynBudget;
+    const size_t smem = meta + (stage ? xbytes : 0);
+    const int cplh = (s.H / 8 + 31) / 32, cpli = (s.I / 8 + 31) / 32;
+#define PE_DEC(A, B) \
+    return launch_pdl(decode_mlp_bf16_kernel<A, B>, grid, kThr, smem, st, L, s, x, host_layer, slots_layer, T, hbuf, merged, out, sync, err, stage)
+    if (cplh <= 1) {
+        if (cpli <= 1) PE_DEC(1, 1);
+        if (cpli <= 2) PE_DEC(1, 2);
+        if (cpli <= 3) PE_DEC(1, 3);
+        PE_DEC(1, 4);
+    }
+    if (cplh <= 2) {
+        if (cpli <= 1) PE_DEC(2, 1);
+        if (cpli <= 2) PE_DEC(2, 2);
+        if (cpli <= 3) PE_DEC(2, 3);
+        PE_DEC(2, 4);
+    }
+    if (cplh <= 4) {
+        if (cpli <= 1) PE_DEC(4, 1);
+        if (cpli <= 2) PE_DEC(4, 2);
+        if (cpli <= 3) PE_DEC(4, 3);
+        PE_DEC(4, 4);
+    }
+    if (cpli <= 1) PE_DEC(8, 1);
+    if (cpli <= 2) PE_DEC(8, 2);
+    if (cpli <= 3) PE_DEC(8, 3);
+    PE_DEC(8, 4);
+#undef PE_DEC
+}
+
+}  // namespace pe

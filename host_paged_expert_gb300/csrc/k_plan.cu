@@ -28,20 +28,27 @@
 namespace pe {
 namespace {
 
-// Selection order: larger logit first, equal logits -> lower id first.
-__device__ __forceinline__ bool ranks_before(float v, int id, float bv, int bid) {
-    return v > bv || (v == bv && id < bid);
+// Order-preserving 32-bit key of a logit (larger logit -> larger key); -0 and
+// +0 share a key, as they compare equal.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+    if (v == 0.f) v = 0.f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
 // One warp routes one token: top-k ids in selection order and the softmax
 // over the chosen logits (equal to the E-wide softmax renormalised on them).
-// EPL = logits per lane (ceil(E / 32)), held in registers.  Lane j < k
-// returns pick j in (id, w); other lanes return id = -1.
+// EPL = logits per lane (ceil(E / 32)), held in registers.  Each of the k
+// picks takes the lane-local best candidate strictly after the previous pick
+// (larger logit first, then lower id), a warp max-reduction of its key, and a
+// min-reduction of the ids that carry that key.  Lane j < k returns pick j in
+// (id, w); other lanes return id = -1.
 template <int EPL>
 __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int& out_id,
                                                  float& out_w, bool& nan_seen) {
     const int lane = threadIdx.x & 31;
     float v[EPL];
+    uint32_t key[EPL];
 #pragma unroll
     for (int q = 0; q < EPL; ++q) {
         const int e = lane + 32 * q;
@@ -51,37 +58,40 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
             nan_seen = true;
         }
         v[q] = x;
+        key[q] = logit_key(x);
     }
-    float prev_v = 0.f, my_v = -INFINITY;
-    int prev_id = -1, my_id = -1;
+    uint32_t prev_key = 0xffffffffu;
+    int prev_id = -1;
+    float my_v = -INFINITY;
+    int my_id = -1;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
+        uint32_t bk = 0;
         int bid = 0x7fffffff;
+        bool have = false;
 #pragma unroll
         for (int q = 0; q < EPL; ++q) {
             const int e = lane + 32 * q;
             // only experts that exist and come strictly after the previous pick
-            const bool ok = e < E && (j == 0 || ranks_before(prev_v, prev_id, v[q], e));
-            if (ok && ranks_before(v[q], e, bv, bid)) {
-                bv = v[q];
+            const bool after = j == 0 || key[q] < prev_key || (key[q] == prev_key && e > prev_id);
+            if (e < E && after && (!have || key[q] > bk)) {  // ids ascend with q: first wins a tie
+                bk = key[q];
                 bid = e;
+                have = true;
             }
         }
+        const uint32_t mk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
+        const uint32_t cand = (have && bk == mk) ? (uint32_t)bid : 0xffffffffu;
+        const int mid = (int)__reduce_min_sync(0xffffffffu, cand);
+        if (lane == j) my_id = mid;
+        prev_key = mk;
+        prev_id = mid;
+    }
+    // the chosen logits: lane j fetches the value of pick j from its owner lane
 #pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oid = __shfl_xor_sync(0xffffffffu, bid, o);
-            if (ranks_before(ov, oid, bv, bid)) {
-                bv = ov;
-                bid = oid;
-            }
-        }
-        if (lane == j) {
-            my_v = bv;
-            my_id = bid;
-        }
-        prev_v = bv;
-        prev_id = bid;
+    for (int q = 0; q < EPL; ++q) {
+        const int owner_q = (my_id >= 0) ? (my_id >> 5) : 0;
+        const float cand_v = __shfl_sync(0xffffffffu, v[q], (my_id >= 0 ? my_id : 0) & 31);
+        if (lane < k && owner_q == q) my_v = cand_v;
     }
     const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
     float ex = 0.f;

@@ -110,11 +110,11 @@ struct Carver {
 };
 
 enum ProfKind {
-    P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_ALIGN, P_GEMM1, P_GEMM2, P_NUM
+    P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_ALIGN, P_GEMM1, P_GEMM2, P_DECODE, P_NUM
 };
-const char* kProfNames[P_NUM] = {"route",    "plan",         "pagein",       "gateup",
-                                 "gateup_pagein", "down",    "topk_sum",     "prefill_align",
-                                 "gemm_gateup",   "gemm_down"};
+const char* kProfNames[P_NUM] = {"route",         "plan",        "pagein",       "gateup",
+                                 "gateup_pagein", "down",        "topk_sum",     "prefill_align",
+                                 "gemm_gateup",   "gemm_down",   "decode_step"};
 
 }  // namespace
 
@@ -208,6 +208,7 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         d.entry_slot = cv.take<int32_t>(maxTk);
         d.entry_wave = cv.take<int32_t>(maxTk);
         d.loaded = loaded ? loaded + (size_t)l * E : nullptr;
+        d.dsync = cv.take<unsigned>(8);
     }
     if (h) {
         h->slots = slots;
@@ -231,6 +232,7 @@ pe_status reset_state(pe_handle* h, cudaStream_t st) {
         if (!e) e = cudaMemsetAsync(d.slot_tick, 0, sizeof(uint32_t) * K, st);
         if (!e) e = cudaMemsetAsync(d.expert_slot, 0xFF, sizeof(int32_t) * E, st);
         if (!e) e = cudaMemsetAsync(d.clock, 0, sizeof(uint32_t), st);
+        if (!e) e = cudaMemsetAsync(d.dsync, 0, sizeof(unsigned) * 8, st);
         if (e) return cuda_fail(h, e, "reset residency");
     }
     return PE_OK;
@@ -547,6 +549,14 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
     const bool fp8 = c.dtype == PE_FP8_BLOCK128;
+    if (decode_fused_supported(s, T)) {
+        // one wave of decode size: everything after the plan in one kernel
+        ProfScope p(h, P_DECODE, st);
+        e = launch_decode_fused(L, s, x, host_layer, slots_layer, T, h->hbuf, h->merged, y, L.dsync, h->err,
+                                h->num_sms, st);
+        if (e) return cuda_fail(h, e, "decode kernel");
+        return PE_OK;
+    }
     if (!pagein_fused && h->tc_ok) {
         // prefill sizes: per wave, page-in then the two tensor-core GEMMs;
         // every entry lands in the merged buffer, summed after the last wave

@@ -266,7 +266,7 @@ def test_odd_slot_and_entry_counts(E, k, K):
 
 def test_prefill_runs_on_the_tensor_core_path(tiny):
     """A 64-token chunk (128 entries) takes the tcgen05 GEMM path; a decode
-    step takes the fused page-in GEMV path."""
+    step whose entries fit the slots takes the one-kernel decode path."""
     s, w, paged, _ = tiny
     _lib = _need_gpu()
     m = _lib.PagedMoE(s, max_tokens=64, store_owner=paged)
@@ -279,5 +279,6 @@ def test_prefill_runs_on_the_tensor_core_path(tiny):
     m.profile_enable(True)
     m.forward(0, gu.to_dev_bf16(xb[:1]), gu.to_dev_f32(lg[:1]))
     prof = m.profile_read()
-    assert prof["gateup_pagein"]["launches"] == 1 and prof["gemm_gateup"]["launches"] == 0
+    assert prof["decode_step"]["launches"] == 1 and prof["gemm_gateup"]["launches"] == 0
+    assert prof["gateup_pagein"]["launches"] == 0 and prof["down"]["launches"] == 0
     m.close()
