@@ -376,6 +376,10 @@ def run_ours(args, rank, world, local_rank):
 def launches_per_layer_step(shape, B):
     from host_paged_expert_gb300 import _lib
 
+    ent = B * shape.top_k
+    if (shape.dtype == "bf16" and ent <= min(64, shape.num_slots) and shape.num_experts <= 256
+            and shape.num_slots <= 256 and shape.hidden <= 2048 and shape.intermediate <= 1024):
+        return 1  # the whole decode step is one kernel
     Wm = _lib.max_waves(shape, B)
     n = 1 + 3 * Wm + (1 if Wm > 1 else 0)
     if B > 32:

@@ -1,11 +1,14 @@
-// Single-wave decode step of the expert MLP in one kernel: page-in, gate/up,
-// down projection and top-k sum.
+// A single-wave decode step in one kernel: routing and LRU plan, page-in,
+// gate/up, down projection and top-k sum.
 //
 // "Paged Experts" (SGLang docs), "Captured decode": a decode step whose
 // entries fit the K slots (tokens * top_k <= K) is one wave decided and paged
 // on the GPU.  Once the plan is written, what bounds that step is the host
 // link: the missing experts' bytes must cross it.  This kernel keeps every
 // other part of the step underneath that transfer.
+//   planner    the first CTA to start routes the tokens and plans the wave
+//              (plan_block, the same code as the standalone planner); every
+//              other CTA stages its inputs meanwhile and waits for the plan;
 //   link SMs   stream the page-ins' gate/up rows from the host store (writing
 //              them to their slots and computing h from them on the way) and
 //              copy the rest of each paged row;
@@ -28,6 +31,7 @@
 
 #include "pe_device.cuh"
 #include "pe_internal.h"
+#include "plan_block.cuh"
 
 namespace pe {
 namespace {
@@ -41,7 +45,8 @@ constexpr int kDynBudget = 48 * 1024;
 constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a second
 
 // Per-layer counters: work queues (next item), completion counts and barriers.
-enum SyncSlot { Q_LINK = 0, Q_HBM, Q_HDOWN, D_LINK, D_HITS, S_DOWN, S_EXIT, S_NUM };
+enum SyncSlot { Q_LINK = 0, Q_HBM, Q_HDOWN, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, S_EXIT, S_NUM };
+constexpr int kPlanCap = 256;   // planner capacity inside this kernel: E, K <= 256
 constexpr int kGrab = 2;        // items a warp takes from a queue at a time
 constexpr int kLinkSmEvery = 3;  // SMs with %smid % 3 == 0 stream the host link
 
@@ -122,9 +127,12 @@ __device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, flo
 
 // Dynamic shared memory: [member experts K][member slots K][entry keys nent]
 // [entry member nent] padded to 4 ints, then the tokens' x when it fits.
-template <int CPLH, int CPLI>
-__global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Shape s,
-                                                                 const __nv_bfloat16* __restrict__ x,
+// CPLH = 8 and CPLI = 4 cover H <= 2048 and I <= 1024; chunks past the row
+// are skipped, so the arithmetic is that of the exact chunk counts.
+constexpr int CPLH = 8, CPLI = 4;
+template <int EPL>
+__global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
+                                                                  const __nv_bfloat16* __restrict__ x,
                                                                  const uint8_t* __restrict__ host,
                                                                  uint8_t* __restrict__ slots, int T,
                                                                  float* __restrict__ hbuf, float* __restrict__ merged,
@@ -138,17 +146,22 @@ __global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Sh
     int32_t* sh_mslot = sh_mexp + s.K;
     int32_t* sh_ekey = sh_mslot + s.K;  // entry's slot (-1 if not in the wave)
     int32_t* sh_eq = sh_ekey + kFusedMaxEntries;  // entry's member index
+    __shared__ int sh_planner;
     const int nent = T * s.k;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();
 
-    const int size = L.member_count[0];
-    const int count = L.plan_count[0];
-    for (int i = threadIdx.x; i < size; i += blockDim.x) {
-        sh_mexp[i] = L.member_expert[i];
-        sh_mslot[i] = L.member_slot[i];
+    // the first CTA to arrive plans the step; the others stage x meanwhile
+    if (threadIdx.x == 0) sh_planner = atomicAdd(&sync[P_TICKET], 1u) == 0;
+    __syncthreads();
+    if (sh_planner) {
+        plan_block<EPL, kPlanCap>(L, s, logits, T, 1, err);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            __threadfence();
+            atomicExch(&sync[P_READY], 1u);
+        }
     }
-    for (int i = threadIdx.x; i < nent; i += blockDim.x) sh_ekey[i] = L.entry_wave[i] == 0 ? L.entry_slot[i] : -1;
     const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
     if (stage_x) {
         int4* sx = reinterpret_cast<int4*>(sh_mexp + ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3));
@@ -156,6 +169,17 @@ __global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Sh
         for (int i = threadIdx.x; i < nvec; i += blockDim.x) sx[i] = ldg16(xbase + 16 * (size_t)i);
         xbase = reinterpret_cast<const uint8_t*>(sx);
     }
+    cta_wait(&sync[P_READY], 1u, err, &sh_flag);
+
+    // the plan (written by the planner CTA in this kernel: read past L1)
+    const int size = __ldcg(L.member_count);
+    const int count = __ldcg(L.plan_count);
+    for (int i = threadIdx.x; i < size; i += blockDim.x) {
+        sh_mexp[i] = __ldcg(L.member_expert + i);
+        sh_mslot[i] = __ldcg(L.member_slot + i);
+    }
+    for (int i = threadIdx.x; i < nent; i += blockDim.x)
+        sh_ekey[i] = __ldcg(L.entry_wave + i) == 0 ? __ldcg(L.entry_slot + i) : -1;
     __syncthreads();
     if (threadIdx.x < nent) {  // member of each entry (nent <= kFusedMaxEntries <= kThr)
         int q = -1;
@@ -293,8 +317,8 @@ __global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Sh
                 const int e = sh_hit_list[it / row_blocks];
                 const int m0 = (int)(it % row_blocks) * kRowsD;
                 const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
-                down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, L.topk_w[e], m0, s.H, s.I, merged + (size_t)e * s.H,
-                                lane);
+                down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, __ldcg(L.topk_w + e), m0, s.H, s.I,
+                                merged + (size_t)e * s.H, lane);
             }
         }
         // then help drain the link queue (nothing of ours is queued on this SM any more)
@@ -308,7 +332,8 @@ __global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Sh
             const int e = sh_miss_list[it / row_blocks];
             const int m0 = (int)(it % row_blocks) * kRowsD;
             const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
-            down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, L.topk_w[e], m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+            down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, __ldcg(L.topk_w + e), m0, s.H, s.I, merged + (size_t)e * s.H,
+                            lane);
         }
     }
     cta_arrive(&sync[S_DOWN]);
@@ -342,44 +367,35 @@ __global__ void __launch_bounds__(kThr, 2) decode_mlp_bf16_kernel(LayerDev L, Sh
 int decode_fused_sync_words() { return S_NUM; }
 
 bool decode_fused_supported(const Shape& s, int T) {
-    const int cplh = (s.H / 8 + 31) / 32, cpli = (s.I / 8 + 31) / 32;
     return s.dtype == PE_BF16 && (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K &&
-           cplh <= 8 && cpli <= 4 && (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
+           s.E <= kPlanCap && s.K <= kPlanCap && s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI &&
+           (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
 }
 
-cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* host_layer,
-                                uint8_t* slots_layer, int T, float* hbuf, float* merged, __nv_bfloat16* out,
-                                unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st) {
+cudaError_t decode_setup_kernels() {
+    cudaError_t e = cudaSuccess;
+#define PE_ATTR(N) \
+    if (!e) e = cudaFuncSetAttribute(decode_step_bf16_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
+    PE_ATTR(1) PE_ATTR(2) PE_ATTR(4) PE_ATTR(8)
+#undef PE_ATTR
+    return e;
+}
+
+cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* logits, const __nv_bfloat16* x,
+                                const uint8_t* host_layer, uint8_t* slots_layer, int T, float* hbuf, float* merged,
+                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st) {
     const int grid = num_sms * 2;  // two CTAs per SM: every CTA is resident at once
     const size_t meta = (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3);
     const size_t xbytes = (size_t)T * s.H * 2;
     const int stage = meta + xbytes <= (size_t)kDynBudget;
     const size_t smem = meta + (stage ? xbytes : 0);
-    const int cplh = (s.H / 8 + 31) / 32, cpli = (s.I / 8 + 31) / 32;
-#define PE_DEC(A, B) \
-    return launch_pdl(decode_mlp_bf16_kernel<A, B>, grid, kThr, smem, st, L, s, x, host_layer, slots_layer, T, hbuf, merged, out, sync, err, stage)
-    if (cplh <= 1) {
-        if (cpli <= 1) PE_DEC(1, 1);
-        if (cpli <= 2) PE_DEC(1, 2);
-        if (cpli <= 3) PE_DEC(1, 3);
-        PE_DEC(1, 4);
-    }
-    if (cplh <= 2) {
-        if (cpli <= 1) PE_DEC(2, 1);
-        if (cpli <= 2) PE_DEC(2, 2);
-        if (cpli <= 3) PE_DEC(2, 3);
-        PE_DEC(2, 4);
-    }
-    if (cplh <= 4) {
-        if (cpli <= 1) PE_DEC(4, 1);
-        if (cpli <= 2) PE_DEC(4, 2);
-        if (cpli <= 3) PE_DEC(4, 3);
-        PE_DEC(4, 4);
-    }
-    if (cpli <= 1) PE_DEC(8, 1);
-    if (cpli <= 2) PE_DEC(8, 2);
-    if (cpli <= 3) PE_DEC(8, 3);
-    PE_DEC(8, 4);
+    const int epl = (s.E + 31) / 32;
+#define PE_DEC(N) \
+    return launch_pdl(decode_step_bf16_kernel<N>, grid, kThr, smem, st, L, s, logits, x, host_layer, slots_layer, T, hbuf, merged, out, sync, err, stage)
+    if (epl <= 1) PE_DEC(1);
+    if (epl <= 2) PE_DEC(2);
+    if (epl <= 4) PE_DEC(4);
+    PE_DEC(8);
 #undef PE_DEC
 }
 

@@ -1,107 +1,12 @@
-// Routing and LRU wave planning on the device.
-//
-// "Paged Experts" (SGLang docs), "A step: waves, page-in, merge", steps 1-3,
-// and "Captured decode": the LRU decision is made on the GPU and written as a
-// page-in plan (experts, slots, count) to device buffers, so a step needs no
-// host synchronisation.  This kernel plans every wave of a step, not only the
-// single decode wave, so prefill is planned on the device too.
-//
-// Conventions the CPU reference fixes and this kernel reproduces bit for bit:
-//   routing: top-k by logit, ties to the lower expert id, NaN as -inf;
-//   D = distinct routed ids; order = resident members of D (ascending id)
-//   followed by the others (ascending id), cut into waves of K;
-//   per wave: clock += 1; resident members get tick = clock; victims are the
-//   slots whose expert is outside the wave, by (tick, slot) ascending; the
-//   missing members in ascending id take the victims in that order and get
-//   tick = clock.
-//
-// The planner is one CTA and sits on the critical path of every decode
-// step, so it is written for latency: all of its global loads are issued
-// up front, routing works on logits held in registers, and everything after
-// routing runs in shared memory until the final stores.
+// Standalone routing and planning kernels (the planner itself is plan_block,
+// shared with the one-kernel decode step): route_kernel routes many tokens,
+// one warp each, ahead of the planner for prefill-sized steps; plan_kernel
+// plans every wave of a step in one CTA, routing inline for small steps.
 
-#include <math.h>
-
-#include "pe_device.cuh"
-#include "pe_internal.h"
+#include "plan_block.cuh"
 
 namespace pe {
 namespace {
-
-// Order-preserving 32-bit key of a logit (larger logit -> larger key); -0 and
-// +0 share a key, as they compare equal.
-__device__ __forceinline__ uint32_t logit_key(float v) {
-    if (v == 0.f) v = 0.f;
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// One warp routes one token: top-k ids in selection order and the softmax
-// over the chosen logits (equal to the E-wide softmax renormalised on them).
-// EPL = logits per lane (ceil(E / 32)), held in registers.  Each of the k
-// picks takes the lane-local best candidate strictly after the previous pick
-// (larger logit first, then lower id), a warp max-reduction of its key, and a
-// min-reduction of the ids that carry that key.  Lane j < k returns pick j in
-// (id, w); other lanes return id = -1.
-template <int EPL>
-__device__ __forceinline__ void route_token_warp(const float* __restrict__ row, int E, int k, int& out_id,
-                                                 float& out_w, bool& nan_seen) {
-    const int lane = threadIdx.x & 31;
-    float v[EPL];
-    uint32_t key[EPL];
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-        const int e = lane + 32 * q;
-        float x = e < E ? row[e] : -INFINITY;
-        if (isnan(x)) {
-            x = -INFINITY;
-            nan_seen = true;
-        }
-        v[q] = x;
-        key[q] = logit_key(x);
-    }
-    uint32_t prev_key = 0xffffffffu;
-    int prev_id = -1;
-    float my_v = -INFINITY;
-    int my_id = -1;
-    for (int j = 0; j < k; ++j) {
-        uint32_t bk = 0;
-        int bid = 0x7fffffff;
-        bool have = false;
-#pragma unroll
-        for (int q = 0; q < EPL; ++q) {
-            const int e = lane + 32 * q;
-            // only experts that exist and come strictly after the previous pick
-            const bool after = j == 0 || key[q] < prev_key || (key[q] == prev_key && e > prev_id);
-            if (e < E && after && (!have || key[q] > bk)) {  // ids ascend with q: first wins a tie
-                bk = key[q];
-                bid = e;
-                have = true;
-            }
-        }
-        const uint32_t mk = __reduce_max_sync(0xffffffffu, have ? bk : 0u);
-        const uint32_t cand = (have && bk == mk) ? (uint32_t)bid : 0xffffffffu;
-        const int mid = (int)__reduce_min_sync(0xffffffffu, cand);
-        if (lane == j) my_id = mid;
-        prev_key = mk;
-        prev_id = mid;
-    }
-    // the chosen logits: lane j fetches the value of pick j from its owner lane
-#pragma unroll
-    for (int q = 0; q < EPL; ++q) {
-        const int owner_q = (my_id >= 0) ? (my_id >> 5) : 0;
-        const float cand_v = __shfl_sync(0xffffffffu, v[q], (my_id >= 0 ? my_id : 0) & 31);
-        if (lane < k && owner_q == q) my_v = cand_v;
-    }
-    const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
-    float ex = 0.f;
-    if (lane < k) ex = (v0 == -INFINITY) ? 1.f : expf(my_v - v0);
-    float sum = ex;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
-    out_id = lane < k ? my_id : -1;
-    out_w = lane < k ? __fdiv_rn(ex, sum) : 0.f;
-}
 
 template <int EPL>
 __global__ void __launch_bounds__(256) route_kernel(LayerDev L, int E, int k, const float* logits,
@@ -122,218 +27,13 @@ __global__ void __launch_bounds__(256) route_kernel(LayerDev L, int E, int k, co
     if (__any_sync(0xffffffffu, nan_seen) && lane == 0) atomicOr(err, PE_DEVERR_NAN_LOGIT);
 }
 
-// One CTA plans every wave of a step.  blockDim.x is a multiple of 32 and at
-// least E (thread e owns expert e in the scans) and K (thread s owns slot s).
+// One CTA plans every wave of a step (see plan_block).
 template <int EPL>
-__global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape s,
-                                                               const float* logits, int T,
+__global__ void __launch_bounds__(kPlanMaxThreads) plan_kernel(LayerDev L, Shape s, const float* logits, int T,
                                                                int route_inline, uint32_t* err) {
-    __shared__ int32_t sh_slot_expert[kMaxSlots];
-    __shared__ uint32_t sh_tick[kMaxSlots];
-    __shared__ int32_t sh_expert_slot[kMaxExperts];
-    __shared__ int32_t sh_order[kMaxExperts];
-    __shared__ int32_t sh_wave_of[kMaxExperts];
-    __shared__ int32_t sh_slot_in_wave[kMaxExperts];
-    __shared__ int32_t sh_ids[kMaxExperts];  // routed ids of an inline-routed step (T*k <= 1024)
-    __shared__ uint8_t sh_used[kMaxExperts];
-    __shared__ uint8_t sh_inwave[kMaxExperts];
-    __shared__ uint8_t sh_loaded[kMaxExperts];
-    __shared__ unsigned long long sh_vkey[kMaxSlots];  // (tick, slot) of victim slots, ~0 otherwise
-    __shared__ int sh_wr[32], sh_wm[32];
-    __shared__ int sh_nR, sh_nM, sh_cold, sh_bad, sh_nan;
-
-    const int tid = threadIdx.x, nthr = blockDim.x;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
-    const int E = s.E, K = s.K, k = s.k;
-    const int nent = T * k;
-    const bool ids_in_smem = route_inline && nent <= kMaxExperts;
-
     pdl_wait();
     pdl_trigger();
-    // every global load of the planner is issued here, before routing
-    for (int i = tid; i < K; i += nthr) {
-        sh_slot_expert[i] = L.slot_expert[i];
-        sh_tick[i] = L.slot_tick[i];
-    }
-    for (int e = tid; e < E; e += nthr) {
-        sh_expert_slot[e] = L.expert_slot[e];
-        sh_loaded[e] = L.loaded[e];
-        sh_used[e] = 0;
-        sh_inwave[e] = 0;
-        sh_wave_of[e] = -1;
-        sh_slot_in_wave[e] = -1;
-    }
-    if (tid == 0) {
-        sh_cold = 0;
-        sh_bad = 0;
-        sh_nan = 0;
-    }
-    uint32_t clock = *L.clock;
-    if (route_inline) {
-        for (int t = warp; t < T; t += nwarps) {
-            int id;
-            float w;
-            bool nan_seen = false;
-            route_token_warp<EPL>(logits + (size_t)t * E, E, k, id, w, nan_seen);
-            if (lane < k) {
-                L.topk_id[(size_t)t * k + lane] = id;
-                L.topk_w[(size_t)t * k + lane] = w;
-                if (ids_in_smem) sh_ids[t * k + lane] = id;
-            }
-            if (nan_seen) sh_nan = 1;
-        }
-    }
-    __syncthreads();  // routing, state and flags are in shared memory from here on
-
-    for (int i = tid; i < nent; i += nthr) {
-        const int e = ids_in_smem ? sh_ids[i] : L.topk_id[i];
-        if (e >= 0 && e < E)
-            sh_used[e] = 1;
-        else
-            sh_bad = 1;
-    }
-    __syncthreads();
-
-    // order = R ++ M, both ascending id (one scan for both lists)
-    const int e = tid;
-    const bool used = e < E && sh_used[e];
-    const bool isR = used && sh_expert_slot[e] >= 0;
-    const bool isM = used && sh_expert_slot[e] < 0;
-    const unsigned bR = __ballot_sync(0xffffffffu, isR), bM = __ballot_sync(0xffffffffu, isM);
-    const unsigned below = (1u << lane) - 1u;
-    if (lane == 0) {
-        sh_wr[warp] = __popc(bR);
-        sh_wm[warp] = __popc(bM);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int vr = lane < nwarps ? sh_wr[lane] : 0, vm = lane < nwarps ? sh_wm[lane] : 0;
-        int ir = vr, im = vm;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int nr = __shfl_up_sync(0xffffffffu, ir, o), nm = __shfl_up_sync(0xffffffffu, im, o);
-            if (lane >= o) {
-                ir += nr;
-                im += nm;
-            }
-        }
-        if (lane < nwarps) {
-            sh_wr[lane] = ir - vr;
-            sh_wm[lane] = im - vm;
-        }
-        if (lane == 31) {
-            sh_nR = ir;
-            sh_nM = im;
-        }
-    }
-    __syncthreads();
-    const int nR = sh_nR, nM = sh_nM;
-    if (isR) sh_order[sh_wr[warp] + __popc(bR & below)] = e;
-    if (isM) sh_order[nR + sh_wm[warp] + __popc(bM & below)] = e;
-    __syncthreads();
-
-    const int nD = nR + nM;
-    int nW = (nD + K - 1) / K;
-    if (nW > s.Wmax) {  // cannot happen for a consistent Wmax; never overrun the plan arrays
-        if (tid == 0) atomicOr(err, PE_DEVERR_PLAN);
-        nW = s.Wmax;
-    }
-    int total_miss = 0;
-    for (int w = 0; w < nW; ++w) {
-        const int base = w * K;
-        const int size = min(K, nD - base);
-        const int nres = (w == 0) ? nR : 0;  // only R can be resident, and R fits in wave 0
-        const int nmiss = size - nres;
-        ++clock;
-        for (int i = tid; i < size; i += nthr) {
-            const int m = sh_order[base + i];
-            sh_inwave[m] = 1;
-            if (i < nres) {
-                const int slot = sh_expert_slot[m];
-                sh_tick[slot] = clock;
-                // hits follow the page-ins in the member list
-                L.member_expert[(size_t)w * K + nmiss + i] = m;
-                L.member_slot[(size_t)w * K + nmiss + i] = slot;
-            }
-        }
-        __syncthreads();
-        // rank of each victim slot in (tick, slot) order
-        unsigned long long my_key = ~0ull;
-        if (tid < K) {
-            const int ex = sh_slot_expert[tid];
-            if (ex < 0 || !sh_inwave[ex]) my_key = ((unsigned long long)sh_tick[tid] << 32) | (unsigned)tid;
-            sh_vkey[tid] = my_key;
-        }
-        __syncthreads();
-        int my_rank = -1;
-        if (tid < K && my_key != ~0ull && nmiss > 0) {
-            int r = 0;
-#pragma unroll 8
-            for (int o = 0; o < K; ++o) r += sh_vkey[o] < my_key;
-            my_rank = r;
-        }
-        __syncthreads();
-        if (my_rank >= 0 && my_rank < nmiss) {
-            const int slot = tid;
-            const int m = sh_order[base + nres + my_rank];
-            const int old = sh_slot_expert[slot];
-            if (old >= 0)
-                sh_expert_slot[old] = -1;
-            else
-                atomicAdd(&sh_cold, 1);
-            sh_slot_expert[slot] = m;
-            sh_expert_slot[m] = slot;
-            sh_tick[slot] = clock;
-            const size_t q = (size_t)w * K + my_rank;
-            L.plan_expert[q] = m;
-            L.plan_slot[q] = slot;
-            L.member_expert[q] = m;
-            L.member_slot[q] = slot;
-            if (!sh_loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
-        }
-        __syncthreads();
-        for (int i = tid; i < size; i += nthr) {
-            const int m = sh_order[base + i];
-            sh_wave_of[m] = w;
-            sh_slot_in_wave[m] = sh_expert_slot[m];
-            sh_inwave[m] = 0;
-        }
-        if (tid == 0) {
-            L.plan_count[w] = nmiss;
-            L.member_count[w] = size;
-        }
-        total_miss += nmiss;
-        __syncthreads();
-    }
-    for (int w = nW + tid; w < s.Wmax; w += nthr) {
-        L.plan_count[w] = 0;
-        L.member_count[w] = 0;
-    }
-
-    for (int i = tid; i < nent; i += nthr) {
-        const int m = ids_in_smem ? sh_ids[i] : L.topk_id[i];
-        const bool ok = m >= 0 && m < E;
-        L.entry_wave[i] = ok ? sh_wave_of[m] : -1;
-        L.entry_slot[i] = ok ? sh_slot_in_wave[m] : 0;
-    }
-    for (int i = tid; i < K; i += nthr) {
-        L.slot_expert[i] = sh_slot_expert[i];
-        L.slot_tick[i] = sh_tick[i];
-    }
-    for (int m = tid; m < E; m += nthr) L.expert_slot[m] = sh_expert_slot[m];
-    if (tid == 0) {
-        *L.clock = clock;
-        *L.num_waves = nW;
-        atomicAdd(&L.counters[C_STEPS], 1ull);
-        atomicAdd(&L.counters[C_WAVES], (unsigned long long)nW);
-        atomicAdd(&L.counters[C_ENTRIES], (unsigned long long)nent);
-        atomicAdd(&L.counters[C_DISTINCT], (unsigned long long)nD);
-        atomicAdd(&L.counters[C_HITS], (unsigned long long)nR);
-        atomicAdd(&L.counters[C_PAGE_INS], (unsigned long long)total_miss);
-        atomicAdd(&L.counters[C_COLD], (unsigned long long)sh_cold);
-        if (sh_bad) atomicOr(err, PE_DEVERR_PLAN);
-        if (sh_nan) atomicOr(err, PE_DEVERR_NAN_LOGIT);
-    }
+    plan_block<EPL, kMaxExperts>(L, s, logits, T, route_inline, err);
 }
 
 inline int epl_for(int E) {

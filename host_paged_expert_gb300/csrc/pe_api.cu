@@ -208,7 +208,7 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         d.entry_slot = cv.take<int32_t>(maxTk);
         d.entry_wave = cv.take<int32_t>(maxTk);
         d.loaded = loaded ? loaded + (size_t)l * E : nullptr;
-        d.dsync = cv.take<unsigned>(8);
+        d.dsync = cv.take<unsigned>(16);
     }
     if (h) {
         h->slots = slots;
@@ -232,7 +232,7 @@ pe_status reset_state(pe_handle* h, cudaStream_t st) {
         if (!e) e = cudaMemsetAsync(d.slot_tick, 0, sizeof(uint32_t) * K, st);
         if (!e) e = cudaMemsetAsync(d.expert_slot, 0xFF, sizeof(int32_t) * E, st);
         if (!e) e = cudaMemsetAsync(d.clock, 0, sizeof(uint32_t), st);
-        if (!e) e = cudaMemsetAsync(d.dsync, 0, sizeof(unsigned) * 8, st);
+        if (!e) e = cudaMemsetAsync(d.dsync, 0, sizeof(unsigned) * 16, st);
         if (e) return cuda_fail(h, e, "reset residency");
     }
     return PE_OK;
@@ -342,6 +342,11 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
     if (ce) {
         delete h;
         return fail(nullptr, PE_ERR_CUDA, std::string("device attribute: ") + cudaGetErrorString(ce));
+    }
+    ce = decode_setup_kernels();
+    if (ce) {
+        delete h;
+        return fail(nullptr, PE_ERR_CUDA, std::string("decode kernel attributes: ") + cudaGetErrorString(ce));
     }
     if (h->tc_ok && setup_prefill(h) != PE_OK) {
         const std::string msg = h->last_error;
@@ -534,6 +539,14 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     const int route_inline = T <= kRouteInlineMaxTokens;
     const int max_count = (int)((long long)T * c.top_k < (long long)K ? (long long)T * c.top_k : (long long)K);
     cudaError_t e = cudaSuccess;
+    if (decode_fused_supported(s, T)) {
+        // one wave of decode size: the whole step, plan included, in one kernel
+        ProfScope p(h, P_DECODE, st);
+        e = launch_decode_fused(L, s, router_logits, x, host_layer, slots_layer, T, h->hbuf, h->merged, y, L.dsync,
+                                h->err, h->num_sms, st);
+        if (e) return cuda_fail(h, e, "decode kernel");
+        return PE_OK;
+    }
     if (!route_inline) {
         ProfScope p(h, P_ROUTE, st);
         e = launch_route(L, s, router_logits, T, h->err, st);
@@ -549,14 +562,6 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
     const bool fp8 = c.dtype == PE_FP8_BLOCK128;
-    if (decode_fused_supported(s, T)) {
-        // one wave of decode size: everything after the plan in one kernel
-        ProfScope p(h, P_DECODE, st);
-        e = launch_decode_fused(L, s, x, host_layer, slots_layer, T, h->hbuf, h->merged, y, L.dsync, h->err,
-                                h->num_sms, st);
-        if (e) return cuda_fail(h, e, "decode kernel");
-        return PE_OK;
-    }
     if (!pagein_fused && h->tc_ok) {
         // prefill sizes: per wave, page-in then the two tensor-core GEMMs;
         // every entry lands in the merged buffer, summed after the last wave

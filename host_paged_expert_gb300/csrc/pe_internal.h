@@ -38,7 +38,7 @@ struct LayerDev {
     int32_t* entry_slot;    // [maxT*k]
     int32_t* entry_wave;    // [maxT*k]
     const uint8_t* loaded;  // [E]   1 once the expert's host row was written
-    unsigned* dsync;        // [8]   queues and phase counters of the one-kernel decode step (zero between steps)
+    unsigned* dsync;        // [16]  queues and phase counters of the one-kernel decode step (zero between steps)
 };
 
 struct Shape {
@@ -115,13 +115,15 @@ cudaError_t launch_gateup(const LayerDev& L, const Shape& s, const __nv_bfloat16
 cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
                         int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
                         int num_sms, cudaStream_t st);
-// Single-wave decode (tokens * top_k <= min(K, kFusedMaxEntries), bf16):
-// page-in, gate/up, down and top-k sum in one kernel after the planner.
+// Single-wave decode (tokens * top_k <= min(K, kFusedMaxEntries), bf16,
+// E and K <= 256): routing, plan, page-in, gate/up, down and top-k sum in one
+// kernel.
 bool decode_fused_supported(const Shape& s, int T);
 int decode_fused_sync_words();
-cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* host_layer,
-                                uint8_t* slots_layer, int T, float* hbuf, float* merged, __nv_bfloat16* out,
-                                unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st);
+cudaError_t decode_setup_kernels();
+cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* logits, const __nv_bfloat16* x,
+                                const uint8_t* host_layer, uint8_t* slots_layer, int T, float* hbuf, float* merged,
+                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st);
 
 // Block-FP8 counterparts of the three decode kernels above.
 cudaError_t launch_gateup_pagein_fp8(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
