@@ -19,7 +19,9 @@
 // A CTA's role follows the SM it runs on (every third SM streams the link):
 // outstanding host reads hold an SM's memory pipeline for tens of
 // microseconds, and HBM loads issued on the same SM would queue behind them.
-// Work inside a role is taken from atomic queues.  Phases are ordered by
+// Work inside a role is split statically: every CTA registers its role and
+// gets a rank within it while the plan is being made, so no work queue is
+// contended during the transfer.  Phases are ordered by
 // counters in global memory (bounded waits; the grid is sized so that every
 // CTA is resident at once).  The last CTA to leave resets the counters for the
 // layer's next step.
@@ -29,6 +31,7 @@
 // warp sum for a down row, p = w * d, the sum over j = 0..k-1 from zero), so
 // the two paths give the same bits and the output still equals K = E.
 
+#include "fp8_device.cuh"
 #include "pe_device.cuh"
 #include "pe_internal.h"
 #include "plan_block.cuh"
@@ -44,11 +47,10 @@ constexpr size_t kCopyItem = (size_t)32 * 16 * kCopyLd;  // 4 KiB
 constexpr int kDynBudget = 48 * 1024;
 constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a second
 
-// Per-layer counters: work queues (next item), completion counts and barriers.
-enum SyncSlot { Q_LINK = 0, Q_HBM, Q_HDOWN, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, S_EXIT, S_NUM };
-constexpr int kPlanCap = 256;   // planner capacity inside this kernel: E, K <= 256
-constexpr int kGrab = 2;        // items a warp takes from a queue at a time
-constexpr int kLinkSmEvery = 3;  // SMs with %smid % 3 == 0 stream the host link
+// Per-layer counters: role registration, completion counts and barriers.
+enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, S_EXIT, S_NUM };
+constexpr int kPlanCap = 256;    // planner capacity inside this kernel: E, K <= 256
+constexpr int kLinkSmEvery = 3;  // CTAs on SMs with %smid % 3 == 0 stream the host link
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
@@ -125,13 +127,57 @@ __device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, flo
     }
 }
 
+// FP8 version: E4M3 codes with the 128x128 block scales of w2 (all kRowsD rows
+// lie in one 128-row block), the same arithmetic as the FP8 down kernel.
+template <int CPL>
+__device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2, const float* h, float wj, int m0,
+                                              int H, int I, float* merged_row, int lane) {
+    const int nchunk = I >> 4;
+    const int nbi = (I + kFp8Block - 1) / kFp8Block;
+    const float* srow = s2 + (size_t)(m0 / kFp8Block) * nbi;
+    int4 wv[kRowsD][CPL];
+#pragma unroll
+    for (int r = 0; r < kRowsD; ++r)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int idx = lane + 32 * c;
+            wv[r][c] = (m0 + r < H && idx < nchunk) ? ldcg16(w2 + (size_t)(m0 + r) * I + 16 * (size_t)idx)
+                                                    : make_int4(0, 0, 0, 0);
+        }
+    float sc[CPL];
+    float4 hv[CPL][4];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        if (idx < nchunk) {
+            sc[c] = __ldcg(srow + (idx * 16) / kFp8Block);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) hv[c][v] = __ldcg(reinterpret_cast<const float4*>(h + 16 * idx + 4 * v));
+        } else {
+            sc[c] = 0.f;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) hv[c][v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kRowsD; ++r) {
+        float d = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (lane + 32 * c < nchunk) d = fmaf(sc[c], dot16_e4m3_f32(wv[r][c], hv[c]), d);
+        d = warp_sum(d);
+        if (lane == 0 && m0 + r < H) merged_row[m0 + r] = __fmul_rn(wj, d);
+    }
+}
+
 // Dynamic shared memory: [member experts K][member slots K][entry keys nent]
 // [entry member nent] padded to 4 ints, then the tokens' x when it fits.
-// CPLH = 8 and CPLI = 4 cover H <= 2048 and I <= 1024; chunks past the row
-// are skipped, so the arithmetic is that of the exact chunk counts.
-constexpr int CPLH = 8, CPLI = 4;
-template <int EPL>
-__global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
+// Chunks per lane cover H <= 2048 and I <= 1024 (bf16: 8 and 4 chunks of 8
+// values, FP8: 4 and 2 chunks of 16 codes); chunks past the row are skipped,
+// so the arithmetic is that of the exact chunk counts.
+constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2;
+template <int EPL, bool FP8>
+__global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
                                                                   const __nv_bfloat16* __restrict__ x,
                                                                  const uint8_t* __restrict__ host,
                                                                  uint8_t* __restrict__ slots, int T,
@@ -151,8 +197,16 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, S
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();
 
-    // the first CTA to arrive plans the step; the others stage x meanwhile
-    if (threadIdx.x == 0) sh_planner = atomicAdd(&sync[P_TICKET], 1u) == 0;
+    // the first CTA to arrive plans the step; the others stage x meanwhile.
+    // Every CTA also registers the role its SM suggests and gets a rank in it.
+    __shared__ int sh_link_sm, sh_role_rank;
+    if (threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        sh_link_sm = (smid % kLinkSmEvery) == 0;
+        sh_role_rank = (int)atomicAdd(&sync[sh_link_sm ? R_LINK : R_HBM], 1u);
+        sh_planner = atomicAdd(&sync[P_TICKET], 1u) == 0;
+    }
     __syncthreads();
     if (sh_planner) {
         plan_block<EPL, kPlanCap>(L, s, logits, T, 1, err);
@@ -211,25 +265,31 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, S
     const long long link_items = miss_rows + (long long)count * copies_per;
     const long long hbm_items = (long long)(size - count) * s.I;
     const int G = gridDim.x;
-    unsigned smid;
-    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-    const bool link_cta = hbm_items == 0 ? true : link_items == 0 ? false : (smid % kLinkSmEvery) == 0;
     const int row_blocks = (s.H + kRowsD - 1) / kRowsD;
+    // roles: registration is complete long before the plan is (bounded wait)
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+            if (ld_acquire_u32(&sync[R_LINK]) + ld_acquire_u32(&sync[R_HBM]) >= (unsigned)G) break;
+            __nanosleep(64);
+        }
+    }
+    __syncthreads();
+    const int nL = (int)__ldcg(&sync[R_LINK]), nH = G - nL;
+    // split: link SMs stream the page-ins while HBM SMs run the resident experts;
+    // with no page-ins, no resident experts, or one group empty, every CTA does both
+    const bool split = link_items > 0 && hbm_items > 0 && nL > 0 && nH > 0;
+    const bool link_cta = split ? sh_link_sm != 0 : true;
+    const bool hbm_cta = split ? sh_link_sm == 0 : true;
+    const int rank = split ? sh_role_rank : (int)blockIdx.x;
+    const int link_ctas = split ? nL : G, hbm_ctas = split ? nH : G;
 
-    // Gate/up (and page-in) items from one role's queue: the link queue (page-in
-    // rows from the host store, then the rest of each paged row) or the HBM
-    // queue (resident members' rows).
-    auto run_queue = [&](const bool as_link) {
-        unsigned* q = &sync[as_link ? Q_LINK : Q_HBM];
-        unsigned* done = &sync[as_link ? D_LINK : D_HITS];
+    // Gate/up (and page-in) items of one role, strided over that role's CTAs:
+    // the link items (page-in rows from the host store, then the rest of each
+    // paged row) or the HBM items (resident members' rows).
+    auto run_items = [&](const bool as_link, int first_cta, int nctas) {
         const long long total = as_link ? link_items : hbm_items;
-        for (;;) {
-            long long base = 0;
-            if (lane == 0) base = atomicAdd(q, (unsigned)kGrab);
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (base >= total) break;
-            const long long end = min(base + kGrab, total);
-            for (long long item = base; item < end; ++item) {
+        {
+            for (long long item = (long long)first_cta * kWp + warp; item < total; item += (long long)nctas * kWp) {
                 if (as_link && item >= miss_rows) {
                     const long long c = item - miss_rows;
                     const int m = (int)(c / copies_per);
@@ -253,6 +313,38 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, S
                 const int mq = as_link ? (int)(item / s.I) : count + (int)(item / s.I);
                 const int n = (int)(item % s.I);
                 const int slot = sh_mslot[mq];
+                if constexpr (FP8) {
+                    uint8_t* slot_base = slots + (size_t)slot * s.stride;
+                    const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
+                    const int nch8 = s.H >> 4;
+                    int4 gv[CPLH8], uv[CPLH8];
+                    float sg[CPLH8], su[CPLH8];
+                    load_row_pair_fp8<CPLH8>(rbase, s, n, lane, nch8, as_link, gv, uv, sg, su);
+                    if (as_link) {
+                        uint8_t* gd = slot_base + s.w13_off + (size_t)n * s.H;
+                        uint8_t* ud = gd + (size_t)s.I * s.H;
+#pragma unroll
+                        for (int c = 0; c < CPLH8; ++c) {
+                            const int idx = lane + 32 * c;
+                            if (idx < nch8) {
+                                *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[c];
+                                *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[c];
+                            }
+                        }
+                    }
+                    for (int b0 = 0; b0 < nent; b0 += 32) {
+                        const int i = b0 + lane;
+                        unsigned mask = __ballot_sync(0xffffffffu, i < nent && sh_ekey[i] == slot);
+                        while (mask) {
+                            const int ei = b0 + __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const float hval = row_pair_h_fp8<CPLH8>(gv, uv, sg, su,
+                                                                     xbase + (size_t)(ei / s.k) * s.H * 2, lane, nch8);
+                            if (lane == 0) hbuf[(size_t)ei * s.I + n] = hval;
+                        }
+                    }
+                    continue;
+                }
                 uint8_t* slot_row = slots + (size_t)slot * s.stride + s.w13_off;
                 const uint8_t* g = (as_link ? host + (size_t)sh_mexp[mq] * s.stride + s.w13_off : slot_row) +
                                    (size_t)n * row_bytes;
@@ -292,48 +384,49 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, S
                     }
                 }
             }
-            __syncwarp();
-            if (lane == 0) {
-                __threadfence();
-                atomicAdd(done, (unsigned)(end - base));
-            }
         }
     };
 
     // ---- phase 1 ----
-    run_queue(link_cta);
+    if (link_cta) {
+        run_items(true, rank, link_ctas);
+        cta_arrive(&sync[D_LINK]);
+    }
+    if (hbm_cta) {
+        run_items(false, rank, hbm_ctas);
+        cta_arrive(&sync[D_HITS]);
+    }
+
+    // down projection rows m0.. of entry e into the merged buffer
+    auto down_entry = [&](int e, int m0) {
+        const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
+        const float we = __ldcg(L.topk_w + e);
+        if constexpr (FP8)
+            down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), hbuf + (size_t)e * s.I,
+                                 we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+        else
+            down_rows<CPLI>(sb + s.w2_off, hbuf + (size_t)e * s.I, we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+    };
 
     // ---- phase 2: down projections ----
-    if (!link_cta) {
+    if (hbm_cta) {
         // resident experts: as soon as every resident expert's h is done
-        cta_wait(&sync[D_HITS], (unsigned)hbm_items, err, &sh_flag);
+        cta_wait(&sync[D_HITS], (unsigned)hbm_ctas, err, &sh_flag);
         const long long items = (long long)sh_nhit * row_blocks;
-        for (;;) {
-            long long base = 0;
-            if (lane == 0) base = atomicAdd(&sync[Q_HDOWN], (unsigned)kGrab);
-            base = __shfl_sync(0xffffffffu, base, 0);
-            if (base >= items) break;
-            for (long long it = base; it < min(base + kGrab, items); ++it) {
-                const int e = sh_hit_list[it / row_blocks];
-                const int m0 = (int)(it % row_blocks) * kRowsD;
-                const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
-                down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, __ldcg(L.topk_w + e), m0, s.H, s.I,
-                                merged + (size_t)e * s.H, lane);
-            }
+        for (long long it = (long long)rank * kWp + warp; it < items; it += (long long)hbm_ctas * kWp) {
+            const int e = sh_hit_list[it / row_blocks];
+            const int m0 = (int)(it % row_blocks) * kRowsD;
+            down_entry(e, m0);
         }
-        // then help drain the link queue (nothing of ours is queued on this SM any more)
-        if (link_items > 0) run_queue(true);
     }
     // paged experts: once the link is drained (their h and their w2 rows)
-    cta_wait(&sync[D_LINK], (unsigned)link_items, err, &sh_flag);
+    cta_wait(&sync[D_LINK], (unsigned)link_ctas, err, &sh_flag);
     {
         const long long items = (long long)sh_nmiss * row_blocks;
         for (long long it = (long long)blockIdx.x * kWp + warp; it < items; it += (long long)G * kWp) {
             const int e = sh_miss_list[it / row_blocks];
             const int m0 = (int)(it % row_blocks) * kRowsD;
-            const uint8_t* w2 = slots + (size_t)sh_ekey[e] * s.stride + s.w2_off;
-            down_rows<CPLI>(w2, hbuf + (size_t)e * s.I, __ldcg(L.topk_w + e), m0, s.H, s.I, merged + (size_t)e * s.H,
-                            lane);
+            down_entry(e, m0);
         }
     }
     cta_arrive(&sync[S_DOWN]);
@@ -367,15 +460,18 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_bf16_kernel(LayerDev L, S
 int decode_fused_sync_words() { return S_NUM; }
 
 bool decode_fused_supported(const Shape& s, int T) {
-    return s.dtype == PE_BF16 && (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K &&
-           s.E <= kPlanCap && s.K <= kPlanCap && s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI &&
+    const bool fp8 = s.dtype == PE_FP8_BLOCK128;
+    const bool dims = fp8 ? (s.H <= 32 * 16 * CPLH8 && s.I <= 32 * 16 * CPLI8) : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
+    return (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K && s.E <= kPlanCap &&
+           s.K <= kPlanCap && dims &&
            (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
 }
 
 cudaError_t decode_setup_kernels() {
     cudaError_t e = cudaSuccess;
-#define PE_ATTR(N) \
-    if (!e) e = cudaFuncSetAttribute(decode_step_bf16_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
+#define PE_ATTR(N)                                                                                                   \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
     PE_ATTR(1) PE_ATTR(2) PE_ATTR(4) PE_ATTR(8)
 #undef PE_ATTR
     return e;
@@ -390,8 +486,12 @@ cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* 
     const int stage = meta + xbytes <= (size_t)kDynBudget;
     const size_t smem = meta + (stage ? xbytes : 0);
     const int epl = (s.E + 31) / 32;
-#define PE_DEC(N) \
-    return launch_pdl(decode_step_bf16_kernel<N>, grid, kThr, smem, st, L, s, logits, x, host_layer, slots_layer, T, hbuf, merged, out, sync, err, stage)
+    const bool fp8 = s.dtype == PE_FP8_BLOCK128;
+#define PE_DEC(N)                                                                                                   \
+    return fp8 ? launch_pdl(decode_step_kernel<N, true>, grid, kThr, smem, st, L, s, logits, x, host_layer, slots_layer, \
+                            T, hbuf, merged, out, sync, err, stage)                                                 \
+               : launch_pdl(decode_step_kernel<N, false>, grid, kThr, smem, st, L, s, logits, x, host_layer,          \
+                            slots_layer, T, hbuf, merged, out, sync, err, stage)
     if (epl <= 1) PE_DEC(1);
     if (epl <= 2) PE_DEC(2);
     if (epl <= 4) PE_DEC(4);
