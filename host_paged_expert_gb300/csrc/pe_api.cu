@@ -282,12 +282,12 @@ pe_status setup_prefill(pe_handle* h) {
     }
     {
         const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H * 2, stride};
-        const cuuint32_t b[3] = {64, 64, 1};
+        const cuuint32_t b[3] = {64, 128, 1};
         ok = ok && encode_bf16(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b);
     }
     {
         const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I * 2, stride};
-        const cuuint32_t b[3] = {64, 128, 1};
+        const cuuint32_t b[3] = {64, 256, 1};
         ok = ok && encode_bf16(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b);
     }
     if (!ok) return fail(h, PE_ERR_CUDA, "could not encode the prefill tensor maps");

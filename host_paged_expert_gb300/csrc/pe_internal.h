@@ -65,8 +65,8 @@ struct PrefillDev {
 struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
-    CUtensorMap w13;     // 3-D bf16 [L*K slots][2I][H], 64 x 64 x 1 boxes
-    CUtensorMap w2;      // 3-D bf16 [L*K slots][H][I], 64 x 128 x 1 boxes
+    CUtensorMap w13;     // 3-D bf16 [L*K slots][2I][H], 64 x 128 x 1 boxes
+    CUtensorMap w2;      // 3-D bf16 [L*K slots][H][I], 64 x 256 x 1 boxes
 };
 
 bool prefill_tc_supported(const Shape& s);

@@ -282,3 +282,29 @@ def test_prefill_runs_on_the_tensor_core_path(tiny):
     assert prof["decode_step"]["launches"] == 1 and prof["gemm_gateup"]["launches"] == 0
     assert prof["gateup_pagein"]["launches"] == 0 and prof["down"]["launches"] == 0
     m.close()
+
+
+def test_prefill_tiles_over_128_rows():
+    """Experts with more than 128 routed rows fill both 128-row halves of a
+    tensor-core tile (and, past 256 rows, several tiles); results match the
+    oracle and the K = E call bit for bit."""
+    _lib = _need_gpu()
+    s = synth.MoEShape(1, 4, 2, 2, 256, 128, "bf16")
+    w = synth.ExpertWeights(s, seed=13)
+    a = _lib.PagedMoE(s, max_tokens=320)
+    gu.load_stack(a, w)
+    b = _lib.PagedMoE(s.with_slots(4), max_tokens=320, store_owner=a)
+    o = omlp.PagedLayer(4, 2, 2, gu.expert_fn(w, 0))
+    for T in (70, 200, 320):
+        xb = synth.hidden_states((T,), s.hidden, seed=T, tag=21)
+        lg = synth.prefill_logits(1, 4, T, seed=T)[0]
+        x, l = gu.to_dev_bf16(xb), gu.to_dev_f32(lg)
+        a.profile_enable(True)
+        ya, yb = a.forward(0, x, l), b.forward(0, x, l)
+        assert a.profile_read()["gemm_gateup"]["launches"] >= 1
+        out, _, plan, ids, wts = o.step(xb, lg)
+        gu.check_plan(a.read_plan(0, T), plan, ids, wts)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), T
+        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"], T
+    b.close()
+    a.close()
