@@ -60,6 +60,9 @@ def workload(name: str):
     if name.startswith("prefill48_T"):
         t = int(name[len("prefill48_T"):])
         return base.with_slots(32), t, f"48 layers, H=2048, I=768, E=128, top-8, K=32, bf16, prefill chunks of {t} tokens"
+    if name.startswith("fp8prefill48_T"):
+        t = int(name[len("fp8prefill48_T"):])
+        return synth.STACK48_FP8, t, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, prefill chunks of {t} tokens"
     if name.startswith("fp8_48_b"):
         b = int(name[len("fp8_48_b"):])
         return synth.STACK48_FP8, b, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, batch {b}"
@@ -486,7 +489,7 @@ def run_prefill(args):
         kernels[name] = e
     line = {"metric": "paged-MoE prefill tok/s (48 layers, K resident)", "value": round(tok_s, 1), "unit": "tok/s",
             "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms / K, 3), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic",
             "config": {"workload": f"{args.workload}: {desc}", "chunks_cycled": nchunk},
             "clocks": clk.summary(),
             "page_in": {"per_layer_step": round(d["page_ins"] / (K * L), 2), "link_probe_gbs": [round(ce_gbs, 1), round(kn_gbs, 1)],
@@ -576,7 +579,7 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
-    if args.workload.startswith("prefill48_T"):
+    if args.workload.startswith(("prefill48_T", "fp8prefill48_T")):
         run_prefill(args)
         return
     r = run_ours(args, rank, world, local_rank)

@@ -22,10 +22,16 @@
 // The weights come straight from the slot table (a 3-D tensor map over
 // [slot][row][k]), so a page-in is all it takes to make them visible.
 //
+// Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) keep bf16
+// activations: TMA brings the code tile into a staging buffer, two converter
+// warps decode it, multiply by its block scale, round to bf16 and write it in
+// the 128-byte-swizzled layout the MMA reads; the MMA then runs as for bf16.
+//
 // Every row of an MMA tile is computed independently and always with the same
 // k order, so an entry's result does not depend on its tile-mates, its slot
 // or its wave: paged and unpaged prefill agree bit for bit.
 
+#include "fp8_device.cuh"
 #include "pe_device.cuh"
 #include "pe_internal.h"
 #include "tc_sm100.cuh"
@@ -33,13 +39,21 @@
 namespace pe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 3;
-constexpr int MT = 2 * BM;                   // rows of one tile: two M=128 MMAs
-constexpr int A_BYTES = BM * BK * 2;         // one 128-row half of the A tile
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES;
-constexpr int GEMM_SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring to 1024 B
-constexpr uint32_t kTmemCols = 2 * BN;       // one 128-column accumulator per half
+constexpr int BM = 128, BK = 64, STAGES = 3;
+constexpr int MT = 2 * BM;            // rows of one tile: two M=128 MMAs
+constexpr int A_BYTES = BM * BK * 2;  // one 128-row half of the A tile
+
+// Tile geometry per weight format.  Stage layout: [A half 0][A half 1]
+// [B tile, bf16, swizzled][FP8 only: code staging], every part 1024-aligned.
+template <bool FP8>
+struct Tile {
+    static constexpr int BN = FP8 ? 128 : 256;       // output columns (MMA N)
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int C_BYTES = FP8 ? BN * BK : 0;  // E4M3 codes of the B tile
+    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + C_BYTES;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring
+    static constexpr uint32_t TMEM_COLS = 2 * BN;    // one accumulator per 128-row half
+};
 
 // ---------------------------------------------------------------- align
 
@@ -121,14 +135,19 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const __nv_bfloat16
 //        h_perm[row, n0 + c] = bf16(SiLU(gate_c) * up_c), c < 128.
 // EPI 1: A = h_perm, B = w2 rows m0..m0+255,
 //        merged[entry, m0 + c] = w_entry * acc_c.
-template <int EPI>
+template <int EPI, bool FP8>
 __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                                               const __grid_constant__ CUtensorMap tmB, PrefillDev P,
-                                                              LayerDev L, Shape s, int n_tiles, int kblocks,
-                                                              float* __restrict__ merged, uint32_t* err) {
+                                                              LayerDev L, Shape s, const uint8_t* __restrict__ slots_all,
+                                                              int n_tiles, int kblocks, float* __restrict__ merged,
+                                                              uint32_t* err) {
+    using TL = Tile<FP8>;
+    constexpr int BN = TL::BN, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
+    constexpr uint32_t kTmemCols = TL::TMEM_COLS;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t conv_bar[STAGES];  // FP8: the bf16 B tile is written
     __shared__ __align__(8) uint64_t acc_bar;
     __shared__ uint32_t tmem_base_sh;
     pdl_wait();
@@ -144,6 +163,7 @@ __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_const
         for (int i = 0; i < STAGES; ++i) {
             tc::mbar_init(&full_bar[i], 1);
             tc::mbar_init(&empty_bar[i], 1);
+            tc::mbar_init(&conv_bar[i], 2);  // one arrive per converter warp
         }
         tc::mbar_init(&acc_bar, 1);
         tc::fence_barrier_init();
@@ -160,14 +180,16 @@ __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_const
         for (int kb = 0; kb < kblocks; ++kb) {
             const int st = kb % STAGES, use = kb / STAGES;
             if (use > 0 && !tc::mbar_wait(&empty_bar[st], (use - 1) & 1, err, PE_DEVERR_TIMEOUT)) break;
-            tc::mbar_arrive_expect_tx(&full_bar[st], two ? STAGE_BYTES : STAGE_BYTES - A_BYTES);
+            const int b_tx = FP8 ? TL::C_BYTES : B_BYTES;
+            tc::mbar_arrive_expect_tx(&full_bar[st], (two ? 2 * A_BYTES : A_BYTES) + b_tx);
             uint8_t* a = ring + st * STAGE_BYTES;
-            uint8_t* b = a + 2 * A_BYTES;
+            // bf16: the B tile itself; FP8: its codes, into the staging buffer
+            uint8_t* b = FP8 ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
             tc::tma_load_2d(a, &tmA, &full_bar[st], kb * BK, ti.x);
             if (two) tc::tma_load_2d(a + A_BYTES, &tmA, &full_bar[st], kb * BK, ti.x + BM);
             if (EPI == 0) {
                 tc::tma_load_3d(b, &tmB, &full_bar[st], kb * BK, n_tile * (BN / 2), ti.y);
-                tc::tma_load_3d(b + B_BYTES / 2, &tmB, &full_bar[st], kb * BK, s.I + n_tile * (BN / 2), ti.y);
+                tc::tma_load_3d(b + b_tx / 2, &tmB, &full_bar[st], kb * BK, s.I + n_tile * (BN / 2), ti.y);
             } else {
                 tc::tma_load_3d(b, &tmB, &full_bar[st], kb * BK, n_tile * BN, ti.y);
             }
@@ -176,7 +198,7 @@ __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_const
         constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
         for (int kb = 0; kb < kblocks; ++kb) {
             const int st = kb % STAGES, use = kb / STAGES;
-            if (!tc::mbar_wait(&full_bar[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
+            if (!tc::mbar_wait(FP8 ? &conv_bar[st] : &full_bar[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
             tc::fence_after_sync();
             const uint32_t a = tc::smem_u32(ring + st * STAGE_BYTES);
             const uint32_t b = a + 2 * A_BYTES;
@@ -189,6 +211,41 @@ __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_const
             tc::mma_commit(&empty_bar[st]);  // frees the stage once these MMAs are done
         }
         tc::mma_commit(&acc_bar);
+    } else if (FP8 && warp >= 2) {  // converters: E4M3 codes -> scaled bf16, swizzled
+        const int ct = threadIdx.x - 64;
+        const int Kdim = EPI == 0 ? s.H : s.I;
+        const int nbk = (Kdim + kFp8Block - 1) / kFp8Block;
+        const float* sc = reinterpret_cast<const float*>(slots_all + (size_t)ti.y * s.stride + (EPI == 0 ? s.s13_off : s.s2_off));
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const int st = kb % STAGES, use = kb / STAGES;
+            if (!tc::mbar_wait(&full_bar[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
+            uint8_t* bt = ring + st * STAGE_BYTES + 2 * A_BYTES;
+            const uint8_t* codes = bt + B_BYTES;
+            for (int q = ct; q < BN * (BK / 16); q += 64) {  // 16-code chunks: row r, chunk j
+                const int r = q >> 2, j = q & 3;
+                const int grow = EPI == 0 ? (r < BN / 2 ? n_tile * (BN / 2) + r : s.I + n_tile * (BN / 2) + r - BN / 2)
+                                          : n_tile * BN + r;
+                const float scale = __ldg(sc + (size_t)(grow / kFp8Block) * nbk + (kb * BK) / kFp8Block);
+                const int4 cv = *reinterpret_cast<const int4*>(codes + r * BK + j * 16);
+                const uint32_t w4[4] = {(uint32_t)cv.x, (uint32_t)cv.y, (uint32_t)cv.z, (uint32_t)cv.w};
+                uint32_t packed[8];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 lo = e4m3x2(w4[t]), hi = e4m3x2(w4[t] >> 16);
+                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(lo.x * scale, lo.y * scale);
+                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(hi.x * scale, hi.y * scale);
+                    packed[2 * t] = *reinterpret_cast<const uint32_t*>(&p0);
+                    packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
+                }
+                // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
+                uint8_t* row = bt + r * 128;
+                *reinterpret_cast<int4*>(row + (((2 * j) ^ (r & 7)) * 16)) = make_int4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<int4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) = make_int4(packed[4], packed[5], packed[6], packed[7]);
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&conv_bar[st]);
+        }
     }
     __syncwarp();
 
@@ -250,6 +307,11 @@ __global__ void __launch_bounds__(128, 1) prefill_gemm_kernel(const __grid_const
 }  // namespace
 
 bool prefill_tc_supported(const Shape& s) {
+    if (s.dtype == PE_FP8_BLOCK128) {
+        constexpr int BN = Tile<true>::BN;
+        return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
+    }
+    constexpr int BN = Tile<false>::BN;
     return s.dtype == PE_BF16 && s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
 
@@ -259,8 +321,17 @@ size_t prefill_max_rows(int max_entries, int K) {
 }
 
 cudaError_t prefill_setup_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
-    if (!e) e = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, GEMM_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(prefill_gemm_kernel<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tile<false>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<false>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<0, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<true>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_gemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<true>::SMEM);
     return e;
 }
 
@@ -272,16 +343,24 @@ cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const Prefil
 }
 
 cudaError_t launch_prefill_gemm(int which, const LayerDev& L, const Shape& s, const PrefillDev& P,
-                                const PrefillMaps& M, float* merged, uint32_t* err, cudaStream_t st) {
+                                const PrefillMaps& M, const uint8_t* slots_all, float* merged, uint32_t* err,
+                                cudaStream_t st) {
     const int m_tiles = P.max_tiles;
+    const bool fp8 = s.dtype == PE_FP8_BLOCK128;
+    const int bn = fp8 ? Tile<true>::BN : Tile<false>::BN;
+    const size_t smem = fp8 ? Tile<true>::SMEM : Tile<false>::SMEM;
     if (which == 0) {
-        const int n1 = s.I / (BN / 2);
-        return launch_pdl(prefill_gemm_kernel<0>, m_tiles * n1, 128, (size_t)GEMM_SMEM, st, M.x_perm, M.w13, P, L, s,
-                          n1, s.H / BK, merged, err);
+        const int n1 = s.I / (bn / 2);
+        return fp8 ? launch_pdl(prefill_gemm_kernel<0, true>, m_tiles * n1, 128, smem, st, M.x_perm, M.w13, P, L, s,
+                                slots_all, n1, s.H / BK, merged, err)
+                   : launch_pdl(prefill_gemm_kernel<0, false>, m_tiles * n1, 128, smem, st, M.x_perm, M.w13, P, L, s,
+                                slots_all, n1, s.H / BK, merged, err);
     }
-    const int n2 = s.H / BN;
-    return launch_pdl(prefill_gemm_kernel<1>, m_tiles * n2, 128, (size_t)GEMM_SMEM, st, M.h_perm, M.w2, P, L, s, n2,
-                      s.I / BK, merged, err);
+    const int n2 = s.H / bn;
+    return fp8 ? launch_pdl(prefill_gemm_kernel<1, true>, m_tiles * n2, 128, smem, st, M.h_perm, M.w2, P, L, s,
+                            slots_all, n2, s.I / BK, merged, err)
+               : launch_pdl(prefill_gemm_kernel<1, false>, m_tiles * n2, 128, smem, st, M.h_perm, M.w2, P, L, s,
+                            slots_all, n2, s.I / BK, merged, err);
 }
 
 }  // namespace pe

@@ -252,15 +252,22 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 tensor map with 128-byte swizzled boxes (inner box = 64 elements).
-bool encode_bf16(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
-                 const cuuint32_t* box) {
+// Tiled tensor map: bf16 with 128-byte swizzled boxes (inner box = 64
+// elements), or unswizzled bytes (FP8 codes, decoded in shared memory).
+bool encode_map(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                const cuuint32_t* box, bool bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint32_t es[3] = {1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
+              const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_bf16(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                 const cuuint32_t* box) {
+    return encode_map(m, base, rank, dims, strides, box, false);
 }
 
 // Tensor maps over the prefill workspace and the whole slot table.
@@ -280,15 +287,28 @@ pe_status setup_prefill(pe_handle* h) {
         const cuuint32_t b[2] = {64, 128};
         ok = ok && encode_bf16(&h->maps.h_perm, P.h_perm, 2, d, st, b);
     }
-    {
-        const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H * 2, stride};
-        const cuuint32_t b[3] = {64, 128, 1};
-        ok = ok && encode_bf16(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b);
-    }
-    {
-        const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I * 2, stride};
-        const cuuint32_t b[3] = {64, 256, 1};
-        ok = ok && encode_bf16(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b);
+    if (c.dtype == PE_FP8_BLOCK128) {  // code tiles, decoded to bf16 in shared memory
+        {
+            const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H, stride};
+            const cuuint32_t b[3] = {64, 64, 1};
+            ok = ok && encode_map(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b, true);
+        }
+        {
+            const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I, stride};
+            const cuuint32_t b[3] = {64, 128, 1};
+            ok = ok && encode_map(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b, true);
+        }
+    } else {
+        {
+            const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H * 2, stride};
+            const cuuint32_t b[3] = {64, 128, 1};
+            ok = ok && encode_bf16(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b);
+        }
+        {
+            const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I * 2, stride};
+            const cuuint32_t b[3] = {64, 256, 1};
+            ok = ok && encode_bf16(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b);
+        }
     }
     if (!ok) return fail(h, PE_ERR_CUDA, "could not encode the prefill tensor maps");
     cudaError_t e = prefill_setup_kernels();
@@ -578,11 +598,11 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             }
             {
                 ProfScope p(h, P_GEMM1, st);
-                e = launch_prefill_gemm(0, L, s, h->pre, h->maps, h->merged, h->err, st);
+                e = launch_prefill_gemm(0, L, s, h->pre, h->maps, h->slots, h->merged, h->err, st);
                 if (e) return cuda_fail(h, e, "gate/up GEMM kernel");
             }
             ProfScope p(h, P_GEMM2, st);
-            e = launch_prefill_gemm(1, L, s, h->pre, h->maps, h->merged, h->err, st);
+            e = launch_prefill_gemm(1, L, s, h->pre, h->maps, h->slots, h->merged, h->err, st);
             if (e) return cuda_fail(h, e, "down GEMM kernel");
         }
         ProfScope p(h, P_SUM, st);

@@ -65,8 +65,8 @@ struct PrefillDev {
 struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
-    CUtensorMap w13;     // 3-D bf16 [L*K slots][2I][H], 64 x 128 x 1 boxes
-    CUtensorMap w2;      // 3-D bf16 [L*K slots][H][I], 64 x 256 x 1 boxes
+    CUtensorMap w13;     // 3-D [L*K slots][2I][H]: bf16 64 x 128 x 1 boxes (swizzled); FP8 codes 64 x 64 x 1
+    CUtensorMap w2;      // 3-D [L*K slots][H][I]:  bf16 64 x 256 x 1 boxes (swizzled); FP8 codes 64 x 128 x 1
 };
 
 bool prefill_tc_supported(const Shape& s);
@@ -79,7 +79,8 @@ cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const Prefil
 // Prefill wave, part 2: which = 0 the gate/up GEMM (h), 1 the down GEMM
 // (merged entries of the wave; the top-k sum runs after the last wave).
 cudaError_t launch_prefill_gemm(int which, const LayerDev& L, const Shape& s, const PrefillDev& P,
-                                const PrefillMaps& M, float* merged, uint32_t* err, cudaStream_t st);
+                                const PrefillMaps& M, const uint8_t* slots_all, float* merged, uint32_t* err,
+                                cudaStream_t st);
 
 // Records the message pe_last_error(NULL) returns in this thread.
 void set_thread_error(const char* msg);

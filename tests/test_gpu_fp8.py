@@ -1,7 +1,8 @@
 """GPU parity for block-FP8 experts (E4M3 codes, fp32 scale per 128x128
 block, bf16 activations): a small stack through decode and multi-wave
-prefill, the stale-scale regression, and the full 48-layer FP8 stack (K=40,
-Zipf-skewed routing) at batch 1 and 4."""
+prefill, the tensor-core prefill with half-block tiles, the stale-scale
+regression, and the full 48-layer FP8 stack (K=40, Zipf-skewed routing) at
+decode batch 1 and 4 and one 512-token prefill chunk."""
 
 import numpy as np
 import pytest
@@ -56,6 +57,39 @@ def test_fp8_small_decode_and_prefill():
     a.close()
 
 
+def test_fp8_prefill_tensor_core():
+    """FP8 prefill on the tensor cores: each 64-row gate (and up) tile is half
+    of a 128-row scale block and each 64-wide K-step half of a scale column,
+    so every scale is applied to two tiles; I = 384 gives an odd number of
+    scale blocks per matrix.  T = 300 and 65 give ragged row tiles; the
+    GEMM kernels (not the GEMV fallback) must run."""
+    _lib = _need()
+    s = synth.MoEShape(1, 12, 2, 4, 512, 384, "fp8")
+    w = synth.ExpertWeights(s, seed=7)
+    a = _lib.PagedMoE(s, max_tokens=300)
+    gu.load_stack(a, w)
+    b = _lib.PagedMoE(s.with_slots(s.num_experts), max_tokens=300, store_owner=a)
+    a.profile_enable(True)
+    o = omlp.PagedLayer(s.num_experts, s.num_slots, s.top_k, gu.expert_fn(w, 0))
+    for T in (300, 65):
+        xb = synth.hidden_states((T,), s.hidden, seed=T, tag=11)
+        lg = synth.prefill_logits(1, s.num_experts, T, seed=T)[0]
+        x, l = gu.to_dev_bf16(xb), gu.to_dev_f32(lg)
+        ya, yb = a.forward(0, x, l), b.forward(0, x, l)
+        out, _, plan, ids, wts = o.step(xb, lg)
+        assert len(plan.waves) >= 2
+        gu.check_plan(a.read_plan(0, T), plan, ids, wts)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), T
+        err = gu.rel_l2(gu.out_f64(ya), out)
+        assert err <= TOL, (T, err)
+    prof = a.profile_read()
+    assert prof["gemm_gateup"]["launches"] >= 2 and prof["gemm_down"]["launches"] >= 2
+    assert prof["gateup"]["launches"] == 0
+    assert a.stats(0)["error_word"] == 0
+    b.close()
+    a.close()
+
+
 def test_fp8_scales_are_paged_with_codes():
     """Rescale one block of one expert's s13 and s2 in its host row: after the
     expert is paged in again the output follows the new scales (a slot never
@@ -90,7 +124,7 @@ def fp8_stack48():
     _lib = _need()
     s = synth.STACK48_FP8
     w = synth.ExpertWeights(s, seed=0)
-    owner = _lib.PagedMoE(s.with_slots(s.num_experts), max_tokens=4)
+    owner = _lib.PagedMoE(s.with_slots(s.num_experts), max_tokens=512)
     gu.load_stack(owner, w)
     yield s, w, owner
     owner.close()
@@ -121,5 +155,35 @@ def test_fp8_stack48_decode(fp8_stack48, B):
                 want = omlp.unpaged_layer(hs[t, l], lg[t, l], k, gu.expert_fn(w, l))
                 assert gu.rel_l2(gu.out_f64(ya), want) <= TOL, (t, l)
     torch.cuda.synchronize()
+    assert model.stats(-1)["error_word"] == 0
+    model.close()
+
+
+def test_fp8_stack48_prefill(fp8_stack48):
+    """One 512-token chunk through all 48 FP8 layers at K=40 on the
+    tensor-core path: plans bit-exact, paged == K=E bit for bit, two sampled
+    layers within the FP8 tolerance of the plain MoE layer."""
+    from host_paged_expert_gb300 import _lib
+
+    s, w, owner = fp8_stack48
+    L, E, k, K, T = s.num_layers, s.num_experts, s.top_k, s.num_slots, 512
+    lg = synth.prefill_logits(L, E, T, seed=1)
+    hs = synth.hidden_states((L, T), s.hidden, seed=1, tag=5)
+    model = _lib.PagedMoE(s, max_tokens=T, store_owner=owner)
+    owner.reset_residency()
+    model.profile_enable(True)
+    sims = [olru.ResidencySim(E, K) for _ in range(L)]
+    for l in range(L):
+        x, lgt = gu.to_dev_bf16(hs[l]), gu.to_dev_f32(lg[l])
+        ya = model.forward(l, x, lgt)
+        yb = owner.forward(l, x, lgt)
+        ids, wts, _ = route(lg[l], k)
+        gu.check_plan(model.read_plan(l, T), sims[l].step(ids), ids, wts)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), l
+        if l in (0, L - 1):
+            want = omlp.unpaged_layer(hs[l], lg[l], k, gu.expert_fn(w, l))
+            assert gu.rel_l2(gu.out_f64(ya), want) <= TOL, l
+    prof = model.profile_read()
+    assert prof["gemm_gateup"]["launches"] >= L
     assert model.stats(-1)["error_word"] == 0
     model.close()
