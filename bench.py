@@ -39,7 +39,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from host_paged_expert_gb300 import synth  # noqa: E402
+from host_paged_expert_gb300 import replicas, synth  # noqa: E402
 
 METRIC = "paged-MoE decode tok/s (48 layers, K resident)"
 _T0 = time.time()
@@ -201,12 +201,12 @@ def ncu_traffic(kernel: str, workload_name: str):
 # ------------------------------------------------------------------ our arm
 
 
-def run_ours(args, rank, world, local_rank):
+def run_ours(args, rep):
     import torch
 
     from host_paged_expert_gb300 import _lib
 
-    dev = local_rank
+    dev, world = rep.local_rank, rep.world
     torch.cuda.set_device(dev)
     shape, B, desc = workload(args.workload)
     if args.layers:
@@ -229,7 +229,7 @@ def run_ours(args, rank, world, local_rank):
     log("experts loaded into the host store")
     payload = model.layout["payload_bytes"]
 
-    lg_h, hs_h = make_inputs(shape, B, S)
+    lg_h, hs_h = make_inputs(shape, B, S, seed=replicas.input_seed(0, rep))
     stream = torch.cuda.Stream(device=dev)
     sp = stream.cuda_stream
     with torch.cuda.stream(stream):
@@ -267,8 +267,7 @@ def run_ours(args, rank, world, local_rank):
             launch_token()
 
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        replicas.barrier(rep)
 
     # ---- value pass
     with torch.cuda.stream(stream):
@@ -291,11 +290,8 @@ def run_ours(args, rank, world, local_rank):
         ms = ev0.elapsed_time(ev1)
         s1 = model.stats(-1)
     clocks = clk.summary()
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
-    tok_s = world * K * B / (ms * 1e-3)
+    ms = replicas.max_over_replicas(rep, ms, device=dev)
+    tok_s = replicas.job_rate(K * B, world, ms)
     log(f"value pass: {ms:.1f} ms for {K} steps -> {tok_s:.1f} tok/s")
     d = {n: s1[n] - s0[n] for n in ("steps", "waves", "entries", "distinct", "hits", "page_ins")}
 
@@ -328,11 +324,8 @@ def run_ours(args, rank, world, local_rank):
             b.record(stream)
             stream.synchronize()
             e_ms = a.elapsed_time(b)
-        if world > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt.item())
-        e2e = {"value": round(world * K * B / (e_ms * 1e-3), 2), "unit": "tok/s",
+        e_ms = replicas.max_over_replicas(rep, e_ms, device=dev)
+        e2e = {"value": round(replicas.job_rate(K * B, world, e_ms), 2), "unit": "tok/s",
                "h2d_bytes_per_step": L * B * (H * 2 + E * 4), "d2h_bytes_per_step": L * B * H * 2}
 
     # ---- trace pass: per-kernel events, per-layer counters, layer-step latency
@@ -540,8 +533,8 @@ def blas_threads():
     return os.cpu_count()
 
 
-def run_reference(args, rank, world):
-    if rank != 0:
+def run_reference(args, rep):
+    if not rep.is_root:  # the oracle arm runs once, on rank 0
         return
     shape, B, desc = workload(args.workload)
     weights = synth.ExpertWeights(shape, seed=0)
@@ -566,11 +559,10 @@ def run_reference(args, rank, world):
 
 def main():
     args = parse()
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    rep = replicas.from_env()
+    rank, world, local_rank = rep.rank, rep.world, rep.local_rank
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        run_reference(args, rep)
         return
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -578,14 +570,15 @@ def main():
 
     if world > 1:
         torch.cuda.set_device(local_rank)
-        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        replicas.init(rep, "nccl", device=torch.device("cuda", local_rank))
     if args.workload.startswith(("prefill48_T", "fp8prefill48_T")):
+        if world > 1:
+            raise SystemExit("prefill workloads time one replica; run them with --gpus 1")
         run_prefill(args)
         return
-    r = run_ours(args, rank, world, local_rank)
+    r = run_ours(args, rep)
     if rank != 0:
-        if world > 1:
-            torch.distributed.destroy_process_group()
+        replicas.finish(rep)
         return
     shape, B = r["shape"], r["B"]
     L = shape.num_layers
@@ -663,8 +656,7 @@ def main():
                                 "sample": f"first {steps} layer-steps (token-major) of this workload, "
                                           f"{sec:.1f} s, fp64 numpy"}
     print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    replicas.finish(rep)
 
 
 if __name__ == "__main__":
