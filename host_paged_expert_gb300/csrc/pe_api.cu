@@ -110,11 +110,11 @@ struct Carver {
 };
 
 enum ProfKind {
-    P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_ALIGN, P_GEMM1, P_GEMM2, P_DECODE, P_NUM
+    P_ROUTE = 0, P_PLAN, P_PAGEIN, P_GATEUP, P_GATEUP_PAGEIN, P_DOWN, P_SUM, P_ALIGN, P_PSTEP, P_DECODE, P_NUM
 };
-const char* kProfNames[P_NUM] = {"route",         "plan",        "pagein",       "gateup",
-                                 "gateup_pagein", "down",        "topk_sum",     "prefill_align",
-                                 "gemm_gateup",   "gemm_down",   "decode_step"};
+const char* kProfNames[P_NUM] = {"route",         "plan",     "pagein",        "gateup",
+                                 "gateup_pagein", "down",     "topk_sum",      "prefill_align",
+                                 "prefill_step",  "decode_step"};
 
 }  // namespace
 
@@ -179,14 +179,24 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
     PrefillDev pre = {};
     const bool tc = tc_enabled(c, r);
     if (tc) {
-        const size_t rows = prefill_max_rows((int)maxTk, K);
+        const size_t rows = prefill_max_rows((int)maxTk, E), tiles = rows / 128;
+        const size_t items = prefill_max_items(make_shape(c, r), tiles);
         pre.x_perm = cv.take<__nv_bfloat16>(rows * c.hidden);
         pre.h_perm = cv.take<__nv_bfloat16>(rows * c.intermediate);
         pre.perm = cv.take<int32_t>(rows);
-        pre.tiles = cv.take<int4>(rows / 128);
-        pre.counts = cv.take<int32_t>(4);
+        pre.tiles = cv.take<int4>(tiles);
+        pre.items = cv.take<int2>(items);
+        pre.members = cv.take<int4>(E);
+        pre.pin_member = cv.take<int32_t>(E);
+        pre.slot_need = cv.take<int32_t>(E);
+        pre.landed = cv.take<unsigned>(E);
+        pre.gu_done = cv.take<unsigned>(tiles);
+        pre.slot_done = cv.take<unsigned>(K);
+        pre.ctl = cv.take<unsigned>(2);
+        pre.counts = cv.take<int32_t>(8);
         pre.max_rows = (int)rows;
-        pre.max_tiles = (int)(rows / 128);
+        pre.max_tiles = (int)tiles;
+        pre.max_items = (int)items;
     }
     std::vector<LayerDev> layers(L);
     for (int l = 0; l < L; ++l) {
@@ -583,27 +593,18 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
     const bool fp8 = c.dtype == PE_FP8_BLOCK128;
     if (!pagein_fused && h->tc_ok) {
-        // prefill sizes: per wave, page-in then the two tensor-core GEMMs;
-        // every entry lands in the merged buffer, summed after the last wave
-        for (int w = 0; w < s.Wmax; ++w) {
-            {
-                ProfScope p(h, P_PAGEIN, st);
-                e = launch_pagein(L, s, host_layer, slots_layer, w, max_count, h->num_sms, st);
-                if (e) return cuda_fail(h, e, "page-in kernel");
-            }
-            {
-                ProfScope p(h, P_ALIGN, st);
-                e = launch_prefill_align(L, s, h->pre, x, layer * c.num_slots, w, T, h->num_sms, st);
-                if (e) return cuda_fail(h, e, "prefill align kernels");
-            }
-            {
-                ProfScope p(h, P_GEMM1, st);
-                e = launch_prefill_gemm(0, L, s, h->pre, h->maps, h->slots, h->merged, h->err, st);
-                if (e) return cuda_fail(h, e, "gate/up GEMM kernel");
-            }
-            ProfScope p(h, P_GEMM2, st);
-            e = launch_prefill_gemm(1, L, s, h->pre, h->maps, h->slots, h->merged, h->err, st);
-            if (e) return cuda_fail(h, e, "down GEMM kernel");
+        // prefill sizes: every wave's page-in and tensor-core GEMMs pipelined
+        // in one kernel; every entry lands in the merged buffer, summed after
+        {
+            ProfScope p(h, P_ALIGN, st);
+            e = launch_prefill_align(L, s, h->pre, x, layer * c.num_slots, T, h->num_sms, st);
+            if (e) return cuda_fail(h, e, "prefill align kernels");
+        }
+        {
+            ProfScope p(h, P_PSTEP, st);
+            e = launch_prefill_step(L, s, h->pre, h->maps, host_layer, h->slots, layer * c.num_slots, h->merged,
+                                    h->err, h->num_sms, st);
+            if (e) return cuda_fail(h, e, "prefill step kernel");
         }
         ProfScope p(h, P_SUM, st);
         e = launch_topk_sum(s, h->merged, y, T, st);

@@ -57,8 +57,16 @@ struct PrefillDev {
     __nv_bfloat16* h_perm;  // [max_rows][I]  A operand of the down GEMM
     int32_t* perm;          // [max_rows]     entry of each row, -1 = padding
     int4* tiles;            // [max_tiles]    (row0, slot in the whole table, valid rows, member)
-    int32_t* counts;        // [4]            tiles, rows of the current wave
-    int max_rows, max_tiles;
+    int2* items;            // [max_items]    GEMM queue: (tile, kind << 16 | column tile), kind 1 = down
+    int4* members;          // [E]            (expert, slot, wave, 1 if paged in) in queue order
+    int32_t* pin_member;    // [E]            page-ins in plan order -> member
+    int32_t* slot_need;     // [E]            GEMM tiles of the slot's earlier occupants before the page-in
+    unsigned* landed;       // [E]            landed page-in chunks per member
+    unsigned* gu_done;      // [max_tiles]    finished gate/up tiles per row tile
+    unsigned* slot_done;    // [K]            finished GEMM tiles per slot in this step
+    unsigned* ctl;          // [2]            GEMM ticket, abort word
+    int32_t* counts;        // [8]            tiles, rows, items, members, page-ins
+    int max_rows, max_tiles, max_items;
 };
 
 // TMA descriptors of the prefill path, encoded once at creation.
@@ -70,17 +78,19 @@ struct PrefillMaps {
 };
 
 bool prefill_tc_supported(const Shape& s);
-size_t prefill_max_rows(int max_entries, int K);
+size_t prefill_max_rows(int max_entries, int E);
+size_t prefill_max_items(const Shape& s, size_t max_tiles);
 cudaError_t prefill_setup_kernels();
-// Prefill wave, part 1: group the wave's entries by expert into 128-row
-// tiles and gather their token rows (align + gather kernels).
+// Prefill step, part 1 (after the planner): lay out every wave's members,
+// tiles, GEMM queue and page-in list, and gather the token rows (align +
+// gather kernels).
 cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const PrefillDev& P, const __nv_bfloat16* x,
-                                 int slot_base, int wave, int T, int num_sms, cudaStream_t st);
-// Prefill wave, part 2: which = 0 the gate/up GEMM (h), 1 the down GEMM
-// (merged entries of the wave; the top-k sum runs after the last wave).
-cudaError_t launch_prefill_gemm(int which, const LayerDev& L, const Shape& s, const PrefillDev& P,
-                                const PrefillMaps& M, const uint8_t* slots_all, float* merged, uint32_t* err,
-                                cudaStream_t st);
+                                 int slot_base, int T, int num_sms, cudaStream_t st);
+// Prefill step, part 2: every wave's page-in and tensor-core GEMMs in one
+// persistent kernel (merged entries; the top-k sum runs after it).
+cudaError_t launch_prefill_step(const LayerDev& L, const Shape& s, const PrefillDev& P, const PrefillMaps& M,
+                                const uint8_t* host_layer, uint8_t* slots_all, int slot_base, float* merged,
+                                uint32_t* err, int num_sms, cudaStream_t st);
 
 // Records the message pe_last_error(NULL) returns in this thread.
 void set_thread_error(const char* msg);
