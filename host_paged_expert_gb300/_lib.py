@@ -24,7 +24,8 @@ PE_BF16, PE_FP8_BLOCK128 = 0, 1
 PE_DEVERR_NAN_LOGIT, PE_DEVERR_NOT_LOADED, PE_DEVERR_PLAN = 1, 2, 4
 
 EXPORTS = [
-    "pe_required_device_bytes", "pe_get_row_layout", "pe_max_waves", "pe_create", "pe_create_shared",
+    "pe_required_device_bytes", "pe_slots_for_budget", "pe_get_row_layout", "pe_max_waves", "pe_create",
+    "pe_create_shared",
     "pe_load_host_expert", "pe_host_row", "pe_forward", "pe_stats", "pe_read_plan", "pe_read_residency",
     "pe_read_slot", "pe_reset_residency", "pe_probe_host_link", "pe_profile_enable", "pe_profile_read",
     "pe_destroy", "pe_last_error", "pe_expert_mlp_noalloc",
@@ -75,6 +76,8 @@ def lib() -> ctypes.CDLL:
     cfgp = POINTER(PEConfig)
     L.pe_required_device_bytes.argtypes = [cfgp]
     L.pe_required_device_bytes.restype = c_size_t
+    L.pe_slots_for_budget.argtypes = [cfgp, c_size_t]
+    L.pe_slots_for_budget.restype = c_int32
     L.pe_get_row_layout.argtypes = [cfgp, POINTER(PERowLayout)]
     L.pe_max_waves.argtypes = [cfgp, c_int32]
     L.pe_max_waves.restype = c_int32
@@ -120,6 +123,12 @@ def make_config(shape: MoEShape, max_tokens: int, device: int = 0) -> PEConfig:
 def required_device_bytes(shape: MoEShape, max_tokens: int) -> int:
     cfg = make_config(shape, max_tokens)
     return int(lib().pe_required_device_bytes(byref(cfg)))
+
+
+def slots_for_budget(shape: MoEShape, max_tokens: int, budget_bytes: int) -> int:
+    """Largest K whose whole arena fits the device-memory budget (0: none)."""
+    cfg = make_config(shape, max_tokens)
+    return int(lib().pe_slots_for_budget(byref(cfg), c_size_t(budget_bytes)))
 
 
 def row_layout(shape: MoEShape) -> dict:

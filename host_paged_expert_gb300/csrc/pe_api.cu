@@ -486,6 +486,26 @@ size_t pe_required_device_bytes(const pe_config* cfg) {
     return carve(nullptr, *cfg, r, nullptr);
 }
 
+int32_t pe_slots_for_budget(const pe_config* cfg, size_t budget_bytes) {
+    if (!cfg) return 0;
+    pe_config c = *cfg;
+    auto fits = [&](int32_t K) {
+        c.num_slots = K;
+        const size_t need = pe_required_device_bytes(&c);
+        return need != 0 && need <= budget_bytes;
+    };
+    int32_t lo = cfg->top_k, hi = cfg->num_experts;  // the arena grows with K
+    if (lo < 1 || hi < lo || !fits(lo)) return 0;
+    while (lo < hi) {
+        const int32_t mid = lo + (hi - lo + 1) / 2;
+        if (fits(mid))
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 pe_status pe_get_row_layout(const pe_config* cfg, pe_row_layout* out) {
     if (!cfg || !out) return PE_ERR_INVALID;
     if (!dtype_ok(cfg->dtype)) return PE_ERR_UNSUPPORTED_DTYPE;

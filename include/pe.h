@@ -132,6 +132,16 @@ typedef struct pe_handle pe_handle;
  * for up to max_tokens tokens.  Returns 0 for an invalid config.  Pure. */
 size_t pe_required_device_bytes(const pe_config* cfg);
 
+/* Slot count for a device-memory budget.  "Paged Experts" (SGLang docs),
+ * "Choosing K": the slot table competes with the rest of GPU memory, and one
+ * resident slot costs expert_bytes x num_moe_layers, so K is what the budget
+ * left for it allows.  Returns the largest K, top_k <= K <= num_experts, for
+ * which pe_required_device_bytes(cfg with num_slots = K) <= budget_bytes
+ * (the whole arena, slot table and workspace, is counted); 0 if even
+ * K = top_k does not fit or the config is invalid for every K.
+ * cfg->num_slots is ignored.  Pure. */
+int32_t pe_slots_for_budget(const pe_config* cfg, size_t budget_bytes);
+
 /* Row layout for a config (see pe_row_layout).  Pure. */
 pe_status pe_get_row_layout(const pe_config* cfg, pe_row_layout* out);
 

@@ -7,7 +7,10 @@ layers*top_k*expert_bytes over the host link.  At a measured decode rate the
 link can only have carried link_bw/tok_s bytes per token, which bounds the
 fraction of expert activations that can have missed; uniform random routing
 would miss 1 - K/E of them.  "Paged Experts" (SGLang docs, "Choosing K"): one
-resident slot costs expert_bytes * num_moe_layers of GPU memory.
+resident slot costs expert_bytes * num_moe_layers of GPU memory, so the
+number of slots is what the memory left for the slot table allows (the
+pages' formula itself did not survive extraction; the plainest reading is
+the floor of that budget over the per-slot cost, kept within top_k..E).
 """
 
 from __future__ import annotations
@@ -45,3 +48,14 @@ def max_miss_rate(link_bytes_per_s: float, tok_per_s: float, num_layers: int, to
 def random_miss_rate(num_slots: int, num_experts: int) -> float:
     """Miss fraction of uniform random routing with K of E experts resident."""
     return 1.0 - num_slots / num_experts
+
+
+def slots_for_budget(budget_bytes: float, fixed_bytes: float, per_slot_bytes: float, num_experts: int,
+                     top_k: int) -> int:
+    """K that a memory budget allows: floor((budget - fixed) / per_slot),
+    at most E; 0 when not even top_k slots fit (the layer needs K >= top_k)."""
+    if per_slot_bytes <= 0:
+        raise ValueError("per-slot bytes must be positive")
+    k = int((budget_bytes - fixed_bytes) // per_slot_bytes) if budget_bytes >= fixed_bytes else 0
+    k = min(k, num_experts)
+    return k if k >= top_k else 0

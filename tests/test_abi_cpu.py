@@ -110,3 +110,27 @@ def test_null_handle_calls_are_errors(L):
     assert L.pe_stats(None, -1, None) == _lib.PE_ERR_INVALID
     assert L.pe_load_host_expert(None, 0, 0, None, None, None, None) == _lib.PE_ERR_INVALID
     L.pe_destroy(None)
+
+
+def test_slots_for_budget(L):
+    """The library's K for a budget is the largest K whose whole arena fits,
+    and agrees within one slot with the oracle's floor formula (the arena's
+    small per-K plan buffers are the difference)."""
+    from oracle import sizing
+
+    s = synth.STACK48
+    T = 8
+    per_slot = s.num_layers * _lib.row_layout(s)["row_stride"]
+    need = {K: _lib.required_device_bytes(s.with_slots(K), T) for K in (8, 39, 40, 41, 128)}
+    assert _lib.slots_for_budget(s, T, need[40]) == 40
+    assert _lib.slots_for_budget(s, T, need[40] - 1) == 39
+    assert _lib.slots_for_budget(s, T, need[41] - 1) == 40
+    assert _lib.slots_for_budget(s, T, need[128] + 10**9) == 128
+    assert _lib.slots_for_budget(s, T, need[8] - 1) == 0
+    fixed = need[8] - 8 * per_slot
+    for budget in (need[8], 100e9, 200e9, 271e9, need[128] - 1):
+        k = _lib.slots_for_budget(s, T, int(budget))
+        assert _lib.required_device_bytes(s.with_slots(k), T) <= budget
+        if k < s.num_experts:
+            assert _lib.required_device_bytes(s.with_slots(k + 1), T) > budget
+        assert abs(k - sizing.slots_for_budget(budget, fixed, per_slot, s.num_experts, s.top_k)) <= 1

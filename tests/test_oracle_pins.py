@@ -185,3 +185,25 @@ def test_sizes_and_miss_bounds_match_pages():
     s = g["slot_mb"]
     assert round(sizing.slot_bytes(2.43e6, L) / 1e6) == s["int4_per_slot"]
     assert round(sizing.slot_bytes(4.72e6, L) / 1e6) == s["fp8_per_slot"]
+
+
+def test_slots_for_budget_closed_forms():
+    # floor of the budget left after the fixed bytes over the per-slot cost
+    assert sizing.slots_for_budget(1000 + 40 * 117, 1000, 117, 128, 8) == 40
+    assert sizing.slots_for_budget(1000 + 40 * 117 - 1, 1000, 117, 128, 8) == 39
+    assert sizing.slots_for_budget(10**12, 1000, 117, 128, 8) == 128   # never above E
+    assert sizing.slots_for_budget(1000 + 7 * 117, 1000, 117, 128, 8) == 0   # below top_k: no layer
+    assert sizing.slots_for_budget(500, 1000, 117, 128, 8) == 0
+    with pytest.raises(ValueError):
+        sizing.slots_for_budget(1, 0, 0, 4, 1)
+
+
+def test_slots_for_budget_pages_example():
+    g = pins.golden("page_numbers.json")["choosing_k_example"]
+    slot = g["per_slot_mb"] * 1e6
+    # the page's K = 92 slots at 117 MB each is 10.76 GB, inside the 0.88 x 16 GB static budget
+    table = g["num_slots"] * slot
+    assert round(table / 1e9, 2) == 10.76
+    assert table <= g["mem_fraction_static"] * g["gpu_gb"] * 1e9
+    assert sizing.slots_for_budget(table, 0, slot, g["num_experts"], 8) == g["num_slots"]
+    assert sizing.slots_for_budget(table - 1, 0, slot, g["num_experts"], 8) == g["num_slots"] - 1
