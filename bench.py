@@ -604,10 +604,10 @@ def main():
                     "bytes_per_token": int(d["page_ins"] / args.steps * r["payload"]),
                     "random_routing_miss_rate": round(1.0 - shape.num_slots / shape.num_experts, 4),
                     # the largest per-entry miss rate this run's token rate allows over the probed
-                    # link if every miss moved a whole expert (the pages' upper bound, batch 1)
+                    # link if every missed entry moved a whole expert (the pages' upper bound)
                     "max_miss_rate_for_rate": round(
                         max(r["link"]["copy_engine_gbs"], r["link"]["kernel_gbs"]) * 1e9 / (r["tok_s"] / world)
-                        / (L * shape.top_k * B * r["payload"]), 4),
+                        / (L * shape.top_k * r["payload"]), 4),
                     "link_probe_gbs": r["link"]},
         "setup_s": round(r["t_load"], 1),
     }
