@@ -173,12 +173,22 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
 
 
-def kernel_source_hash():
+# The sources each timed kernel is compiled from: a DRAM-traffic record is
+# reported only while these still hash to the value it was captured on.
+KERNEL_SOURCES = {
+    "decode_step": ("k_decode.cu", "plan_block.cuh", "pe_device.cuh", "fp8_device.cuh", "pe_internal.h"),
+    "prefill_step": ("k_prefill.cu", "tc_sm100.cuh", "pe_device.cuh", "fp8_device.cuh", "pe_internal.h"),
+}
+
+
+def kernel_source_hash(kernel: str):
+    files = KERNEL_SOURCES.get(kernel)
+    if not files:
+        return None
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "host_paged_expert_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".h")):
-            h.update(open(os.path.join(csrc, n), "rb").read())
+    for n in files:
+        h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -191,7 +201,7 @@ def ncu_traffic(kernel: str, workload_name: str):
     try:
         d = json.load(open(p))
         e = d.get(workload_name, {}).get(kernel)
-        if e and e.get("source_hash") == kernel_source_hash():
+        if e and e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         return None
