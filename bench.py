@@ -63,6 +63,12 @@ def workload(name: str):
     if name.startswith("fp8prefill48_T"):
         t = int(name[len("fp8prefill48_T"):])
         return synth.STACK48_FP8, t, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, prefill chunks of {t} tokens"
+    if name.startswith("int4_48_b"):
+        b = int(name[len("int4_48_b"):])
+        return synth.STACK48_INT4, b, f"48 layers, H=2048, I=768, E=128, top-8, K=92, GPTQ int4 (group 128), batch {b}"
+    if name.startswith("int4prefill48_T"):
+        t = int(name[len("int4prefill48_T"):])
+        return synth.STACK48_INT4, t, f"48 layers, H=2048, I=768, E=128, top-8, K=92, GPTQ int4 (group 128), prefill chunks of {t} tokens"
     if name.startswith("fp8_48_b"):
         b = int(name[len("fp8_48_b"):])
         return synth.STACK48_FP8, b, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, batch {b}"
@@ -380,17 +386,19 @@ def run_ours(args, rep):
 
 
 def launches_per_layer_step(shape, B):
+    """Kernel launches pe_forward makes for one decode layer-step of B tokens
+    (the path choice the library makes from shapes and B)."""
     from host_paged_expert_gb300 import _lib
 
     ent = B * shape.top_k
-    if (shape.dtype == "bf16" and ent <= min(64, shape.num_slots) and shape.num_experts <= 256
-            and shape.num_slots <= 256 and shape.hidden <= 2048 and shape.intermediate <= 1024):
-        return 1  # the whole decode step is one kernel
+    if (ent <= min(64, shape.num_slots) and shape.num_experts <= 256 and shape.num_slots <= 256
+            and shape.hidden <= 2048 and shape.intermediate <= 1024):
+        return 1  # the whole decode step is one kernel (every format)
     Wm = _lib.max_waves(shape, B)
-    n = 1 + 3 * Wm + (1 if Wm > 1 else 0)
-    if B > 32:
-        n += 1
-    return n
+    route = 1 if B > 32 else 0
+    if ent > 64:  # the pipelined prefill step: route, plan, align, gather, step, top-k sum
+        return 5 + route
+    return route + 1 + 2 * Wm + (1 if Wm > 1 else 0)  # plan, per wave gate/up+page-in and down, sum
 
 
 # ------------------------------------------------------------------ prefill workload
@@ -583,7 +591,7 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         replicas.init(rep, "nccl", device=torch.device("cuda", local_rank))
-    if args.workload.startswith(("prefill48_T", "fp8prefill48_T")):
+    if args.workload.startswith(("prefill48_T", "fp8prefill48_T", "int4prefill48_T")):
         if world > 1:
             raise SystemExit("prefill workloads time one replica; run them with --gpus 1")
         run_prefill(args)

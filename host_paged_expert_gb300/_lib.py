@@ -20,7 +20,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpe.so")
 
 PE_OK, PE_ERR_INVALID, PE_ERR_UNSUPPORTED_DTYPE, PE_ERR_HOST_ALLOC, PE_ERR_CUDA, PE_ERR_RANGE, PE_ERR_ARENA = range(7)
-PE_BF16, PE_FP8_BLOCK128 = 0, 1
+PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ = 0, 1, 2
+_DTYPE = {"bf16": PE_BF16, "fp8": PE_FP8_BLOCK128, "int4": PE_INT4_GPTQ}
 PE_DEVERR_NAN_LOGIT, PE_DEVERR_NOT_LOADED, PE_DEVERR_PLAN = 1, 2, 4
 
 EXPORTS = [
@@ -116,7 +117,7 @@ class PEError(RuntimeError):
 
 def make_config(shape: MoEShape, max_tokens: int, device: int = 0) -> PEConfig:
     return PEConfig(shape.num_layers, shape.num_experts, shape.top_k, shape.num_slots, shape.hidden,
-                    shape.intermediate, PE_BF16 if shape.dtype == "bf16" else PE_FP8_BLOCK128, max_tokens,
+                    shape.intermediate, _DTYPE[shape.dtype], max_tokens,
                     device)
 
 
@@ -208,8 +209,9 @@ class PagedMoE:
         w2 = np.ascontiguousarray(row["w2"])
         s13 = row.get("s13")
         s2 = row.get("s2")
-        s13 = None if s13 is None else np.ascontiguousarray(s13, dtype=np.float32)
-        s2 = None if s2 is None else np.ascontiguousarray(s2, dtype=np.float32)
+        sdt = np.float16 if self.shape.dtype == "int4" else np.float32
+        s13 = None if s13 is None else np.ascontiguousarray(s13, dtype=sdt)
+        s2 = None if s2 is None else np.ascontiguousarray(s2, dtype=sdt)
         self._check(self._L.pe_load_host_expert(
             self.handle, layer, expert, w13.ctypes.data, w2.ctypes.data,
             None if s13 is None else s13.ctypes.data, None if s2 is None else s2.ctypes.data))

@@ -1,0 +1,177 @@
+// GPTQ int4 device helpers shared by every int4 kernel: code decoding, the
+// 32-code dot products, the gate/up row pair of one expert row and the down
+// rows.  A weight is (q - 8) * s with q a 4-bit code and s the fp16 scale of
+// its output row and group of 128 inputs.  A 16-byte chunk holds 32 codes of
+// one row (input 2j in the low nibble of byte j) and never crosses a group,
+// so each lane decodes its chunk, forms the chunk's dot product and adds it
+// scaled by the chunk's group scale.  Every int4 kernel computes a value with
+// these functions in the same order, so all paths agree bit for bit.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "pe_device.cuh"
+#include "pe_internal.h"
+
+namespace pe {
+
+// q - 8 for nibble i of a 32-bit word, exactly: 2^23 + q as a float, minus
+// 2^23 + 8.
+__device__ __forceinline__ float i4_val(uint32_t w, int i) {
+    return __int_as_float(0x4B000000u | ((w >> (4 * i)) & 0xFu)) - 8388616.0f;
+}
+
+__device__ __forceinline__ float i4_bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float i4_bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// sum_{e<32} (q_e - 8) * x_e in input order: 32 codes against 32 bf16 values.
+__device__ __forceinline__ float dot32_int4_bf16(int4 w, const int4 (&x)[4]) {
+    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+    float p = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            p = fmaf(i4_val(wv[q], 2 * i), i4_bf_lo(xv[i]), p);
+            p = fmaf(i4_val(wv[q], 2 * i + 1), i4_bf_hi(xv[i]), p);
+        }
+    }
+    return p;
+}
+
+// sum_{e<32} (q_e - 8) * h_e in input order: 32 codes against 32 fp32 values.
+__device__ __forceinline__ float dot32_int4_f32(int4 w, const float4 (&h)[8]) {
+    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+    float p = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float4 a = h[2 * q], b = h[2 * q + 1];
+        p = fmaf(i4_val(wv[q], 0), a.x, p);
+        p = fmaf(i4_val(wv[q], 1), a.y, p);
+        p = fmaf(i4_val(wv[q], 2), a.z, p);
+        p = fmaf(i4_val(wv[q], 3), a.w, p);
+        p = fmaf(i4_val(wv[q], 4), b.x, p);
+        p = fmaf(i4_val(wv[q], 5), b.y, p);
+        p = fmaf(i4_val(wv[q], 6), b.z, p);
+        p = fmaf(i4_val(wv[q], 7), b.w, p);
+    }
+    return p;
+}
+
+__device__ __forceinline__ float ld_half(const __half* p) { return __half2float(__ldg(p)); }
+__device__ __forceinline__ float ldcg_half(const __half* p) {
+    return __half2float(__ushort_as_half(__ldcg(reinterpret_cast<const unsigned short*>(p))));
+}
+
+// h = SiLU(gate . x) * (up . x) for one int4 gate/up row pair held by the
+// warp (chunk c of lane l covers codes 32*(l + 32c) .. +31, scaled by sg[c],
+// su[c]).
+template <int CPL>
+__device__ __forceinline__ float row_pair_h_int4(const int4 (&gv)[CPL], const int4 (&uv)[CPL], const float (&sg)[CPL],
+                                                 const float (&su)[CPL], const uint8_t* xr, int lane, int nchunk) {
+    float ag = 0.f, au = 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        if (idx < nchunk) {
+            int4 x[4];
+#pragma unroll
+            for (int v = 0; v < 4; ++v) x[v] = *reinterpret_cast<const int4*>(xr + 64 * (size_t)idx + 16 * v);
+            ag = fmaf(sg[c], dot32_int4_bf16(gv[c], x), ag);
+            au = fmaf(su[c], dot32_int4_bf16(uv[c], x), au);
+        }
+    }
+    ag = warp_sum(ag);
+    au = warp_sum(au);
+    return __fmul_rn(silu(ag), au);
+}
+
+// Loads a gate/up row pair (codes and the lane's group scales) of expert row
+// `base` (host row or slot).  stream_host selects the no-L1 load path;
+// l2_only reads codes and scales past L1 (slots written in the same kernel).
+template <int CPL>
+__device__ __forceinline__ void load_row_pair_int4(const uint8_t* base, const Shape& s, int n, int lane, int nchunk,
+                                                   bool stream_host, bool l2_only, int4 (&gv)[CPL], int4 (&uv)[CPL],
+                                                   float (&sg)[CPL], float (&su)[CPL]) {
+    const size_t rb = (size_t)s.H / 2;
+    const uint8_t* g = base + s.w13_off + (size_t)n * rb;
+    const uint8_t* u = g + (size_t)s.I * rb;
+    const int ng = s.H / kInt4Group;
+    const __half* sc = reinterpret_cast<const __half*>(base + s.s13_off);
+    const __half* sgr = sc + (size_t)n * ng;
+    const __half* sur = sc + (size_t)(s.I + n) * ng;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+        if (idx < nchunk) {
+            const int grp = (idx * 32) / kInt4Group;
+            if (stream_host) {
+                gv[c] = ld_nc_na(g + 16 * (size_t)idx);
+                uv[c] = ld_nc_na(u + 16 * (size_t)idx);
+                sg[c] = ld_half(sgr + grp);
+                su[c] = ld_half(sur + grp);
+            } else if (l2_only) {
+                gv[c] = __ldcg(reinterpret_cast<const int4*>(g + 16 * (size_t)idx));
+                uv[c] = __ldcg(reinterpret_cast<const int4*>(u + 16 * (size_t)idx));
+                sg[c] = ldcg_half(sgr + grp);
+                su[c] = ldcg_half(sur + grp);
+            } else {
+                gv[c] = ldg16(g + 16 * (size_t)idx);
+                uv[c] = ldg16(u + 16 * (size_t)idx);
+                sg[c] = ld_half(sgr + grp);
+                su[c] = ld_half(sur + grp);
+            }
+        } else {
+            gv[c] = uv[c] = make_int4(0, 0, 0, 0);
+            sg[c] = su[c] = 0.f;
+        }
+    }
+}
+
+// p = w * (down_m . h) for ROWS rows m0.. of one entry, written to out_row
+// (or returned in p_out when it is not null).  The down rows' codes are
+// [H, I/2] bytes, their scales [H, I/128] fp16.  CPL = 16-byte chunks (32
+// codes) of an I-long row per lane.  l2_only reads past L1.
+template <int CPL, int ROWS>
+__device__ __forceinline__ void down_rows_int4(const uint8_t* w2, const __half* s2, const float* h, float wj, int m0,
+                                               int H, int I, bool l2_only, float* out_row, float* p_out, int lane) {
+    const int nchunk = I >> 5;
+    const size_t rb = (size_t)I / 2;
+    const int ng = I / kInt4Group;
+    int4 wv[ROWS][CPL];
+    float sc[ROWS][CPL];
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const int idx = lane + 32 * c;
+            const bool ok = m0 + r < H && idx < nchunk;
+            const uint8_t* p = w2 + (size_t)(m0 + r) * rb + 16 * (size_t)idx;
+            const __half* sp = s2 + (size_t)(m0 + r) * ng + (idx * 32) / kInt4Group;
+            wv[r][c] = ok ? (l2_only ? __ldcg(reinterpret_cast<const int4*>(p)) : ldg16(p)) : make_int4(0, 0, 0, 0);
+            sc[r][c] = ok ? (l2_only ? ldcg_half(sp) : ld_half(sp)) : 0.f;
+        }
+    float4 hv[CPL][8];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+        const int idx = lane + 32 * c;
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            hv[c][v] = idx < nchunk ? __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int r = 0; r < ROWS; ++r) {
+        float d = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c)
+            if (lane + 32 * c < nchunk) d = fmaf(sc[r][c], dot32_int4_f32(wv[r][c], hv[c]), d);
+        d = warp_sum(d);
+        const float p = __fmul_rn(wj, d);
+        if (p_out) p_out[r] = p;
+        if (lane == 0 && out_row && m0 + r < H) out_row[m0 + r] = p;
+    }
+}
+
+}  // namespace pe

@@ -32,6 +32,7 @@
 // the two paths give the same bits and the output still equals K = E.
 
 #include "fp8_device.cuh"
+#include "int4_device.cuh"
 #include "pe_device.cuh"
 #include "pe_internal.h"
 #include "plan_block.cuh"
@@ -173,10 +174,12 @@ __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2
 // Dynamic shared memory: [member experts K][member slots K][entry keys nent]
 // [entry member nent] padded to 4 ints, then the tokens' x when it fits.
 // Chunks per lane cover H <= 2048 and I <= 1024 (bf16: 8 and 4 chunks of 8
-// values, FP8: 4 and 2 chunks of 16 codes); chunks past the row are skipped,
+// values, FP8: 4 and 2 chunks of 16 codes, int4: 2 and 1 chunks of 32 codes);
+// chunks past the row are skipped,
 // so the arithmetic is that of the exact chunk counts.
-constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2;
-template <int EPL, bool FP8>
+constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
+// FMT: the expert format (PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ).
+template <int EPL, int FMT>
 __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
                                                                   const __nv_bfloat16* __restrict__ x,
                                                                  const uint8_t* __restrict__ host,
@@ -313,7 +316,39 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                 const int mq = as_link ? (int)(item / s.I) : count + (int)(item / s.I);
                 const int n = (int)(item % s.I);
                 const int slot = sh_mslot[mq];
-                if constexpr (FP8) {
+                if constexpr (FMT == PE_INT4_GPTQ) {
+                    uint8_t* slot_base = slots + (size_t)slot * s.stride;
+                    const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
+                    const int nch4 = s.H >> 5;
+                    int4 gv[CPLH4], uv[CPLH4];
+                    float sg[CPLH4], su[CPLH4];
+                    load_row_pair_int4<CPLH4>(rbase, s, n, lane, nch4, as_link, false, gv, uv, sg, su);
+                    if (as_link) {
+                        uint8_t* gd = slot_base + s.w13_off + (size_t)n * (s.H / 2);
+                        uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
+#pragma unroll
+                        for (int c = 0; c < CPLH4; ++c) {
+                            const int idx = lane + 32 * c;
+                            if (idx < nch4) {
+                                *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[c];
+                                *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[c];
+                            }
+                        }
+                    }
+                    for (int b0 = 0; b0 < nent; b0 += 32) {
+                        const int i = b0 + lane;
+                        unsigned mask = __ballot_sync(0xffffffffu, i < nent && sh_ekey[i] == slot);
+                        while (mask) {
+                            const int ei = b0 + __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const float hval = row_pair_h_int4<CPLH4>(gv, uv, sg, su,
+                                                                      xbase + (size_t)(ei / s.k) * s.H * 2, lane, nch4);
+                            if (lane == 0) hbuf[(size_t)ei * s.I + n] = hval;
+                        }
+                    }
+                    continue;
+                }
+                if constexpr (FMT == PE_FP8_BLOCK128) {
                     uint8_t* slot_base = slots + (size_t)slot * s.stride;
                     const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
                     const int nch8 = s.H >> 4;
@@ -401,7 +436,11 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     auto down_entry = [&](int e, int m0) {
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
         const float we = __ldcg(L.topk_w + e);
-        if constexpr (FP8)
+        if constexpr (FMT == PE_INT4_GPTQ)
+            down_rows_int4<CPLI4, kRowsD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
+                                          hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true, merged + (size_t)e * s.H,
+                                          nullptr, lane);
+        else if constexpr (FMT == PE_FP8_BLOCK128)
             down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), hbuf + (size_t)e * s.I,
                                  we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
         else
@@ -460,8 +499,9 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
 int decode_fused_sync_words() { return S_NUM; }
 
 bool decode_fused_supported(const Shape& s, int T) {
-    const bool fp8 = s.dtype == PE_FP8_BLOCK128;
-    const bool dims = fp8 ? (s.H <= 32 * 16 * CPLH8 && s.I <= 32 * 16 * CPLI8) : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
+    const bool dims = s.dtype == PE_FP8_BLOCK128 ? (s.H <= 32 * 16 * CPLH8 && s.I <= 32 * 16 * CPLI8)
+                      : s.dtype == PE_INT4_GPTQ ? (s.H <= 32 * 32 * CPLH4 && s.I <= 32 * 32 * CPLI4)
+                                                : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
     return (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K && s.E <= kPlanCap &&
            s.K <= kPlanCap && dims &&
            (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
@@ -470,8 +510,9 @@ bool decode_fused_supported(const Shape& s, int T) {
 cudaError_t decode_setup_kernels() {
     cudaError_t e = cudaSuccess;
 #define PE_ATTR(N)                                                                                                   \
-    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
-    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_FP8_BLOCK128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
     PE_ATTR(1) PE_ATTR(2) PE_ATTR(4) PE_ATTR(8)
 #undef PE_ATTR
     return e;
@@ -486,17 +527,19 @@ cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* 
     const int stage = meta + xbytes <= (size_t)kDynBudget;
     const size_t smem = meta + (stage ? xbytes : 0);
     const int epl = (s.E + 31) / 32;
-    const bool fp8 = s.dtype == PE_FP8_BLOCK128;
+#define PE_DEC1(N, F)                                                                                               \
+    launch_pdl(decode_step_kernel<N, F>, grid, kThr, smem, st, L, s, logits, x, host_layer, slots_layer, T, hbuf,     \
+               merged, out, sync, err, stage)
 #define PE_DEC(N)                                                                                                   \
-    return fp8 ? launch_pdl(decode_step_kernel<N, true>, grid, kThr, smem, st, L, s, logits, x, host_layer, slots_layer, \
-                            T, hbuf, merged, out, sync, err, stage)                                                 \
-               : launch_pdl(decode_step_kernel<N, false>, grid, kThr, smem, st, L, s, logits, x, host_layer,          \
-                            slots_layer, T, hbuf, merged, out, sync, err, stage)
+    return s.dtype == PE_FP8_BLOCK128 ? PE_DEC1(N, PE_FP8_BLOCK128)                                                 \
+           : s.dtype == PE_INT4_GPTQ  ? PE_DEC1(N, PE_INT4_GPTQ)                                                    \
+                                      : PE_DEC1(N, PE_BF16)
     if (epl <= 1) PE_DEC(1);
     if (epl <= 2) PE_DEC(2);
     if (epl <= 4) PE_DEC(4);
     PE_DEC(8);
 #undef PE_DEC
+#undef PE_DEC1
 }
 
 }  // namespace pe

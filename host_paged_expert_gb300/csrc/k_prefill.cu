@@ -38,12 +38,14 @@
 // TMEM, and eight warps run the epilogue from TMEM.  The weights come straight
 // from the slot table (a 3-D tensor map over [slot][row][k]).
 //
-// Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) keep bf16
-// activations: TMA brings the code tile into a staging buffer, six converter
-// warps decode it, multiply by its block scale, round to bf16 and write it in
-// the 128-byte-swizzled layout the MMA reads; the MMA then runs as for bf16.
-// A tile's scales (one row of blocks for each of its gate, up or down row
-// ranges) are staged in shared memory once per tile.
+// Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) and GPTQ
+// int4 experts (4-bit codes, zero point 8, one fp16 scale per output row and
+// 128 inputs) keep bf16 activations: TMA brings the code tile into a staging
+// buffer, six converter warps decode it, multiply by its scale, round to bf16
+// and write it in the 128-byte-swizzled layout the MMA reads; the MMA then
+// runs as for bf16.  A tile's scales are staged in shared memory once per
+// tile (FP8: one row of blocks for each of its gate, up or down row ranges;
+// int4: every row's group scales).
 //
 // Every row of an MMA tile is computed independently and always with the same
 // k order, so an entry's result does not depend on its tile-mates, its slot,
@@ -54,6 +56,8 @@
 // raises the step's abort word, after which every wait gives up at once; the
 // work behind a failed wait is skipped but still counted as done, so the
 // kernel always ends.
+
+#include <cuda_fp16.h>
 
 #include "fp8_device.cuh"
 #include "pe_device.cuh"
@@ -70,17 +74,20 @@ constexpr int kStepThreads = 256;
 constexpr int kLinkEvery = 4;         // CTAs 0, 4, 8, ... of the step stream the host link
 constexpr int kLinkUnroll = 16;
 constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 64 KiB per item
-constexpr int kConvWarps = 6;         // FP8: warps 2..7 decode the weight tiles
-constexpr int kMaxScaleCols = 64;     // FP8: K / 128 of either GEMM (H, I <= 8192)
+constexpr int kConvWarps = 6;         // FP8 / int4: warps 2..7 decode the weight tiles
+constexpr int kMaxScaleCols = 64;     // FP8 / int4: K / 128 of either GEMM (H, I <= 8192)
 constexpr uint32_t kSpin = 1u << 22;  // polls, >= 128 ns apart
 
-// Tile geometry per weight format.  Stage layout: [A half 0][A half 1]
-// [B tile, bf16, swizzled][FP8 only: code staging], every part 1024-aligned.
-template <bool FP8>
+// Tile geometry per weight format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ).
+// Stage layout: [A half 0][A half 1][B tile, bf16, swizzled][quantised
+// formats only: code staging], every part 1024-aligned.
+template <int FMT>
 struct Tile {
-    static constexpr int BN = FP8 ? 128 : 256;         // output columns (MMA N)
+    static constexpr int BN = FMT == PE_BF16 ? 256 : 128;  // output columns (MMA N)
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int C_BYTES = FP8 ? BN * BK : 0;  // E4M3 codes of the B tile
+    static constexpr int C_BYTES = FMT == PE_FP8_BLOCK128 ? BN * BK          // E4M3 codes of the B tile
+                                   : FMT == PE_INT4_GPTQ  ? BN * BK / 2      // int4 codes of the B tile
+                                                          : 0;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + C_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring
     static constexpr uint32_t TMEM_COLS = 2 * BN;      // one accumulator per 128-row half
@@ -293,21 +300,23 @@ struct Ring {
     uint8_t* base;
     uint64_t* full;
     uint64_t* empty;
-    uint64_t* conv;  // FP8: the bf16 B tile of the stage is written
+    uint64_t* conv;  // quantised formats: the bf16 B tile of the stage is written
     uint64_t* acc;
     float* scale;    // FP8: [2][kMaxScaleCols] block scales of the tile's two row ranges
+    __half* scale4;  // int4: [BN][kMaxScaleCols] group scales of the tile's rows
 };
 
 // One tile.  EPI 0: A = x_perm, B = w13 (gate rows n0.. and up rows I+n0..,
 //   BN/2 each), h_perm[row, n0 + c] = bf16(SiLU(gate_c) * up_c), c < BN/2.
 // EPI 1: A = h_perm, B = w2 rows m0..m0+BN-1, merged[entry, m0 + c] = w * acc_c.
 // kb0 = k-steps this CTA ran before (ring position); acc_phase = tiles before, mod 2.
-template <int EPI, bool FP8>
+template <int EPI, int FMT>
 __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, const Ring& R, int4 ti,
                                           int n_tile, int kblocks, uint32_t kb0, uint32_t acc_phase, uint32_t tmem,
                                           const PrefillDev& P, const LayerDev& L, const Shape& s,
                                           const uint8_t* slots_all, float* __restrict__ merged, uint32_t* err) {
-    using TL = Tile<FP8>;
+    using TL = Tile<FMT>;
+    constexpr bool QUANT = FMT != PE_BF16;
     constexpr int BN = TL::BN, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool two = ti.z > BM;  // the tile's second 128-row half is used
@@ -316,25 +325,27 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensor
         for (int kb = 0; kb < kblocks; ++kb) {
             const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
             if (use > 0 && !tc::mbar_wait(&R.empty[st], (use - 1) & 1, err, PE_DEVERR_TIMEOUT)) break;
-            const int b_tx = FP8 ? TL::C_BYTES : B_BYTES;
+            const int b_tx = QUANT ? TL::C_BYTES : B_BYTES;
             tc::mbar_arrive_expect_tx(&R.full[st], (two ? 2 * A_BYTES : A_BYTES) + b_tx);
             uint8_t* a = R.base + st * STAGE_BYTES;
-            // bf16: the B tile itself; FP8: its codes, into the staging buffer
-            uint8_t* b = FP8 ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
+            // bf16: the B tile itself; quantised: its codes, into the staging buffer
+            uint8_t* b = QUANT ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
+            // the weight map's inner coordinate counts bytes for int4 (two codes each)
+            const int kx = FMT == PE_INT4_GPTQ ? kb * (BK / 2) : kb * BK;
             tc::tma_load_2d(a, tmA, &R.full[st], kb * BK, ti.x);
             if (two) tc::tma_load_2d(a + A_BYTES, tmA, &R.full[st], kb * BK, ti.x + BM);
             if (EPI == 0) {
-                tc::tma_load_3d(b, tmB, &R.full[st], kb * BK, n_tile * (BN / 2), ti.y);
-                tc::tma_load_3d(b + b_tx / 2, tmB, &R.full[st], kb * BK, s.I + n_tile * (BN / 2), ti.y);
+                tc::tma_load_3d(b, tmB, &R.full[st], kx, n_tile * (BN / 2), ti.y);
+                tc::tma_load_3d(b + b_tx / 2, tmB, &R.full[st], kx, s.I + n_tile * (BN / 2), ti.y);
             } else {
-                tc::tma_load_3d(b, tmB, &R.full[st], kb * BK, n_tile * BN, ti.y);
+                tc::tma_load_3d(b, tmB, &R.full[st], kx, n_tile * BN, ti.y);
             }
         }
     } else if (threadIdx.x == 32) {  // MMA issuer
         constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
         for (int kb = 0; kb < kblocks; ++kb) {
             const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
-            if (!tc::mbar_wait(FP8 ? &R.conv[st] : &R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
+            if (!tc::mbar_wait(QUANT ? &R.conv[st] : &R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
             tc::fence_after_sync();
             const uint32_t a = tc::smem_u32(R.base + st * STAGE_BYTES);
             const uint32_t b = a + 2 * A_BYTES;
@@ -347,7 +358,56 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensor
             tc::mma_commit(&R.empty[st]);  // frees the stage once these MMAs are done
         }
         tc::mma_commit(R.acc);
-    } else if (FP8 && warp >= 2) {  // converters: E4M3 codes -> scaled bf16, swizzled
+    } else if (FMT == PE_INT4_GPTQ && warp >= 2) {  // converters: int4 codes -> scaled bf16, swizzled
+        constexpr int NCT = kConvWarps * 32;
+        const int ct = threadIdx.x - 64;
+        const int Kdim = EPI == 0 ? s.H : s.I;
+        const int ng = Kdim / kInt4Group;
+        {
+            // every row of the tile has its own group scales; they live in
+            // the slot, which this kernel's link CTAs write: read through L2
+            const unsigned short* sc = reinterpret_cast<const unsigned short*>(
+                slots_all + (size_t)ti.y * s.stride + (EPI == 0 ? s.s13_off : s.s2_off));
+            for (int i = ct; i < BN * ng; i += NCT) {
+                const int r = i / ng, c = i - r * ng;
+                const int grow = EPI == 0 ? (r < BN / 2 ? n_tile * (BN / 2) + r : s.I + n_tile * (BN / 2) + r - BN / 2)
+                                          : n_tile * BN + r;
+                R.scale4[r * kMaxScaleCols + c] = __ushort_as_half(__ldcg(sc + (size_t)grow * ng + c));
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
+        }
+        for (int kb = 0; kb < kblocks; ++kb) {
+            const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
+            if (!tc::mbar_wait(&R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
+            uint8_t* bt = R.base + st * STAGE_BYTES + 2 * A_BYTES;
+            const uint8_t* codes = bt + B_BYTES;
+            const int grp = (kb * BK) / kInt4Group;
+            for (int q = ct; q < BN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
+                const int r = q >> 2, j = q & 3;
+                const float scale = __half2float(R.scale4[r * kMaxScaleCols + grp]);
+                const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
+                uint32_t packed[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {  // codes 2t, 2t+1 of the chunk
+                    const uint32_t w = t < 4 ? cv.x : cv.y;
+                    const int sh = 8 * (t & 3);
+                    const float v0 = (float)(int)((w >> sh) & 0xFu) - 8.f;
+                    const float v1 = (float)(int)((w >> (sh + 4)) & 0xFu) - 8.f;
+                    const __nv_bfloat162 pv = __floats2bfloat162_rn(v0 * scale, v1 * scale);
+                    packed[t] = *reinterpret_cast<const uint32_t*>(&pv);
+                }
+                // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
+                uint8_t* row = bt + r * 128;
+                *reinterpret_cast<int4*>(row + (((2 * j) ^ (r & 7)) * 16)) =
+                    make_int4(packed[0], packed[1], packed[2], packed[3]);
+                *reinterpret_cast<int4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) =
+                    make_int4(packed[4], packed[5], packed[6], packed[7]);
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&R.conv[st]);
+        }
+    } else if (FMT == PE_FP8_BLOCK128 && warp >= 2) {  // converters: E4M3 codes -> scaled bf16, swizzled
         constexpr int NCT = kConvWarps * 32;
         const int ct = threadIdx.x - 64;
         const int Kdim = EPI == 0 ? s.H : s.I;
@@ -458,20 +518,21 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensor
 
 // ---------------------------------------------------------------- step kernel
 
-template <bool FP8>
+template <int FMT>
 __global__ void __launch_bounds__(kStepThreads, 1)
     prefill_step_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmH,
                         const __grid_constant__ CUtensorMap tmW13, const __grid_constant__ CUtensorMap tmW2,
                         PrefillDev P, LayerDev L, Shape s, const uint8_t* __restrict__ host_layer,
                         uint8_t* __restrict__ slots_all, int slot_base, int n1, int n2, unsigned nchunk,
                         float* __restrict__ merged, uint32_t* err) {
-    using TL = Tile<FP8>;
+    using TL = Tile<FMT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(8) uint64_t conv_bar[STAGES];
     __shared__ __align__(8) uint64_t acc_bar;
-    __shared__ float sh_scale[FP8 ? 2 * kMaxScaleCols : 1];
+    __shared__ float sh_scale[FMT == PE_FP8_BLOCK128 ? 2 * kMaxScaleCols : 1];
+    __shared__ __half sh_scale4[FMT == PE_INT4_GPTQ ? Tile<FMT>::BN * kMaxScaleCols : 1];
     __shared__ uint32_t tmem_base_sh;
     __shared__ int2 sh_item;
     __shared__ int sh_ok;
@@ -485,7 +546,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     Ring R{reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)), full_bar,
-           empty_bar, conv_bar, &acc_bar, sh_scale};
+           empty_bar, conv_bar, &acc_bar, sh_scale, sh_scale4};
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             tc::mbar_init(&full_bar[i], 1);
@@ -532,11 +593,11 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         const int4 ti = P.tiles[it.x];
         if (sh_ok) {
             if (!down) {
-                gemm_tile<0, FP8>(&tmX, &tmW13, R, ti, n, s.H / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
+                gemm_tile<0, FMT>(&tmX, &tmW13, R, ti, n, s.H / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
                                   merged, err);
                 kb_ring += s.H / BK;
             } else {
-                gemm_tile<1, FP8>(&tmH, &tmW2, R, ti, n, s.I / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
+                gemm_tile<1, FMT>(&tmH, &tmW2, R, ti, n, s.I / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
                                   merged, err);
                 kb_ring += s.I / BK;
             }
@@ -553,7 +614,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tmem, TL::TMEM_COLS);
 }
 
-int step_bn(const Shape& s) { return s.dtype == PE_FP8_BLOCK128 ? Tile<true>::BN : Tile<false>::BN; }
+int step_bn(const Shape& s) { return s.dtype == PE_BF16 ? Tile<PE_BF16>::BN : Tile<PE_FP8_BLOCK128>::BN; }
 int step_n1(const Shape& s) { return s.I / (step_bn(s) / 2); }
 int step_n2(const Shape& s) { return s.H / step_bn(s); }
 unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkChunk - 1) / kLinkChunk); }
@@ -561,9 +622,8 @@ unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkCh
 }  // namespace
 
 bool prefill_tc_supported(const Shape& s) {
-    if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128) return false;
-    if (s.dtype == PE_FP8_BLOCK128 && (s.H > kMaxScaleCols * kFp8Block || s.I > kMaxScaleCols * kFp8Block))
-        return false;
+    if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128 && s.dtype != PE_INT4_GPTQ) return false;
+    if (s.dtype != PE_BF16 && (s.H > kMaxScaleCols * 128 || s.I > kMaxScaleCols * 128)) return false;
     const int BN = step_bn(s);
     return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
@@ -578,11 +638,14 @@ size_t prefill_max_rows(int max_entries, int E) {
 size_t prefill_max_items(const Shape& s, size_t max_tiles) { return max_tiles * (size_t)(step_n1(s) + step_n2(s)); }
 
 cudaError_t prefill_setup_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(prefill_step_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Tile<false>::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(prefill_step_kernel<PE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Tile<PE_BF16>::SMEM);
     if (!e)
-        e = cudaFuncSetAttribute(prefill_step_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Tile<true>::SMEM);
+        e = cudaFuncSetAttribute(prefill_step_kernel<PE_FP8_BLOCK128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<PE_FP8_BLOCK128>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_step_kernel<PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<PE_INT4_GPTQ>::SMEM);
     return e;
 }
 
@@ -600,11 +663,13 @@ cudaError_t launch_prefill_step(const LayerDev& L, const Shape& s, const Prefill
     const int grid = num_sms < kLinkEvery + 1 ? kLinkEvery + 1 : num_sms;  // at least one CTA of each role
     const int n1 = step_n1(s), n2 = step_n2(s);
     const unsigned nchunk = step_nchunk(s);
-    if (s.dtype == PE_FP8_BLOCK128)
-        return launch_pdl(prefill_step_kernel<true>, grid, kStepThreads, Tile<true>::SMEM, st, M.x_perm, M.h_perm,
-                          M.w13, M.w2, P, L, s, host_layer, slots_all, slot_base, n1, n2, nchunk, merged, err);
-    return launch_pdl(prefill_step_kernel<false>, grid, kStepThreads, Tile<false>::SMEM, st, M.x_perm, M.h_perm,
-                      M.w13, M.w2, P, L, s, host_layer, slots_all, slot_base, n1, n2, nchunk, merged, err);
+#define PE_STEP(F)                                                                                          \
+    return launch_pdl(prefill_step_kernel<F>, grid, kStepThreads, Tile<F>::SMEM, st, M.x_perm, M.h_perm, M.w13, M.w2, \
+                      P, L, s, host_layer, slots_all, slot_base, n1, n2, nchunk, merged, err)
+    if (s.dtype == PE_FP8_BLOCK128) PE_STEP(PE_FP8_BLOCK128);
+    if (s.dtype == PE_INT4_GPTQ) PE_STEP(PE_INT4_GPTQ);
+    PE_STEP(PE_BF16);
+#undef PE_STEP
 }
 
 }  // namespace pe

@@ -29,7 +29,7 @@ constexpr int kRouteInlineMaxTokens = 32;  // plan CTA routes up to one token pe
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool dtype_ok(int d) { return d == PE_BF16 || d == PE_FP8_BLOCK128; }
+bool dtype_ok(int d) { return d == PE_BF16 || d == PE_FP8_BLOCK128 || d == PE_INT4_GPTQ; }
 
 // Returns "" when the config is valid, else the reason.
 std::string validate(const pe_config& c) {
@@ -45,21 +45,32 @@ std::string validate(const pe_config& c) {
     if (c.device < 0) return "device must be >= 0";
     if (c.dtype == PE_FP8_BLOCK128 && (c.hidden % kFp8Block || c.intermediate % kFp8Block))
         return "block-FP8 needs hidden and intermediate to be multiples of 128";
+    if (c.dtype == PE_INT4_GPTQ && (c.hidden % kInt4Group || c.intermediate % kInt4Group))
+        return "int4 needs hidden and intermediate to be multiples of the 128-input group";
     return "";
 }
 
 void row_layout(const pe_config& c, pe_row_layout* r) {
     const uint64_t H = (uint64_t)c.hidden, I = (uint64_t)c.intermediate;
-    const uint64_t esz = c.dtype == PE_BF16 ? 2 : 1;
     std::memset(r, 0, sizeof(*r));
+    // bytes per 2 weights: bf16 4, E4M3 2, int4 1
+    const uint64_t per2 = c.dtype == PE_BF16 ? 4 : c.dtype == PE_FP8_BLOCK128 ? 2 : 1;
+    uint64_t s13 = 0, s2 = 0;
+    if (c.dtype == PE_FP8_BLOCK128) {  // fp32 per 128x128 block
+        s13 = 4 * ((2 * I + 127) / 128) * ((H + 127) / 128);
+        s2 = 4 * ((H + 127) / 128) * ((I + 127) / 128);
+    } else if (c.dtype == PE_INT4_GPTQ) {  // fp16 per output row and 128 inputs
+        s13 = 2 * (2 * I) * ((H + kInt4Group - 1) / kInt4Group);
+        s2 = 2 * H * ((I + kInt4Group - 1) / kInt4Group);
+    }
     r->w13_offset = 0;
-    r->w13_bytes = 2 * I * H * esz;
+    r->w13_bytes = I * H * per2;
     r->s13_offset = align_up(r->w13_offset + r->w13_bytes, 128);
-    r->s13_bytes = c.dtype == PE_BF16 ? 0 : 4 * ((2 * I + 127) / 128) * ((H + 127) / 128);
+    r->s13_bytes = s13;
     r->w2_offset = align_up(r->s13_offset + r->s13_bytes, 128);
-    r->w2_bytes = H * I * esz;
+    r->w2_bytes = H * I * per2 / 2;
     r->s2_offset = align_up(r->w2_offset + r->w2_bytes, 128);
-    r->s2_bytes = c.dtype == PE_BF16 ? 0 : 4 * ((H + 127) / 128) * ((I + 127) / 128);
+    r->s2_bytes = s2;
     r->payload_bytes = r->w13_bytes + r->s13_bytes + r->w2_bytes + r->s2_bytes;
     r->row_stride = align_up(r->s2_offset + r->s2_bytes, 256);
 }
@@ -297,7 +308,18 @@ pe_status setup_prefill(pe_handle* h) {
         const cuuint32_t b[2] = {64, 128};
         ok = ok && encode_bf16(&h->maps.h_perm, P.h_perm, 2, d, st, b);
     }
-    if (c.dtype == PE_FP8_BLOCK128) {  // code tiles, decoded to bf16 in shared memory
+    if (c.dtype == PE_INT4_GPTQ) {  // packed int4 code tiles (two codes per byte), decoded in shared memory
+        {
+            const cuuint64_t d[3] = {H / 2, 2 * I, nslots}, st[2] = {H / 2, stride};
+            const cuuint32_t b[3] = {32, 64, 1};
+            ok = ok && encode_map(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b, true);
+        }
+        {
+            const cuuint64_t d[3] = {I / 2, H, nslots}, st[2] = {I / 2, stride};
+            const cuuint32_t b[3] = {32, 128, 1};
+            ok = ok && encode_map(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b, true);
+        }
+    } else if (c.dtype == PE_FP8_BLOCK128) {  // code tiles, decoded to bf16 in shared memory
         {
             const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H, stride};
             const cuuint32_t b[3] = {64, 64, 1};
@@ -530,20 +552,20 @@ pe_status pe_create_shared(const pe_config* cfg, void* dev_arena, size_t arena_b
 }
 
 pe_status pe_load_host_expert(pe_handle* h, int32_t layer, int32_t expert, const void* w13,
-                              const void* w2, const float* s13, const float* s2) {
+                              const void* w2, const void* s13, const void* s2) {
     if (!h) return PE_ERR_INVALID;
     if (!h->owns_store) return fail(h, PE_ERR_INVALID, "load experts through the handle that owns the host store");
     if (layer < 0 || layer >= h->cfg.num_layers || expert < 0 || expert >= h->cfg.num_experts)
         return fail(h, PE_ERR_RANGE, "layer or expert out of range");
     if (!w13 || !w2) return fail(h, PE_ERR_INVALID, "w13 and w2 must not be NULL");
-    const bool fp8 = h->cfg.dtype == PE_FP8_BLOCK128;
-    if (fp8 && (!s13 || !s2)) return fail(h, PE_ERR_INVALID, "block-FP8 experts need s13 and s2");
-    if (!fp8 && (s13 || s2)) return fail(h, PE_ERR_INVALID, "bf16 experts take no scales");
+    const bool scaled = h->cfg.dtype != PE_BF16;
+    if (scaled && (!s13 || !s2)) return fail(h, PE_ERR_INVALID, "quantised experts need s13 and s2");
+    if (!scaled && (s13 || s2)) return fail(h, PE_ERR_INVALID, "bf16 experts take no scales");
     const pe_row_layout& r = h->row;
     uint8_t* row = h->store_host + ((size_t)layer * h->cfg.num_experts + expert) * r.row_stride;
     std::memcpy(row + r.w13_offset, w13, r.w13_bytes);
     std::memcpy(row + r.w2_offset, w2, r.w2_bytes);
-    if (fp8) {
+    if (scaled) {
         std::memcpy(row + r.s13_offset, s13, r.s13_bytes);
         std::memcpy(row + r.s2_offset, s2, r.s2_bytes);
     }
@@ -611,7 +633,7 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // decode sizes page in inside the gate/up kernel; the choice depends on T
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
-    const bool fp8 = c.dtype == PE_FP8_BLOCK128;
+    const int fmt = c.dtype;  // PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ
     if (!pagein_fused && h->tc_ok) {
         // prefill sizes: every wave's page-in and tensor-core GEMMs pipelined
         // in one kernel; every entry lands in the merged buffer, summed after
@@ -634,7 +656,10 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     for (int w = 0; w < s.Wmax; ++w) {
         if (pagein_fused) {
             ProfScope p(h, P_GATEUP_PAGEIN, st);
-            e = fp8 ? launch_gateup_pagein_fp8(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
+            e = fmt == PE_FP8_BLOCK128
+                    ? launch_gateup_pagein_fp8(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                : fmt == PE_INT4_GPTQ
+                    ? launch_gateup_pagein_int4(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
                     : launch_gateup_pagein(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st);
             if (e) return cuda_fail(h, e, "gate/up + page-in kernel");
         } else {
@@ -645,14 +670,18 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             }
             {
                 ProfScope p(h, P_GATEUP, st);
-                e = fp8 ? launch_gateup_fp8(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
-                        : launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
+                e = fmt == PE_FP8_BLOCK128 ? launch_gateup_fp8(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                    : fmt == PE_INT4_GPTQ  ? launch_gateup_int4(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                                           : launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
                 if (e) return cuda_fail(h, e, "gate/up kernel");
             }
         }
         {
             ProfScope p(h, P_DOWN, st);
-            e = fp8 ? launch_down_fp8(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
+            e = fmt == PE_FP8_BLOCK128
+                    ? launch_down_fp8(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
+                : fmt == PE_INT4_GPTQ
+                    ? launch_down_int4(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
                     : launch_down(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st);
             if (e) return cuda_fail(h, e, "down kernel");
         }

@@ -16,6 +16,7 @@ constexpr int kMaxTopK = 32;       // one warp lane per chosen expert
 constexpr int kPlanMaxThreads = 1024;
 constexpr int kFusedMaxEntries = 64;  // decode: one warp scans a wave's entries per weight row
 constexpr int kFp8Block = 128;
+constexpr int kInt4Group = 128;  // GPTQ int4: inputs per scale
 
 enum Counter { C_STEPS = 0, C_WAVES, C_ENTRIES, C_DISTINCT, C_HITS, C_PAGE_INS, C_COLD, C_NUM };
 
@@ -73,8 +74,10 @@ struct PrefillDev {
 struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
-    CUtensorMap w13;     // 3-D [L*K slots][2I][H]: bf16 64 x 128 x 1 boxes (swizzled); FP8 codes 64 x 64 x 1
-    CUtensorMap w2;      // 3-D [L*K slots][H][I]:  bf16 64 x 256 x 1 boxes (swizzled); FP8 codes 64 x 128 x 1
+    CUtensorMap w13;     // 3-D [L*K slots][2I][H]: bf16 64 x 128 x 1 boxes (swizzled); FP8 codes 64 x 64 x 1;
+                         //   int4 [..][2I][H/2 bytes] 32 x 64 x 1
+    CUtensorMap w2;      // 3-D [L*K slots][H][I]:  bf16 64 x 256 x 1 boxes (swizzled); FP8 codes 64 x 128 x 1;
+                         //   int4 [..][H][I/2 bytes] 32 x 128 x 1
 };
 
 bool prefill_tc_supported(const Shape& s);
@@ -146,6 +149,16 @@ cudaError_t launch_gateup_fp8(const LayerDev& L, const Shape& s, const __nv_bflo
 cudaError_t launch_down_fp8(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
                             int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
                             int num_sms, cudaStream_t st);
+// GPTQ int4 counterparts of the three decode kernels above.
+cudaError_t launch_gateup_pagein_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                      const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
+                                      float* hbuf, int num_sms, cudaStream_t st);
+cudaError_t launch_gateup_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                               const uint8_t* slots_layer, int wave, int T, float* hbuf, int num_sms,
+                               cudaStream_t st);
+cudaError_t launch_down_int4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
+                             int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
+                             int num_sms, cudaStream_t st);
 // out[t] = sum_j merged[t, j] in entry order, rounded to bf16.
 cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
                             cudaStream_t st);

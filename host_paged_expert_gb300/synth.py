@@ -53,7 +53,8 @@ class MoEShape:
     num_slots: int
     hidden: int
     intermediate: int
-    dtype: str = "bf16"  # "bf16" or "fp8" (E4M3, 128x128 blocks, fp32 scales)
+    dtype: str = "bf16"  # "bf16", "fp8" (E4M3, 128x128 blocks, fp32 scales) or
+    # "int4" (GPTQ: 4-bit codes, zero point 8, fp16 scale per output row and 128 inputs)
     block: int = 128
 
     def with_slots(self, k: int) -> "MoEShape":
@@ -71,26 +72,33 @@ class MoEShape:
     @property
     def s13_shape(self) -> tuple[int, int]:
         b = self.block
+        if self.dtype == "int4":
+            return (2 * self.intermediate, -(-self.hidden // b))
         return (-(-2 * self.intermediate // b), -(-self.hidden // b))
 
     @property
     def s2_shape(self) -> tuple[int, int]:
         b = self.block
+        if self.dtype == "int4":
+            return (self.hidden, -(-self.intermediate // b))
         return (-(-self.hidden // b), -(-self.intermediate // b))
 
     @property
     def expert_bytes(self) -> int:
-        """Payload bytes of one expert (weights plus, for FP8, its scales)."""
+        """Payload bytes of one expert (weights plus, for FP8 and int4, its scales)."""
         if self.dtype == "bf16":
             return 2 * (self.w13_elems + self.w2_elems)
         s13 = self.s13_shape[0] * self.s13_shape[1]
         s2 = self.s2_shape[0] * self.s2_shape[1]
+        if self.dtype == "int4":
+            return (self.w13_elems + self.w2_elems) // 2 + 2 * (s13 + s2)
         return self.w13_elems + self.w2_elems + 4 * (s13 + s2)
 
 
 TINY = MoEShape(1, 16, 2, 6, 256, 128, "bf16")
 STACK48 = MoEShape(48, 128, 8, 32, 2048, 768, "bf16")
 STACK48_FP8 = MoEShape(48, 128, 8, 40, 2048, 768, "fp8")
+STACK48_INT4 = MoEShape(48, 128, 8, 92, 2048, 768, "int4")
 
 
 # ----------------------------------------------------------------------------
@@ -137,20 +145,33 @@ class ExpertWeights:
     format: bf16 experts give ``w13`` ([2I, H] uint16 bf16 bits, rows 0..I-1 the
     gate projection, rows I..2I-1 the up projection) and ``w2`` ([H, I]); FP8
     experts give E4M3 codes (uint8) for ``w13``/``w2`` plus fp32 block scales
-    ``s13`` ([ceil(2I/128), ceil(H/128)]) and ``s2`` ([ceil(H/128), ceil(I/128)]).
+    ``s13`` ([ceil(2I/128), ceil(H/128)]) and ``s2`` ([ceil(H/128), ceil(I/128)]);
+    GPTQ int4 experts give packed 4-bit codes (uint8, [2I, H/2] and [H, I/2],
+    input 2j in the low nibble of byte j) plus fp16 scales ``s13`` ([2I, H/128])
+    and ``s2`` ([H, I/128]).
     """
 
     def __init__(self, shape: MoEShape, seed: int = 0, std: float = 0.02):
         self.shape = shape
         self.seed = seed
         n = shape.w13_elems + shape.w2_elems
+        if shape.dtype == "int4":
+            n //= 2  # two codes per byte
         n_experts = shape.num_layers * shape.num_experts
         pool = max(1 << 25, n + 64 * n_experts)
         rng = np.random.default_rng([seed, 0x5EED, 1])
-        z = rng.standard_normal(pool, dtype=np.float32)
+        if shape.dtype == "int4":
+            # codes 8 + round(N(0, 2.5)) in 0..15; with scales |N(0,1)|*0.008
+            # the weights are of the 0.02 scale of the bf16 experts
+            z = rng.standard_normal(2 * pool, dtype=np.float32)
+            q = np.clip(np.rint(z * np.float32(2.5)) + 8, 0, 15).astype(np.uint8)
+            self._pool = q[0::2] | (q[1::2] << 4)
+            z = None
+        else:
+            z = rng.standard_normal(pool, dtype=np.float32)
         if shape.dtype == "bf16":
             self._pool = f32_to_bf16_bits(z * np.float32(std))
-        else:
+        elif shape.dtype == "fp8":
             # E4M3 codes with sd 2; the per-block scale |N(0,1)|*0.01 brings
             # code*scale to the 0.02 scale of the bf16 experts.
             self._pool = _encode_e4m3(z * np.float32(2.0))
@@ -165,13 +186,22 @@ class ExpertWeights:
         s = self.shape
         o = self.offset(layer, expert)
         win = self._pool[o : o + self._n]
-        w13 = win[: s.w13_elems].reshape(2 * s.intermediate, s.hidden)
-        w2 = win[s.w13_elems :].reshape(s.hidden, s.intermediate)
+        if s.dtype == "int4":
+            n13 = s.w13_elems // 2
+            w13 = win[:n13].reshape(2 * s.intermediate, s.hidden // 2)
+            w2 = win[n13:].reshape(s.hidden, s.intermediate // 2)
+        else:
+            w13 = win[: s.w13_elems].reshape(2 * s.intermediate, s.hidden)
+            w2 = win[s.w13_elems :].reshape(s.hidden, s.intermediate)
         out = {"w13": w13, "w2": w2}
         if s.dtype == "fp8":
             rng = np.random.default_rng([self.seed, 0x5CA1E, layer, expert])
             out["s13"] = (np.abs(rng.standard_normal(s.s13_shape)) * 0.01).astype(np.float32)
             out["s2"] = (np.abs(rng.standard_normal(s.s2_shape)) * 0.01).astype(np.float32)
+        elif s.dtype == "int4":
+            rng = np.random.default_rng([self.seed, 0x5CA1E, layer, expert])
+            out["s13"] = (np.abs(rng.standard_normal(s.s13_shape)) * 0.008).astype(np.float16)
+            out["s2"] = (np.abs(rng.standard_normal(s.s2_shape)) * 0.008).astype(np.float16)
         return out
 
 

@@ -42,7 +42,7 @@ extern "C" {
 typedef enum pe_status {
     PE_OK = 0,
     PE_ERR_INVALID = 1,           /* bad configuration or argument           */
-    PE_ERR_UNSUPPORTED_DTYPE = 2, /* expert format other than bf16/block-FP8 */
+    PE_ERR_UNSUPPORTED_DTYPE = 2, /* expert format not among pe_dtype        */
     PE_ERR_HOST_ALLOC = 3,        /* host store could not be pinned          */
     PE_ERR_CUDA = 4,              /* a CUDA runtime call failed              */
     PE_ERR_RANGE = 5,             /* layer/expert/slot/token count too large */
@@ -50,11 +50,13 @@ typedef enum pe_status {
 } pe_status;
 
 /* Expert storage formats ("Paged Experts", "Supported Configurations and
- * Limitations": unquantised and block-quantised FP8 with 128x128 blocks;
- * other formats are rejected at creation). */
+ * Limitations": unquantised, block-quantised FP8 with 128x128 blocks, and
+ * GPTQ int4; other formats are rejected at creation). */
 typedef enum pe_dtype {
-    PE_BF16 = 0,         /* bf16 weights                                    */
-    PE_FP8_BLOCK128 = 1  /* E4M3 weights, one fp32 scale per 128x128 block  */
+    PE_BF16 = 0,          /* bf16 weights                                    */
+    PE_FP8_BLOCK128 = 1,  /* E4M3 weights, one fp32 scale per 128x128 block  */
+    PE_INT4_GPTQ = 2      /* GPTQ int4: 4-bit codes, zero point 8, one fp16
+                             scale per output row and group of 128 inputs    */
 } pe_dtype;
 
 /* Device error word bits (read through pe_stats). */
@@ -68,8 +70,8 @@ typedef struct pe_config {
     int32_t num_experts;  /* E, routed experts per layer (1..1024)        */
     int32_t top_k;        /* experts per token (1..min(E, 32))            */
     int32_t num_slots;    /* K, resident experts per layer (top_k..E)     */
-    int32_t hidden;       /* H, model width (multiple of 8; of 128 for FP8)*/
-    int32_t intermediate; /* I, expert width (multiple of 8; of 128 for FP8)*/
+    int32_t hidden;       /* H, model width (multiple of 8; of 128 for FP8, int4)*/
+    int32_t intermediate; /* I, expert width (multiple of 8; of 128 for FP8, int4)*/
     int32_t dtype;        /* pe_dtype                                     */
     int32_t max_tokens;   /* largest num_tokens a forward call may pass   */
     int32_t device;       /* CUDA device ordinal                          */
@@ -80,7 +82,14 @@ typedef struct pe_config {
  *       w2 = [H, I] (down projection), both row-major bf16; no scales.
  * FP8:  w13 and w2 as E4M3 codes (one byte each, same shapes), s13 =
  *       [ceil(2I/128), ceil(H/128)] and s2 = [ceil(H/128), ceil(I/128)]
- *       row-major fp32 block scales.  Offsets are 128-byte aligned. */
+ *       row-major fp32 block scales.
+ * int4: w13 = [2I, H/2] and w2 = [H, I/2] bytes, byte j of a row holding
+ *       input 2j in its low nibble and 2j+1 in its high nibble; the weight
+ *       is (code - 8) * scale with s13 = [2I, H/128] and s2 = [H, I/128]
+ *       row-major fp16 scales (one per output row and 128 inputs).  A GPTQ
+ *       checkpoint (8 codes per int32 along the input, scales [K/128, N])
+ *       maps to this by a transpose of both.
+ * Offsets are 128-byte aligned. */
 typedef struct pe_row_layout {
     uint64_t w13_offset, w13_bytes;
     uint64_t s13_offset, s13_bytes;  /* 0 bytes for bf16 */
@@ -170,8 +179,9 @@ pe_status pe_create_shared(const pe_config* cfg, void* dev_arena, size_t arena_b
                            pe_handle* store_owner, pe_handle** out);
 
 /* Copy one expert into its host-store row (a synchronous host memcpy).
- *   w13, w2: host pointers in the row layout's formats (bf16 bits or E4M3
- *   codes); s13, s2: fp32 block scales for FP8, must be NULL for bf16.
+ *   w13, w2: host pointers in the row layout's formats (bf16 bits, E4M3
+ *   codes or packed int4 codes); s13, s2: the scales, fp32 for FP8 and fp16
+ *   for int4, NULL for bf16.
  *   Marks the expert loaded; a later forward that routes to an expert that
  *   was never loaded sets PE_DEVERR_NOT_LOADED.  Loading an expert that is
  *   currently resident does not refresh its slot: load before forwarding, or
@@ -179,7 +189,7 @@ pe_status pe_create_shared(const pe_config* cfg, void* dev_arena, size_t arena_b
  * Errors: PE_ERR_RANGE (layer/expert), PE_ERR_INVALID (NULL or stray
  *   scale pointers), PE_ERR_CUDA. */
 pe_status pe_load_host_expert(pe_handle* h, int32_t layer, int32_t expert, const void* w13,
-                              const void* w2, const float* s13, const float* s2);
+                              const void* w2, const void* s13, const void* s2);
 
 /* Host pointer to an expert's row in the host store (for inspection). */
 void* pe_host_row(pe_handle* h, int32_t layer, int32_t expert);

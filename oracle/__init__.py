@@ -18,15 +18,17 @@ Sources (the pages this follows):
   and the miss-rate arithmetic used as worked examples in the tests.
 
 Everything floating-point here is computed in float64, from the storage
-formats (bf16 bits, E4M3 codes with fp32 scales, fp32 router logits).  Where
+formats (bf16 bits, E4M3 codes with fp32 scales, GPTQ int4 codes with fp16
+group scales, fp32 router logits).  Where
 the pages are silent the plainest reading is taken; each such reading is
 listed in the function that makes it.
 
 Modules:
   routing  softmax over E, top-k on the logits, renormalised weights
   fp8      E4M3 decoding and 128x128 block dequantisation
+  int4     GPTQ int4 codes, group-128 dequantisation, checkpoint layout
   mlp      SiLU-gated expert MLP, merged buffer, top-k sum, whole layer
   lru      the LRU residency simulator that defines plans, slots and counts
 """
 
-from . import fp8, lru, mlp, routing  # noqa: F401
+from . import fp8, int4, lru, mlp, routing  # noqa: F401

@@ -27,6 +27,7 @@ from typing import Callable
 import numpy as np
 
 from . import fp8 as _fp8
+from . import int4 as _int4
 from .lru import ResidencySim, StepPlan
 from .routing import route
 
@@ -45,6 +46,11 @@ def expert_weights(row: dict, dtype: str, block: int = 128) -> tuple[np.ndarray,
         return (
             _fp8.dequant_block(row["w13"], row["s13"], block),
             _fp8.dequant_block(row["w2"], row["s2"], block),
+        )
+    if dtype == "int4":
+        return (
+            _int4.dequant_rows(row["w13"], row["s13"], block),
+            _int4.dequant_rows(row["w2"], row["s2"], block),
         )
     raise ValueError(f"unsupported expert dtype {dtype!r}")
 

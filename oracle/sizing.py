@@ -18,7 +18,8 @@ from __future__ import annotations
 
 def expert_bytes(hidden: int, inter: int, dtype: str, block: int = 128) -> int:
     """Bytes of one expert: gate+up [2I, H] and down [H, I] weights, plus one
-    fp32 scale per 128x128 block for block-FP8."""
+    fp32 scale per 128x128 block for block-FP8, or 4-bit codes plus one fp16
+    scale per output row and 128-input group for GPTQ int4."""
     n = 3 * hidden * inter
     if dtype == "bf16":
         return 2 * n
@@ -26,6 +27,10 @@ def expert_bytes(hidden: int, inter: int, dtype: str, block: int = 128) -> int:
         s13 = -(-2 * inter // block) * -(-hidden // block)
         s2 = -(-hidden // block) * -(-inter // block)
         return n + 4 * (s13 + s2)
+    if dtype == "int4":  # 4-bit codes, one fp16 scale per output row and 128-input group
+        s13 = 2 * inter * -(-hidden // block)
+        s2 = hidden * -(-inter // block)
+        return n // 2 + 2 * (s13 + s2)
     raise ValueError(dtype)
 
 

@@ -262,3 +262,69 @@ def check_lru_textbook(sim_cls, max_e=5, max_len=3):
                     assert got == [(m, c, h) for m, c, h in ref], (E, K, seq, got, ref)
                     res = {e: s for e, s in enumerate(a.expert_slot) if s >= 0}
                     assert res == b.resident_map()
+
+
+# ---------------------------------------------------------------- int4
+
+
+def _pack_rows_by_hand(q):
+    """Integer codes [N, K] -> row-layout bytes, written as plain loops."""
+    n, k = len(q), len(q[0])
+    out = np.zeros((n, k // 2), dtype=np.uint8)
+    for r in range(n):
+        for j in range(k // 2):
+            out[r, j] = int(q[r][2 * j]) | (int(q[r][2 * j + 1]) << 4)
+    return out
+
+
+def _pack_gptq_by_hand(q):
+    """Integer codes [N, K] -> checkpoint qweight int32 [K/8, N], by loops."""
+    n, k = len(q), len(q[0])
+    out = np.zeros((k // 8, n), dtype=np.uint32)
+    for c in range(n):
+        for r in range(k // 8):
+            word = 0
+            for i in range(8):
+                word |= int(q[c][8 * r + i]) << (4 * i)
+            out[r, c] = word
+    return out.view(np.int32)
+
+
+def check_int4_values(dequant_rows):
+    """Hand values: a byte 0x9F holds 15 (low) and 9 (high), i.e. +7 and +1
+    around the zero point 8; every code 8 dequantises to 0; codes 0..15 give
+    -8..7 times the scale."""
+    codes = np.array([[0x9F] + [0x88] * 63], dtype=np.uint8)  # one row, K = 128
+    w = dequant_rows(codes, np.array([[0.5]], dtype=np.float16))
+    assert w.shape == (1, 128)
+    assert w[0, 0] == 3.5 and w[0, 1] == 0.5 and not w[0, 2:].any()
+    q = np.tile(np.arange(16), 8).reshape(1, 128)  # K = 128: 0..15 eight times
+    w = dequant_rows(_pack_rows_by_hand(q), np.array([[0.25]], dtype=np.float16))
+    assert np.array_equal(w[0, :16], (np.arange(16) - 8) * 0.25)
+
+
+def check_int4_brute_force(dequant_rows, seed=0):
+    """Plain loops over (n, k) with the group index written out, on
+    non-square shapes with more than one group."""
+    rng = np.random.default_rng(seed)
+    for n, k in ((3, 256), (5, 384)):
+        q = rng.integers(0, 16, size=(n, k))
+        s = (rng.random((n, k // 128)) + 0.1).astype(np.float16)
+        w = dequant_rows(_pack_rows_by_hand(q), s)
+        for r in range(n):
+            for c in range(k):
+                assert w[r, c] == (q[r, c] - 8) * float(s[r, c // 128]), (r, c)
+
+
+def check_int4_gptq_layout(dequant_gptq, seed=1):
+    """The checkpoint layout (8 codes per int32 along the input, scales
+    [K/128, N]) dequantises to the same matrix as loops over the codes."""
+    rng = np.random.default_rng(seed)
+    n, k = 6, 256
+    q = rng.integers(0, 16, size=(n, k))
+    s = (rng.random((n, k // 128)) + 0.1).astype(np.float16)
+    w = dequant_gptq(_pack_gptq_by_hand(q), np.ascontiguousarray(s.T))
+    assert w.shape == (n, k)
+    for r in range(n):
+        for c in range(k):
+            assert w[r, c] == (q[r, c] - 8) * float(s[r, c // 128]), (r, c)

@@ -56,6 +56,12 @@ def test_row_layout_matches_expert_sizes(L):
     assert f8["row_stride"] % 256 == 0 and f8["row_stride"] >= f8["s2_offset"] + f8["s2_bytes"]
     tiny = _lib.row_layout(synth.TINY)
     assert tiny["payload_bytes"] == 3 * 256 * 128 * 2
+    i4 = _lib.row_layout(synth.STACK48_INT4)  # the pages' 2.43 MB GPTQ int4 expert
+    assert i4["payload_bytes"] == 2_433_024 == synth.STACK48_INT4.expert_bytes
+    assert i4["w13_bytes"] == 1536 * 1024 and i4["w2_bytes"] == 2048 * 384
+    assert i4["s13_bytes"] == 2 * 1536 * 16 and i4["s2_bytes"] == 2 * 2048 * 6
+    for k in ("w13_offset", "s13_offset", "w2_offset", "s2_offset"):
+        assert i4[k] % 128 == 0
 
 
 def test_max_waves_from_shapes(L):
@@ -101,6 +107,9 @@ def test_unsupported_dtype_and_fp8_shape(L):
     h = ctypes.c_void_p()
     assert L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == _lib.PE_ERR_UNSUPPORTED_DTYPE
     s = MoEShape(1, 16, 2, 6, 200, 128, "fp8")  # H not a multiple of 128
+    cfg = _lib.make_config(s, 4)
+    assert L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == _lib.PE_ERR_INVALID
+    s = MoEShape(1, 16, 2, 6, 256, 192, "int4")  # I not a multiple of the 128-input group
     cfg = _lib.make_config(s, 4)
     assert L.pe_create(ctypes.byref(cfg), None, 0, ctypes.byref(h)) == _lib.PE_ERR_INVALID
 

@@ -42,6 +42,15 @@ MUTANTS = [
      lambda m: pins.check_block_dequant(m.dequant_block)),
     ("oracle.fp8", "sr = np.arange(n) // block", "sr = np.arange(n) % (-(-n // block))",
      lambda m: pins.check_block_dequant(m.dequant_block)),
+    # int4
+    ("oracle.int4", "q[:, 0::2] = c & 0xF", "q[:, 0::2] = c >> 4",
+     lambda m: pins.check_int4_values(m.dequant_rows)),
+    ("oracle.int4", "q = unpack_rows(codes).astype(np.float64) - 8.0", "q = unpack_rows(codes).astype(np.float64) - 7.0",
+     lambda m: pins.check_int4_values(m.dequant_rows)),
+    ("oracle.int4", "return q * s[:, np.arange(k) // group]", "return q * s[:, np.arange(k) % s.shape[1]]",
+     lambda m: pins.check_int4_brute_force(m.dequant_rows)),
+    ("oracle.int4", "q[i::8] = (w >> (4 * i)) & 0xF", "q[i::8] = (w >> (4 * (7 - i))) & 0xF",
+     lambda m: pins.check_int4_gptq_layout(m.dequant_gptq)),
     # mlp
     ("oracle.mlp", "return (silu(gate) * up) @ w2.T", "return (silu(up) * gate) @ w2.T",
      lambda m: pins.check_mlp_hand(m.expert_mlp)),

@@ -4,7 +4,7 @@ import numpy as np
 import pytest
 
 import pins
-from oracle import fp8, lru, mlp, routing, sizing
+from oracle import fp8, int4, lru, mlp, routing, sizing
 
 
 def test_route_brute_force():
@@ -207,3 +207,45 @@ def test_slots_for_budget_pages_example():
     assert table <= g["mem_fraction_static"] * g["gpu_gb"] * 1e9
     assert sizing.slots_for_budget(table, 0, slot, g["num_experts"], 8) == g["num_slots"]
     assert sizing.slots_for_budget(table - 1, 0, slot, g["num_experts"], 8) == g["num_slots"] - 1
+
+
+def test_int4_hand_values():
+    pins.check_int4_values(int4.dequant_rows)
+
+
+def test_int4_brute_force():
+    pins.check_int4_brute_force(int4.dequant_rows)
+
+
+def test_int4_checkpoint_layout():
+    pins.check_int4_gptq_layout(int4.dequant_gptq)
+
+
+def test_int4_rejects_bad_grid():
+    with pytest.raises(ValueError):
+        int4.dequant_rows(np.zeros((2, 128), np.uint8), np.ones((2, 1), np.float16))
+
+
+def test_int4_expert_size_is_the_pages_2_43_mb():
+    g = pins.golden("page_numbers.json")
+    b = sizing.expert_bytes(2048, 768, "int4")
+    assert b == 3 * 2048 * 768 // 2 + 2 * (1536 * 16 + 2048 * 6) == 2_433_024
+    assert round(b / 1e6, 2) == g["int4_expert_mb"]["value"]
+    m = g["model"]
+    assert round(sizing.slot_bytes(b, m["num_layers"]) / 1e6) == g["slot_mb"]["int4_per_slot"]
+
+
+def test_gptq_checkpoint_repack_matches_the_oracle():
+    """The loader's repack of a GPTQ checkpoint tensor dequantises, in the
+    row layout, to the matrix the oracle reads from the checkpoint layout."""
+    from host_paged_expert_gb300 import formats
+
+    rng = np.random.default_rng(3)
+    n, k = 48, 384
+    qweight = rng.integers(0, 2**32, size=(k // 8, n), dtype=np.uint64).astype(np.uint32).view(np.int32)
+    scales = (rng.random((k // 128, n)) * 0.01 + 1e-3).astype(np.float16)
+    codes, srow = formats.gptq_int4_to_row(qweight, scales)
+    assert codes.shape == (n, k // 2) and srow.shape == (n, k // 128)
+    assert np.array_equal(int4.dequant_rows(codes, srow), int4.dequant_gptq(qweight, scales))
+    w13, s13 = formats.gate_up_rows((codes, srow), (codes[::-1], srow[::-1]))
+    assert w13.shape == (2 * n, k // 2) and np.array_equal(w13[n:], codes[::-1]) and np.array_equal(s13[:n], srow)
