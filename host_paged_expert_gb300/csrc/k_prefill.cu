@@ -19,10 +19,12 @@
 //           this step must finish before its page-in may overwrite the slot;
 //   gather  copies each entry's token row of x into the packed A operand;
 //   step    one persistent CTA per SM.  Every fourth CTA streams the host
-//           link: it copies 64 KiB chunks of the planned experts, in plan
+//           link: it copies 72 KiB chunks of the planned experts, in plan
 //           order, from the pinned host store into their slots and counts
-//           each expert's landed chunks.  The other CTAs take GEMM tiles
-//           from a queue in the same order (the hits of wave 0 first): a
+//           each expert's landed chunks, then joins the GEMM CTAs.  Those
+//           take GEMM tiles from a queue in the same order (the hits of
+//           wave 0 first, each expert's down tiles trailing its gate/up
+//           tiles by two rounds of the GEMM CTAs within its wave): a
 //           gate/up tile starts once every chunk of its expert has landed, a
 //           down tile once all gate/up tiles of its rows are done.  So the
 //           resident experts compute while the misses page in, every paged
@@ -31,12 +33,23 @@
 // The waves stay exactly the planner's: a page-in never overwrites a slot
 // before the GEMMs of the slot's previous expert are done with it.
 //
-// A GEMM tile is up to 256 rows of one expert x BN output columns.  TMA
-// (128-byte swizzle) feeds a 3-stage shared-memory ring, one thread issues
-// two M=128 tcgen05.mma per k-step that share the weight tile (the second
-// only when the expert has more than 128 rows), the accumulators live in
-// TMEM, and eight warps run the epilogue from TMEM.  The weights come straight
-// from the slot table (a 3-D tensor map over [slot][row][k]).
+// A GEMM tile is up to 256 rows of one expert x 128 output columns.  A GEMM
+// CTA is a pipeline of warp roles that hand tiles on through mbarriers:
+//   warp 0      scheduler and TMA producer: takes the next tile, waits for
+//               what it reads, publishes it to the other roles (a 4-deep
+//               queue) and streams its k-steps (128-byte-swizzled A and B
+//               tiles) into a 4-stage shared-memory ring;
+//   warp 1      MMA issuer: two M=128 tcgen05.mma per k-step that share the
+//               weight tile (the second only when the expert has more than
+//               128 rows), into one of two TMEM accumulator buffers;
+//   warps 2-7   converters for quantised weights (below);
+//   warps 8-11  epilogue: TMEM -> SiLU(gate)*up into h (bf16), or router
+//               weight x result into the merged entries, then count the
+//               tile done.
+// With two accumulator buffers the MMAs of one tile run while the epilogue
+// of the previous one drains, and the producer streams ahead across tiles.
+// The weights come straight from the slot table (a 3-D tensor map over
+// [slot][row][k]).
 //
 // Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) and GPTQ
 // int4 experts (4-bit codes, zero point 8, one fp16 scale per output row and
@@ -67,30 +80,32 @@
 namespace pe {
 namespace {
 
-constexpr int BM = 128, BK = 64, STAGES = 3;
+constexpr int BM = 128, BK = 64, STAGES = 4;
+constexpr int BN = kPrefillBN;        // output columns of a tile (MMA N)
 constexpr int MT = 2 * BM;            // rows of one tile: two M=128 MMAs
 constexpr int A_BYTES = BM * BK * 2;  // one 128-row half of the A tile
-constexpr int kStepThreads = 256;
+constexpr int B_BYTES = BN * BK * 2;  // the bf16 B tile
+constexpr int kConvWarps = 6;         // warps 2..7: decode quantised weight tiles (idle for bf16)
+constexpr int kEpiWarps = 4;          // warps 8..11: the epilogue (one per TMEM lane quarter)
+constexpr int kStepThreads = (2 + kConvWarps + kEpiWarps) * 32;
+constexpr int kInfoDepth = 4;         // tiles the scheduler may publish ahead
+constexpr uint32_t kTmemCols = 4 * BN;  // two accumulator buffers x two 128-row halves
 constexpr int kLinkEvery = 4;         // CTAs 0, 4, 8, ... of the step stream the host link
-constexpr int kLinkUnroll = 16;
-constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 64 KiB per item
-constexpr int kConvWarps = 6;         // FP8 / int4: warps 2..7 decode the weight tiles
+constexpr int kLinkUnroll = 12;
+constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 72 KiB per item
 constexpr int kMaxScaleCols = 64;     // FP8 / int4: K / 128 of either GEMM (H, I <= 8192)
 constexpr uint32_t kSpin = 1u << 22;  // polls, >= 128 ns apart
 
-// Tile geometry per weight format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ).
-// Stage layout: [A half 0][A half 1][B tile, bf16, swizzled][quantised
-// formats only: code staging], every part 1024-aligned.
+// Stage layout per weight format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ):
+// [A half 0][A half 1][B tile, bf16, swizzled][quantised formats only: code
+// staging], every part 1024-aligned.
 template <int FMT>
 struct Tile {
-    static constexpr int BN = FMT == PE_BF16 ? 256 : 128;  // output columns (MMA N)
-    static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int C_BYTES = FMT == PE_FP8_BLOCK128 ? BN * BK          // E4M3 codes of the B tile
                                    : FMT == PE_INT4_GPTQ  ? BN * BK / 2      // int4 codes of the B tile
                                                           : 0;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + C_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring
-    static constexpr uint32_t TMEM_COLS = 2 * BN;      // one accumulator per 128-row half
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -115,12 +130,19 @@ __device__ __forceinline__ int spin_geq(const unsigned* p, unsigned target, unsi
 
 // ---------------------------------------------------------------- align
 
+// The GEMM queue, wave by wave: each member's gate/up tiles in member order,
+// and its down tiles `lag` items later (so that a CTA taking a down tile
+// rarely waits for the member's gate/up tiles), never past the end of the
+// member's wave.  Every tile therefore depends only on tiles before it in
+// the queue (its own member's gate/up tiles, the page-in of its expert, and
+// through that page-in the tiles of earlier waves that used its slot), which
+// keeps the persistent pipeline free of deadlock.
 __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s, PrefillDev P, int slot_base, int T,
-                                                             int n1, int n2, unsigned nchunk) {
+                                                             int n1, int n2, unsigned nchunk, int lag) {
     __shared__ int sh_g_of_e[kMaxExperts];  // expert -> member
-    __shared__ int sh_me[kMaxExperts], sh_ms[kMaxExperts], sh_paged[kMaxExperts];
+    __shared__ int sh_me[kMaxExperts], sh_ms[kMaxExperts], sh_wp[kMaxExperts];  // expert, slot, wave*2 + paged
     __shared__ int sh_cnt[kMaxExperts], sh_off[kMaxExperts], sh_fill[kMaxExperts];
-    __shared__ int sh_t0[kMaxExperts + 1], sh_i0[kMaxExperts];
+    __shared__ int sh_t0[kMaxExperts + 1], sh_i0[kMaxExperts], sh_d0[kMaxExperts];  // tiles, gate/up and down queue bases
     __shared__ int sh_cum[kMaxSlots];
     __shared__ int sh_G;
     pdl_wait();
@@ -145,7 +167,7 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
                     const int e = L.member_expert[(size_t)w * K + q], slot = L.member_slot[(size_t)w * K + q];
                     sh_me[g] = e;
                     sh_ms[g] = slot;
-                    sh_paged[g] = pass;
+                    sh_wp[g] = (w << 1) | pass;
                     P.members[g] = make_int4(e, slot, w, pass);
                     if (pass) P.pin_member[np++] = g;
                     ++g;
@@ -173,7 +195,7 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         }
     __syncthreads();
     if (tid == 0) {
-        int off = 0, nt = 0, ni = 0;
+        int off = 0, nt = 0;
         for (int g = 0; g < G; ++g) {
             const int c = sh_cnt[g], slot = sh_ms[g];
             sh_off[g] = off;
@@ -181,29 +203,48 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             for (int r = 0; r < c && nt < P.max_tiles; r += MT)
                 P.tiles[nt++] = make_int4(off + r, slot_base + slot, min(MT, c - r), g);
             const int work = (nt - sh_t0[g]) * (n1 + n2);
-            sh_i0[g] = ni;
-            ni += work;
             // GEMM tiles of this slot's earlier occupants (members are in wave order)
             P.slot_need[g] = sh_cum[slot];
             sh_cum[slot] += work;
             off += (c + BM - 1) / BM * BM;
         }
         sh_t0[G] = nt;
+        // queue bases: gate/up blocks in member order, each down block once
+        // `lag` more items have been queued, flushed at every wave's end
+        int ni = 0, head = 0;
+        for (int g = 0; g < G; ++g) {
+            if (g > 0 && (sh_wp[g] >> 1) != (sh_wp[g - 1] >> 1))
+                for (; head < g; ++head) {
+                    sh_d0[head] = ni;
+                    ni += (sh_t0[head + 1] - sh_t0[head]) * n2;
+                }
+            sh_i0[g] = ni;
+            ni += (sh_t0[g + 1] - sh_t0[g]) * n1;
+            for (; head < g && ni - (sh_i0[head] + (sh_t0[head + 1] - sh_t0[head]) * n1) >= lag; ++head) {
+                sh_d0[head] = ni;
+                ni += (sh_t0[head + 1] - sh_t0[head]) * n2;
+            }
+        }
+        for (; head < G; ++head) {
+            sh_d0[head] = ni;
+            ni += (sh_t0[head + 1] - sh_t0[head]) * n2;
+        }
         P.counts[0] = nt;
         P.counts[1] = off <= P.max_rows ? off : P.max_rows;
         P.counts[2] = ni <= P.max_items ? ni : P.max_items;
     }
     __syncthreads();
     for (int g = tid; g < G; g += nthr) {
-        // the member's gate/up tiles, then its down tiles
+        // the member's gate/up tiles and its down tiles at their queue bases
         int j = sh_i0[g];
         for (int t = sh_t0[g]; t < sh_t0[g + 1]; ++t)
             for (int n = 0; n < n1; ++n, ++j)
                 if (j < P.max_items) P.items[j] = make_int2(t, n);
+        j = sh_d0[g];
         for (int t = sh_t0[g]; t < sh_t0[g + 1]; ++t)
             for (int n = 0; n < n2; ++n, ++j)
                 if (j < P.max_items) P.items[j] = make_int2(t, 0x10000 | n);
-        P.landed[g] = sh_paged[g] ? 0u : nchunk;  // a hit is ready at once
+        P.landed[g] = (sh_wp[g] & 1) ? 0u : nchunk;  // a hit is ready at once
     }
     for (int t = tid; t < sh_t0[G]; t += nthr) P.gu_done[t] = 0;
     for (int i = tid; i < nent; i += nthr)
@@ -244,7 +285,7 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const __nv_bfloat16
 
 // ---------------------------------------------------------------- link role
 
-// One 64 KiB item (a multiple of 16 bytes, possibly shorter at the row end).
+// One 72 KiB item (a multiple of 16 bytes, possibly shorter at the row end).
 __device__ __forceinline__ void link_copy(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t bytes) {
     const int4* sp = reinterpret_cast<const int4*>(src);
     int4* dp = reinterpret_cast<int4*>(dst);
@@ -296,188 +337,179 @@ __device__ void link_role(const PrefillDev& P, const Shape& s, const uint8_t* __
 
 // ---------------------------------------------------------------- GEMM role
 
-struct Ring {
-    uint8_t* base;
-    uint64_t* full;
-    uint64_t* empty;
-    uint64_t* conv;  // quantised formats: the bf16 B tile of the stage is written
-    uint64_t* acc;
-    float* scale;    // FP8: [2][kMaxScaleCols] block scales of the tile's two row ranges
-    __half* scale4;  // int4: [BN][kMaxScaleCols] group scales of the tile's rows
+// One GEMM tile as the scheduler hands it to the other roles.
+struct TileInfo {
+    int4 ti;    // row0, slot (whole table), valid rows, member
+    int t;      // tile index (gate/up counters)
+    int n;      // column tile
+    int kind;   // 0 gate/up, 1 down, -1 no more tiles
+    int ok;     // 0: a dependency wait gave up; the tile is skipped but counted
 };
 
-// One tile.  EPI 0: A = x_perm, B = w13 (gate rows n0.. and up rows I+n0..,
-//   BN/2 each), h_perm[row, n0 + c] = bf16(SiLU(gate_c) * up_c), c < BN/2.
-// EPI 1: A = h_perm, B = w2 rows m0..m0+BN-1, merged[entry, m0 + c] = w * acc_c.
-// kb0 = k-steps this CTA ran before (ring position); acc_phase = tiles before, mod 2.
-template <int EPI, int FMT>
-__device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, const Ring& R, int4 ti,
-                                          int n_tile, int kblocks, uint32_t kb0, uint32_t acc_phase, uint32_t tmem,
-                                          const PrefillDev& P, const LayerDev& L, const Shape& s,
-                                          const uint8_t* slots_all, float* __restrict__ merged, uint32_t* err) {
-    using TL = Tile<FMT>;
-    constexpr bool QUANT = FMT != PE_BF16;
-    constexpr int BN = TL::BN, B_BYTES = TL::B_BYTES, STAGE_BYTES = TL::STAGE_BYTES;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool two = ti.z > BM;  // the tile's second 128-row half is used
+struct StepShared {
+    uint64_t full[STAGES], empty[STAGES], conv[STAGES];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t info_full[kInfoDepth], info_empty[kInfoDepth];
+    TileInfo info[kInfoDepth];
+    uint32_t tmem_base;
+};
 
-    if (threadIdx.x == 0) {  // TMA producer
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
-            if (use > 0 && !tc::mbar_wait(&R.empty[st], (use - 1) & 1, err, PE_DEVERR_TIMEOUT)) break;
-            const int b_tx = QUANT ? TL::C_BYTES : B_BYTES;
-            tc::mbar_arrive_expect_tx(&R.full[st], (two ? 2 * A_BYTES : A_BYTES) + b_tx);
-            uint8_t* a = R.base + st * STAGE_BYTES;
-            // bf16: the B tile itself; quantised: its codes, into the staging buffer
-            uint8_t* b = QUANT ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
-            // the weight map's inner coordinate counts bytes for int4 (two codes each)
-            const int kx = FMT == PE_INT4_GPTQ ? kb * (BK / 2) : kb * BK;
-            tc::tma_load_2d(a, tmA, &R.full[st], kb * BK, ti.x);
-            if (two) tc::tma_load_2d(a + A_BYTES, tmA, &R.full[st], kb * BK, ti.x + BM);
-            if (EPI == 0) {
-                tc::tma_load_3d(b, tmB, &R.full[st], kx, n_tile * (BN / 2), ti.y);
-                tc::tma_load_3d(b + b_tx / 2, tmB, &R.full[st], kx, s.I + n_tile * (BN / 2), ti.y);
-            } else {
-                tc::tma_load_3d(b, tmB, &R.full[st], kx, n_tile * BN, ti.y);
-            }
+// The tile's rows of the B operand for column tile n: gate rows n*BN/2.. and
+// up rows I + n*BN/2.. (gate/up), or rows n*BN.. (down).
+template <int EPI>
+__device__ __forceinline__ int b_row(const Shape& s, int n_tile, int r) {
+    return EPI == 0 ? (r < BN / 2 ? n_tile * (BN / 2) + r : s.I + n_tile * (BN / 2) + r - BN / 2) : n_tile * BN + r;
+}
+
+// Producer: TMA loads of one tile's k-steps into the ring.
+template <int EPI, int FMT>
+__device__ __forceinline__ void produce_tile(const CUtensorMap* tmA, const CUtensorMap* tmB, StepShared& S,
+                                             uint8_t* ring, const TileInfo& I, int kblocks, uint32_t kb0,
+                                             const Shape& s, uint32_t* err) {
+    constexpr bool QUANT = FMT != PE_BF16;
+    const bool two = I.ti.z > BM;
+    const int b_tx = QUANT ? Tile<FMT>::C_BYTES : B_BYTES;
+    for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
+        if (use > 0 && !tc::mbar_wait(&S.empty[st], (use - 1) & 1, err, PE_DEVERR_TIMEOUT)) return;
+        tc::mbar_arrive_expect_tx(&S.full[st], (two ? 2 * A_BYTES : A_BYTES) + b_tx);
+        uint8_t* a = ring + st * Tile<FMT>::STAGE_BYTES;
+        // bf16: the B tile itself; quantised: its codes, into the staging buffer
+        uint8_t* b = QUANT ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
+        // the weight map's inner coordinate counts bytes for int4 (two codes each)
+        const int kx = FMT == PE_INT4_GPTQ ? kb * (BK / 2) : kb * BK;
+        tc::tma_load_2d(a, tmA, &S.full[st], kb * BK, I.ti.x);
+        if (two) tc::tma_load_2d(a + A_BYTES, tmA, &S.full[st], kb * BK, I.ti.x + BM);
+        if (EPI == 0) {
+            tc::tma_load_3d(b, tmB, &S.full[st], kx, I.n * (BN / 2), I.ti.y);
+            tc::tma_load_3d(b + b_tx / 2, tmB, &S.full[st], kx, s.I + I.n * (BN / 2), I.ti.y);
+        } else {
+            tc::tma_load_3d(b, tmB, &S.full[st], kx, I.n * BN, I.ti.y);
         }
-    } else if (threadIdx.x == 32) {  // MMA issuer
-        constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
-            if (!tc::mbar_wait(QUANT ? &R.conv[st] : &R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
-            tc::fence_after_sync();
-            const uint32_t a = tc::smem_u32(R.base + st * STAGE_BYTES);
-            const uint32_t b = a + 2 * A_BYTES;
+    }
+}
+
+// Converters (warps 2..7): decode the tile's weight codes into the
+// swizzled bf16 B tile of each stage, applying the scales.
+template <int EPI, int FMT>
+__device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float* scale, __half* scale4,
+                                             const TileInfo& I, int kblocks, uint32_t kb0, const Shape& s,
+                                             const uint8_t* slots_all, uint32_t* err) {
+    constexpr int NCT = kConvWarps * 32;
+    const int ct = threadIdx.x - 64, lane = threadIdx.x & 31;
+    const int Kdim = EPI == 0 ? s.H : s.I;
+    const int ng = Kdim / 128;  // FP8 block columns, int4 groups
+    // the scales live in the slot, which this kernel's link CTAs write: read them through L2
+    const uint8_t* sc = slots_all + (size_t)I.ti.y * s.stride + (EPI == 0 ? s.s13_off : s.s2_off);
+    // every converter warp is done with the previous tile's scales
+    asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
+    if (FMT == PE_FP8_BLOCK128) {
+        // the tile's rows lie in one 128-row block per range (gate and up, or down)
+        const int rb0 = b_row<EPI>(s, I.n, 0) / kFp8Block, rb1 = b_row<EPI>(s, I.n, BN - 1) / kFp8Block;
+        for (int i = ct; i < 2 * ng; i += NCT) {
+            const int h = i / ng, c = i - h * ng;
+            scale[h * kMaxScaleCols + c] = __ldcg(reinterpret_cast<const float*>(sc) + (size_t)(h ? rb1 : rb0) * ng + c);
+        }
+    } else {
+        // every row has its own group scales [rows][ng] fp16; the tile's rows
+        // are one or two contiguous 16-byte-aligned ranges: copy as vectors
+        const int half_vecs = (BN / 2) * ng * 2 / 16;
+        const uint8_t* src0 = sc + (size_t)b_row<EPI>(s, I.n, 0) * ng * 2;
+        const uint8_t* src1 = sc + (size_t)b_row<EPI>(s, I.n, BN / 2) * ng * 2;
+        int4* dst = reinterpret_cast<int4*>(scale4);
+        for (int i = ct; i < 2 * half_vecs; i += NCT) {
+            const uint8_t* src = i < half_vecs ? src0 + 16 * (size_t)i : src1 + 16 * (size_t)(i - half_vecs);
+            dst[i] = __ldcg(reinterpret_cast<const int4*>(src));
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
+    for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
+        if (!tc::mbar_wait(&S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) return;
+        uint8_t* bt = ring + st * Tile<FMT>::STAGE_BYTES + 2 * A_BYTES;
+        const uint8_t* codes = bt + B_BYTES;
+        for (int q = ct; q < BN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
+            const int r = q >> 2, j = q & 3;
+            uint32_t packed[8];
+            if (FMT == PE_FP8_BLOCK128) {
+                const float scl = scale[((EPI == 0 && r >= BN / 2) ? kMaxScaleCols : 0) + (kb * BK) / kFp8Block];
+                const int4 cv = *reinterpret_cast<const int4*>(codes + r * BK + j * 16);
+                const uint32_t w4[4] = {(uint32_t)cv.x, (uint32_t)cv.y, (uint32_t)cv.z, (uint32_t)cv.w};
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                const uint64_t bd = tc::smem_desc_sw128(b + kk * 32);
-                tc::mma_f16(tmem, tc::smem_desc_sw128(a + kk * 32), bd, idesc, (kb | kk) != 0);
-                if (two) tc::mma_f16(tmem + BN, tc::smem_desc_sw128(a + A_BYTES + kk * 32), bd, idesc, (kb | kk) != 0);
-            }
-            tc::mma_commit(&R.empty[st]);  // frees the stage once these MMAs are done
-        }
-        tc::mma_commit(R.acc);
-    } else if (FMT == PE_INT4_GPTQ && warp >= 2) {  // converters: int4 codes -> scaled bf16, swizzled
-        constexpr int NCT = kConvWarps * 32;
-        const int ct = threadIdx.x - 64;
-        const int Kdim = EPI == 0 ? s.H : s.I;
-        const int ng = Kdim / kInt4Group;
-        {
-            // every row of the tile has its own group scales; they live in
-            // the slot, which this kernel's link CTAs write: read through L2
-            const unsigned short* sc = reinterpret_cast<const unsigned short*>(
-                slots_all + (size_t)ti.y * s.stride + (EPI == 0 ? s.s13_off : s.s2_off));
-            for (int i = ct; i < BN * ng; i += NCT) {
-                const int r = i / ng, c = i - r * ng;
-                const int grow = EPI == 0 ? (r < BN / 2 ? n_tile * (BN / 2) + r : s.I + n_tile * (BN / 2) + r - BN / 2)
-                                          : n_tile * BN + r;
-                R.scale4[r * kMaxScaleCols + c] = __ushort_as_half(__ldcg(sc + (size_t)grow * ng + c));
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
-        }
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
-            if (!tc::mbar_wait(&R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
-            uint8_t* bt = R.base + st * STAGE_BYTES + 2 * A_BYTES;
-            const uint8_t* codes = bt + B_BYTES;
-            const int grp = (kb * BK) / kInt4Group;
-            for (int q = ct; q < BN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
-                const int r = q >> 2, j = q & 3;
-                const float scale = __half2float(R.scale4[r * kMaxScaleCols + grp]);
+                for (int t = 0; t < 4; ++t) {
+                    const float2 lo = e4m3x2(w4[t]), hi = e4m3x2(w4[t] >> 16);
+                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(lo.x * scl, lo.y * scl);
+                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(hi.x * scl, hi.y * scl);
+                    packed[2 * t] = *reinterpret_cast<const uint32_t*>(&p0);
+                    packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
+                }
+            } else {
+                const float scl = __half2float(scale4[r * ng + (kb * BK) / kInt4Group]);
                 const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
-                uint32_t packed[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) {  // codes 2t, 2t+1 of the chunk
                     const uint32_t w = t < 4 ? cv.x : cv.y;
                     const int sh = 8 * (t & 3);
-                    const float v0 = (float)(int)((w >> sh) & 0xFu) - 8.f;
-                    const float v1 = (float)(int)((w >> (sh + 4)) & 0xFu) - 8.f;
-                    const __nv_bfloat162 pv = __floats2bfloat162_rn(v0 * scale, v1 * scale);
+                    // q - 8 exactly: 2^23 + q as a float, minus 2^23 + 8
+                    const float v0 = __int_as_float(0x4B000000u | ((w >> sh) & 0xFu)) - 8388616.0f;
+                    const float v1 = __int_as_float(0x4B000000u | ((w >> (sh + 4)) & 0xFu)) - 8388616.0f;
+                    const __nv_bfloat162 pv = __floats2bfloat162_rn(v0 * scl, v1 * scl);
                     packed[t] = *reinterpret_cast<const uint32_t*>(&pv);
                 }
-                // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
-                uint8_t* row = bt + r * 128;
-                *reinterpret_cast<int4*>(row + (((2 * j) ^ (r & 7)) * 16)) =
-                    make_int4(packed[0], packed[1], packed[2], packed[3]);
-                *reinterpret_cast<int4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) =
-                    make_int4(packed[4], packed[5], packed[6], packed[7]);
             }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&R.conv[st]);
+            // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
+            uint8_t* row = bt + r * 128;
+            *reinterpret_cast<int4*>(row + (((2 * j) ^ (r & 7)) * 16)) =
+                make_int4(packed[0], packed[1], packed[2], packed[3]);
+            *reinterpret_cast<int4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) =
+                make_int4(packed[4], packed[5], packed[6], packed[7]);
         }
-    } else if (FMT == PE_FP8_BLOCK128 && warp >= 2) {  // converters: E4M3 codes -> scaled bf16, swizzled
-        constexpr int NCT = kConvWarps * 32;
-        const int ct = threadIdx.x - 64;
-        const int Kdim = EPI == 0 ? s.H : s.I;
-        const int nbk = (Kdim + kFp8Block - 1) / kFp8Block;
-        {
-            // The tile's rows lie in one 128-row block per range (gate and up
-            // for w13, one range for w2).  The scales live in the slot, which
-            // this kernel's link CTAs write: read them through L2.
-            const float* sc = reinterpret_cast<const float*>(slots_all + (size_t)ti.y * s.stride +
-                                                             (EPI == 0 ? s.s13_off : s.s2_off));
-            const int rb0 = EPI == 0 ? n_tile * (BN / 2) / kFp8Block : n_tile * BN / kFp8Block;
-            const int rb1 = EPI == 0 ? (s.I + n_tile * (BN / 2)) / kFp8Block : rb0;
-            for (int i = ct; i < 2 * nbk; i += NCT) {
-                const int h = i / nbk, c = i - h * nbk;
-                R.scale[h * kMaxScaleCols + c] = __ldcg(sc + (size_t)(h ? rb1 : rb0) * nbk + c);
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
-        }
-        for (int kb = 0; kb < kblocks; ++kb) {
-            const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
-            if (!tc::mbar_wait(&R.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
-            uint8_t* bt = R.base + st * STAGE_BYTES + 2 * A_BYTES;
-            const uint8_t* codes = bt + B_BYTES;
-            const float* srow = R.scale + (kb * BK) / kFp8Block;
-            for (int q = ct; q < BN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
-                const int r = q >> 2, j = q & 3;
-                const float scale = srow[(EPI == 0 && r >= BN / 2) ? kMaxScaleCols : 0];
-                const int4 cv = *reinterpret_cast<const int4*>(codes + r * BK + j * 16);
-                const uint32_t w4[4] = {(uint32_t)cv.x, (uint32_t)cv.y, (uint32_t)cv.z, (uint32_t)cv.w};
-                uint32_t packed[8];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 lo = e4m3x2(w4[t]), hi = e4m3x2(w4[t] >> 16);
-                    const __nv_bfloat162 p0 = __floats2bfloat162_rn(lo.x * scale, lo.y * scale);
-                    const __nv_bfloat162 p1 = __floats2bfloat162_rn(hi.x * scale, hi.y * scale);
-                    packed[2 * t] = *reinterpret_cast<const uint32_t*>(&p0);
-                    packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
-                }
-                // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
-                uint8_t* row = bt + r * 128;
-                *reinterpret_cast<int4*>(row + (((2 * j) ^ (r & 7)) * 16)) =
-                    make_int4(packed[0], packed[1], packed[2], packed[3]);
-                *reinterpret_cast<int4*>(row + (((2 * j + 1) ^ (r & 7)) * 16)) =
-                    make_int4(packed[4], packed[5], packed[6], packed[7]);
-            }
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&R.conv[st]);
-        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&S.conv[st]);
     }
-    __syncwarp();
+}
 
-    // epilogue: warp w reads TMEM lanes 32*(w%4).. (its lane quarter) and the
-    // (w/4)-th half of the tile's output columns; in row half hf, lane l owns
-    // tile row hf*128 + 32*(w%4) + l
-    const bool ok = tc::mbar_wait(R.acc, acc_phase, err, PE_DEVERR_TIMEOUT);
-    tc::fence_after_sync();
-    const int quarter = warp & 3, colh = warp >> 2;
-    for (int hf = 0; hf < (two ? 2 : 1); ++hf) {
+// MMA issuer: one tile into TMEM accumulator buffer acc (256 columns: two
+// 128-row halves x BN).
+template <int FMT>
+__device__ __forceinline__ void mma_tile(StepShared& S, uint8_t* ring, const TileInfo& I, int kblocks, uint32_t kb0,
+                                         uint32_t dst, uint32_t* err) {
+    constexpr bool QUANT = FMT != PE_BF16;
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+    const bool two = I.ti.z > BM;
+    for (int kb = 0; kb < kblocks; ++kb) {
+        const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
+        if (!tc::mbar_wait(QUANT ? &S.conv[st] : &S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
+        tc::fence_after_sync();
+        const uint32_t a = tc::smem_u32(ring + st * Tile<FMT>::STAGE_BYTES);
+        const uint32_t b = a + 2 * A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t bd = tc::smem_desc_sw128(b + kk * 32);
+            tc::mma_f16(dst, tc::smem_desc_sw128(a + kk * 32), bd, idesc, (kb | kk) != 0);
+            if (two) tc::mma_f16(dst + BN, tc::smem_desc_sw128(a + A_BYTES + kk * 32), bd, idesc, (kb | kk) != 0);
+        }
+        tc::mma_commit(&S.empty[st]);  // frees the stage once these MMAs are done
+    }
+}
+
+// Epilogue (warps 8..11): warp w reads TMEM lanes 32*(w%4).. of the
+// accumulator buffer; in row half hf, lane l owns tile row hf*128 + 32*(w%4) + l.
+template <int EPI>
+__device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, const PrefillDev& P, const LayerDev& L,
+                                              const Shape& s, float* __restrict__ merged) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
+    for (int hf = 0; hf < (I.ti.z > BM ? 2 : 1); ++hf) {
         const int r = hf * BM + quarter * 32 + lane;
-        const uint32_t trow = tmem + hf * BN + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t trow = acc + hf * BN + ((uint32_t)(quarter * 32) << 16);
         if (EPI == 0) {
-            constexpr int NCH = BN / 128;  // 32-column chunks of gate (and up, BN/2 further) per column half
-            for (int c0 = 0; c0 < NCH; ++c0) {
-                const int cc = colh * NCH + c0;
+            for (int cc = 0; cc < BN / 64; ++cc) {  // 32 gate columns and the 32 up columns BN/2 further
                 uint32_t g[32], u[32];
                 tc::tmem_ld32(trow + cc * 32, g);
                 tc::tmem_ld32(trow + BN / 2 + cc * 32, u);
                 tc::tmem_ld_wait();
-                if (ok && r < ti.z) {
+                if (r < I.ti.z) {
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -487,23 +519,21 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmA, const CUtensor
                         packed[c] = *reinterpret_cast<const uint32_t*>(&hv);
                     }
                     int4* dst =
-                        reinterpret_cast<int4*>(P.h_perm + (size_t)(ti.x + r) * s.I + n_tile * (BN / 2) + cc * 32);
+                        reinterpret_cast<int4*>(P.h_perm + (size_t)(I.ti.x + r) * s.I + I.n * (BN / 2) + cc * 32);
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
                         dst[v] = make_int4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
                 }
             }
         } else {
-            const int entry = r < ti.z ? P.perm[ti.x + r] : -1;
+            const int entry = r < I.ti.z ? P.perm[I.ti.x + r] : -1;
             const float w = entry >= 0 ? L.topk_w[entry] : 0.f;
-            constexpr int NCH = BN / 64;  // 32-column chunks per column half
-            for (int c0 = 0; c0 < NCH; ++c0) {
-                const int c4 = colh * NCH + c0;
+            for (int c4 = 0; c4 < BN / 32; ++c4) {
                 uint32_t v[32];
                 tc::tmem_ld32(trow + c4 * 32, v);
                 tc::tmem_ld_wait();
-                if (ok && entry >= 0) {
-                    float4* dst = reinterpret_cast<float4*>(merged + (size_t)entry * s.H + n_tile * BN + c4 * 32);
+                if (entry >= 0) {
+                    float4* dst = reinterpret_cast<float4*>(merged + (size_t)entry * s.H + I.n * BN + c4 * 32);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         dst[q] = make_float4(__fmul_rn(w, __uint_as_float(v[4 * q])),
@@ -525,98 +555,148 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                         PrefillDev P, LayerDev L, Shape s, const uint8_t* __restrict__ host_layer,
                         uint8_t* __restrict__ slots_all, int slot_base, int n1, int n2, unsigned nchunk,
                         float* __restrict__ merged, uint32_t* err) {
-    using TL = Tile<FMT>;
+    constexpr bool QUANT = FMT != PE_BF16;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[STAGES];
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];
-    __shared__ __align__(8) uint64_t conv_bar[STAGES];
-    __shared__ __align__(8) uint64_t acc_bar;
+    __shared__ StepShared S;
     __shared__ float sh_scale[FMT == PE_FP8_BLOCK128 ? 2 * kMaxScaleCols : 1];
-    __shared__ __half sh_scale4[FMT == PE_INT4_GPTQ ? Tile<FMT>::BN * kMaxScaleCols : 1];
-    __shared__ uint32_t tmem_base_sh;
-    __shared__ int2 sh_item;
+    __shared__ __align__(16) __half sh_scale4[FMT == PE_INT4_GPTQ ? BN * kMaxScaleCols : 8];
     __shared__ int sh_ok;
     pdl_wait();
     pdl_trigger();
     if (blockIdx.x % kLinkEvery == 0) {
+        // a link CTA joins the GEMM queue once its share of the page-ins is
+        // done (it then depends only on work queued before its next tile)
         link_role(P, s, host_layer, slots_all + (size_t)slot_base * s.stride, blockIdx.x / kLinkEvery,
                   (gridDim.x + kLinkEvery - 1) / kLinkEvery, nchunk, err, &sh_ok);
-        return;
+        __syncthreads();
     }
 
-    const int warp = threadIdx.x >> 5;
-    Ring R{reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023)), full_bar,
-           empty_bar, conv_bar, &acc_bar, sh_scale, sh_scale4};
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // readers of each tile-info entry: the MMA warp, the converter warps, the epilogue warps
+    constexpr uint32_t kReaders = 1 + (QUANT ? kConvWarps : 0) + kEpiWarps;
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
-            tc::mbar_init(&full_bar[i], 1);
-            tc::mbar_init(&empty_bar[i], 1);
-            tc::mbar_init(&conv_bar[i], kConvWarps);  // one arrive per converter warp
+            tc::mbar_init(&S.full[i], 1);
+            tc::mbar_init(&S.empty[i], 1);
+            tc::mbar_init(&S.conv[i], kConvWarps);  // one arrive per converter warp
         }
-        tc::mbar_init(&acc_bar, 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(&S.acc_full[i], 1);
+            tc::mbar_init(&S.acc_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kInfoDepth; ++i) {
+            tc::mbar_init(&S.info_full[i], 1);
+            tc::mbar_init(&S.info_empty[i], kReaders);
+        }
         tc::fence_barrier_init();
         tc::tma_prefetch(&tmX);
         tc::tma_prefetch(&tmH);
         tc::tma_prefetch(&tmW13);
         tc::tma_prefetch(&tmW2);
     }
-    if (warp == 0) tc::tmem_alloc(&tmem_base_sh, TL::TMEM_COLS);
+    if (warp == 0) tc::tmem_alloc(&S.tmem_base, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = tmem_base_sh;
+    const uint32_t tmem = S.tmem_base;
     const int nitems = P.counts[2];
-    uint32_t kb_ring = 0, acc_phase = 0;
-    for (;;) {
-        if (threadIdx.x == 0) {
-            const int j = (int)atomicAdd(&P.ctl[0], 1u);
-            int2 it = make_int2(-1, 0);
-            int ok = 0;
-            if (j < nitems) {
-                it = P.items[j];
-                if ((it.y >> 16) == 0)  // gate/up: every chunk of the expert has landed
-                    ok = spin_geq(&P.landed[P.tiles[it.x].w], nchunk, &P.ctl[1], err);
-                else  // down: all gate/up tiles of these rows are done
-                    ok = spin_geq(&P.gu_done[it.x], (unsigned)n1, &P.ctl[1], err);
-                // the tensor-memory-access loads below read what other CTAs wrote
-                asm volatile("fence.proxy.async.global;" ::: "memory");
+
+    if (warp == 0) {
+        // scheduler and TMA producer (lane 0): take a tile, wait for what it
+        // reads, publish it to the other roles, stream its k-steps
+        if (lane == 0) {
+            uint32_t kb_ring = 0;
+            for (uint32_t q = 0;; ++q) {
+                const int j = (int)atomicAdd(&P.ctl[0], 1u);
+                TileInfo I{make_int4(0, 0, 0, 0), 0, 0, -1, 0};
+                if (j < nitems) {
+                    const int2 it = P.items[j];
+                    I.t = it.x;
+                    I.kind = it.y >> 16;
+                    I.n = it.y & 0xffff;
+                    I.ti = P.tiles[it.x];
+                    I.ok = I.kind == 0 ? spin_geq(&P.landed[I.ti.w], nchunk, &P.ctl[1], err)  // the expert has landed
+                                       : spin_geq(&P.gu_done[it.x], (unsigned)n1, &P.ctl[1], err);  // its h is done
+                    // the tensor-memory-access loads below read what other CTAs wrote
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                }
+                const uint32_t e = q % kInfoDepth, use = q / kInfoDepth;
+                if (use > 0) tc::mbar_wait(&S.info_empty[e], (use - 1) & 1, err, PE_DEVERR_TIMEOUT);
+                S.info[e] = I;
+                tc::mbar_arrive(&S.info_full[e]);
+                if (I.kind < 0) break;
+                if (!I.ok) continue;
+                if (I.kind == 0) {
+                    produce_tile<0, FMT>(&tmX, &tmW13, S, ring, I, s.H / BK, kb_ring, s, err);
+                    kb_ring += s.H / BK;
+                } else {
+                    produce_tile<1, FMT>(&tmH, &tmW2, S, ring, I, s.I / BK, kb_ring, s, err);
+                    kb_ring += s.I / BK;
+                }
             }
-            sh_item = it;
-            sh_ok = ok;
         }
-        __syncthreads();
-        tc::fence_after_sync();
-        const int2 it = sh_item;
-        if (it.x < 0) break;
-        const bool down = (it.y >> 16) != 0;
-        const int n = it.y & 0xffff;
-        const int4 ti = P.tiles[it.x];
-        if (sh_ok) {
-            if (!down) {
-                gemm_tile<0, FMT>(&tmX, &tmW13, R, ti, n, s.H / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
-                                  merged, err);
-                kb_ring += s.H / BK;
-            } else {
-                gemm_tile<1, FMT>(&tmH, &tmW2, R, ti, n, s.I / BK, kb_ring, acc_phase, tmem, P, L, s, slots_all,
-                                  merged, err);
-                kb_ring += s.I / BK;
+    } else if (warp == 1 || (QUANT && warp < 2 + kConvWarps) || warp >= 2 + kConvWarps) {
+        const bool is_mma = warp == 1, is_conv = warp >= 2 && warp < 2 + kConvWarps;
+        uint32_t kb_ring = 0, acc_iter = 0;
+        for (uint32_t q = 0;; ++q) {
+            const uint32_t e = q % kInfoDepth, use = q / kInfoDepth;
+            tc::mbar_wait(&S.info_full[e], use & 1, err, PE_DEVERR_TIMEOUT);
+            const TileInfo I = S.info[e];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&S.info_empty[e]);
+            if (I.kind < 0) break;
+            const int kblocks = I.kind == 0 ? s.H / BK : s.I / BK;
+            const uint32_t buf = acc_iter & 1, buse = acc_iter >> 1;
+            if (I.ok) {
+                if (is_mma) {
+                    if (lane == 0) {
+                        if (buse > 0) tc::mbar_wait(&S.acc_empty[buf], (buse - 1) & 1, err, PE_DEVERR_TIMEOUT);
+                        tc::fence_after_sync();
+                        mma_tile<FMT>(S, ring, I, kblocks, kb_ring, tmem + buf * (2 * BN), err);
+                        tc::mma_commit(&S.acc_full[buf]);
+                    }
+                    __syncwarp();
+                } else if (is_conv) {
+                    if (I.kind == 0)
+                        convert_tile<0, FMT>(S, ring, sh_scale, sh_scale4, I, kblocks, kb_ring, s, slots_all, err);
+                    else
+                        convert_tile<1, FMT>(S, ring, sh_scale, sh_scale4, I, kblocks, kb_ring, s, slots_all, err);
+                } else {  // epilogue
+                    tc::mbar_wait(&S.acc_full[buf], buse & 1, err, PE_DEVERR_TIMEOUT);
+                    tc::fence_after_sync();
+                    if (I.kind == 0)
+                        epilogue_tile<0>(I, tmem + buf * (2 * BN), P, L, s, merged);
+                    else
+                        epilogue_tile<1>(I, tmem + buf * (2 * BN), P, L, s, merged);
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&S.acc_empty[buf]);  // the buffer may be overwritten
+                }
+                kb_ring += kblocks;
+                ++acc_iter;
             }
-            acc_phase ^= 1u;
-        }
-        tc::fence_before_sync();
-        __syncthreads();  // the tile's outputs are written and its TMEM reads are done
-        if (threadIdx.x == 0) {
-            __threadfence();
-            if (!down) atomicAdd(&P.gu_done[it.x], 1u);
-            atomicAdd(&P.slot_done[ti.y - slot_base], 1u);
+            if (!is_mma && !is_conv) {
+                // the tile's outputs are written (or it was skipped): count it
+                asm volatile("bar.sync 2, %0;" ::"n"(kEpiWarps * 32) : "memory");
+                if (warp == 2 + kConvWarps && lane == 0) {
+                    __threadfence();
+                    if (I.kind == 0) atomicAdd(&P.gu_done[I.t], 1u);
+                    atomicAdd(&P.slot_done[I.ti.y - slot_base], 1u);
+                }
+            }
         }
     }
-    if (warp == 0) tc::tmem_dealloc(tmem, TL::TMEM_COLS);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
-int step_bn(const Shape& s) { return s.dtype == PE_BF16 ? Tile<PE_BF16>::BN : Tile<PE_FP8_BLOCK128>::BN; }
-int step_n1(const Shape& s) { return s.I / (step_bn(s) / 2); }
-int step_n2(const Shape& s) { return s.H / step_bn(s); }
+int step_n1(const Shape& s) { return s.I / (BN / 2); }
+int step_n2(const Shape& s) { return s.H / BN; }
 unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkChunk - 1) / kLinkChunk); }
 
 }  // namespace
@@ -624,7 +704,6 @@ unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkCh
 bool prefill_tc_supported(const Shape& s) {
     if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128 && s.dtype != PE_INT4_GPTQ) return false;
     if (s.dtype != PE_BF16 && (s.H > kMaxScaleCols * 128 || s.I > kMaxScaleCols * 128)) return false;
-    const int BN = step_bn(s);
     return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
 
@@ -651,8 +730,10 @@ cudaError_t prefill_setup_kernels() {
 
 cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const PrefillDev& P, const __nv_bfloat16* x,
                                  int slot_base, int T, int num_sms, cudaStream_t st) {
+    // down tiles trail their gate/up tiles by two rounds of the GEMM CTAs
+    const int gemm_ctas = num_sms - (num_sms + kLinkEvery - 1) / kLinkEvery;
     cudaError_t e = launch_pdl(prefill_align_kernel, 1, 1024, 0, st, L, s, P, slot_base, T, step_n1(s), step_n2(s),
-                               step_nchunk(s));
+                               step_nchunk(s), 2 * (gemm_ctas > 1 ? gemm_ctas : 1));
     if (e) return e;
     return launch_pdl(prefill_gather_kernel, num_sms * 4, 256, 0, st, x, P, s.H, s.k);
 }

@@ -308,37 +308,39 @@ pe_status setup_prefill(pe_handle* h) {
         const cuuint32_t b[2] = {64, 128};
         ok = ok && encode_bf16(&h->maps.h_perm, P.h_perm, 2, d, st, b);
     }
+    // weight boxes: BN/2 rows of w13 (the gate or the up half of a tile), BN rows of w2
+    const cuuint32_t r13 = kPrefillBN / 2, r2 = kPrefillBN;
     if (c.dtype == PE_INT4_GPTQ) {  // packed int4 code tiles (two codes per byte), decoded in shared memory
         {
             const cuuint64_t d[3] = {H / 2, 2 * I, nslots}, st[2] = {H / 2, stride};
-            const cuuint32_t b[3] = {32, 64, 1};
+            const cuuint32_t b[3] = {32, r13, 1};
             ok = ok && encode_map(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b, true);
         }
         {
             const cuuint64_t d[3] = {I / 2, H, nslots}, st[2] = {I / 2, stride};
-            const cuuint32_t b[3] = {32, 128, 1};
+            const cuuint32_t b[3] = {32, r2, 1};
             ok = ok && encode_map(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b, true);
         }
     } else if (c.dtype == PE_FP8_BLOCK128) {  // code tiles, decoded to bf16 in shared memory
         {
             const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H, stride};
-            const cuuint32_t b[3] = {64, 64, 1};
+            const cuuint32_t b[3] = {64, r13, 1};
             ok = ok && encode_map(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b, true);
         }
         {
             const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I, stride};
-            const cuuint32_t b[3] = {64, 128, 1};
+            const cuuint32_t b[3] = {64, r2, 1};
             ok = ok && encode_map(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b, true);
         }
     } else {
         {
             const cuuint64_t d[3] = {H, 2 * I, nslots}, st[2] = {H * 2, stride};
-            const cuuint32_t b[3] = {64, 128, 1};
+            const cuuint32_t b[3] = {64, r13, 1};
             ok = ok && encode_bf16(&h->maps.w13, h->slots + h->row.w13_offset, 3, d, st, b);
         }
         {
             const cuuint64_t d[3] = {I, H, nslots}, st[2] = {I * 2, stride};
-            const cuuint32_t b[3] = {64, 256, 1};
+            const cuuint32_t b[3] = {64, r2, 1};
             ok = ok && encode_bf16(&h->maps.w2, h->slots + h->row.w2_offset, 3, d, st, b);
         }
     }

@@ -17,6 +17,10 @@ constexpr int kPlanMaxThreads = 1024;
 constexpr int kFusedMaxEntries = 64;  // decode: one warp scans a wave's entries per weight row
 constexpr int kFp8Block = 128;
 constexpr int kInt4Group = 128;  // GPTQ int4: inputs per scale
+// Output columns of one prefill GEMM tile: a gate/up tile reads BN/2 gate and
+// BN/2 up rows of w13, a down tile BN rows of w2 (the weight tensor maps'
+// box heights).
+constexpr int kPrefillBN = 128;
 
 enum Counter { C_STEPS = 0, C_WAVES, C_ENTRIES, C_DISTINCT, C_HITS, C_PAGE_INS, C_COLD, C_NUM };
 
@@ -74,10 +78,10 @@ struct PrefillDev {
 struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
-    CUtensorMap w13;     // 3-D [L*K slots][2I][H]: bf16 64 x 128 x 1 boxes (swizzled); FP8 codes 64 x 64 x 1;
-                         //   int4 [..][2I][H/2 bytes] 32 x 64 x 1
-    CUtensorMap w2;      // 3-D [L*K slots][H][I]:  bf16 64 x 256 x 1 boxes (swizzled); FP8 codes 64 x 128 x 1;
-                         //   int4 [..][H][I/2 bytes] 32 x 128 x 1
+    CUtensorMap w13;     // 3-D [L*K slots][2I][H], boxes of BN/2 rows: bf16 64 x 64 x 1 (swizzled),
+                         //   FP8 codes 64 x 64 x 1, int4 [..][2I][H/2 bytes] 32 x 64 x 1
+    CUtensorMap w2;      // 3-D [L*K slots][H][I], boxes of BN rows: bf16 64 x 128 x 1 (swizzled),
+                         //   FP8 codes 64 x 128 x 1, int4 [..][H][I/2 bytes] 32 x 128 x 1
 };
 
 bool prefill_tc_supported(const Shape& s);
