@@ -18,8 +18,8 @@
 //           member how many GEMM tiles of its slot's earlier occupants in
 //           this step must finish before its page-in may overwrite the slot;
 //   gather  copies each entry's token row of x into the packed A operand;
-//   step    one persistent CTA per SM.  Every fourth CTA streams the host
-//           link: it copies 72 KiB chunks of the planned experts, in plan
+//   step    one persistent CTA per SM.  The CTA on every fourth SM streams
+//           the host link: it copies 64 KiB chunks of the planned experts, in plan
 //           order, from the pinned host store into their slots and counts
 //           each expert's landed chunks, then joins the GEMM CTAs.  Those
 //           take GEMM tiles from a queue in the same order (the hits of
@@ -42,8 +42,8 @@
 //   warp 1      MMA issuer: two M=128 tcgen05.mma per k-step that share the
 //               weight tile (the second only when the expert has more than
 //               128 rows), into one of two TMEM accumulator buffers;
-//   warps 2-7   converters for quantised weights (below);
-//   warps 8-11  epilogue: TMEM -> SiLU(gate)*up into h (bf16), or router
+//   warps 2-11  converters for quantised weights (below);
+//   warps 12-15 epilogue: TMEM -> SiLU(gate)*up into h (bf16), or router
 //               weight x result into the merged entries, then count the
 //               tile done.
 // With two accumulator buffers the MMAs of one tile run while the epilogue
@@ -54,7 +54,7 @@
 // Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) and GPTQ
 // int4 experts (4-bit codes, zero point 8, one fp16 scale per output row and
 // 128 inputs) keep bf16 activations: TMA brings the code tile into a staging
-// buffer, six converter warps decode it, multiply by its scale, round to bf16
+// buffer, ten converter warps decode it, multiply by its scale, round to bf16
 // and write it in the 128-byte-swizzled layout the MMA reads; the MMA then
 // runs as for bf16.  A tile's scales are staged in shared memory once per
 // tile (FP8: one row of blocks for each of its gate, up or down row ranges;
@@ -85,14 +85,14 @@ constexpr int BN = kPrefillBN;        // output columns of a tile (MMA N)
 constexpr int MT = 2 * BM;            // rows of one tile: two M=128 MMAs
 constexpr int A_BYTES = BM * BK * 2;  // one 128-row half of the A tile
 constexpr int B_BYTES = BN * BK * 2;  // the bf16 B tile
-constexpr int kConvWarps = 6;         // warps 2..7: decode quantised weight tiles (idle for bf16)
-constexpr int kEpiWarps = 4;          // warps 8..11: the epilogue (one per TMEM lane quarter)
+constexpr int kConvWarps = 10;        // warps 2..11: decode quantised weight tiles (idle for bf16)
+constexpr int kEpiWarps = 4;          // warps 12..15: the epilogue (one per TMEM lane quarter)
 constexpr int kStepThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr int kInfoDepth = 4;         // tiles the scheduler may publish ahead
 constexpr uint32_t kTmemCols = 4 * BN;  // two accumulator buffers x two 128-row halves
-constexpr int kLinkEvery = 4;         // CTAs 0, 4, 8, ... of the step stream the host link
-constexpr int kLinkUnroll = 12;
-constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 72 KiB per item
+constexpr int kLinkEvery = 4;         // the CTAs on SMs 0, 4, 8, ... stream the host link
+constexpr int kLinkUnroll = 8;
+constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 64 KiB per item
 constexpr int kMaxScaleCols = 64;     // FP8 / int4: K / 128 of either GEMM (H, I <= 8192)
 constexpr uint32_t kSpin = 1u << 22;  // polls, >= 128 ns apart
 
@@ -155,30 +155,51 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         P.slot_done[i] = 0;
     }
     if (tid == 0) {
-        // members in queue order: wave by wave; in each wave the hits (no
-        // page-in to wait for) first, then the page-ins in plan order
+        // Members in queue order, wave by wave.  In each wave: first the hits
+        // whose slots the next wave's page-ins evict, in the order those
+        // page-ins run (so the link can go on to the next wave early); then
+        // the other hits; then the page-ins in plan order (the order they
+        // land).  sh_off and sh_fill serve here as slot -> member-list index
+        // and as "queued" flags; both are set afresh below.
         const int nW = min(*L.num_waves, s.Wmax);
         int g = 0, np = 0;
+        auto emit = [&](int w, int q, int paged) {
+            const int e = L.member_expert[(size_t)w * K + q], slot = L.member_slot[(size_t)w * K + q];
+            sh_me[g] = e;
+            sh_ms[g] = slot;
+            sh_wp[g] = (w << 1) | paged;
+            P.members[g] = make_int4(e, slot, w, paged);
+            if (paged) P.pin_member[np++] = g;
+            ++g;
+        };
         for (int w = 0; w < nW; ++w) {
             const int size = L.member_count[w], nmiss = L.plan_count[w];
-            for (int pass = 0; pass < 2; ++pass) {
-                const int q0 = pass == 0 ? nmiss : 0, q1 = pass == 0 ? size : nmiss;
-                for (int q = q0; q < q1; ++q) {
-                    const int e = L.member_expert[(size_t)w * K + q], slot = L.member_slot[(size_t)w * K + q];
-                    sh_me[g] = e;
-                    sh_ms[g] = slot;
-                    sh_wp[g] = (w << 1) | pass;
-                    P.members[g] = make_int4(e, slot, w, pass);
-                    if (pass) P.pin_member[np++] = g;
-                    ++g;
+            for (int i = 0; i < K; ++i) sh_off[i] = -1;
+            for (int q = 0; q < size; ++q) {
+                sh_off[L.member_slot[(size_t)w * K + q]] = q;
+                sh_fill[q] = 0;
+            }
+            if (w + 1 < nW) {
+                const int next = L.plan_count[w + 1];
+                for (int p = 0; p < next; ++p) {
+                    const int q = sh_off[L.plan_slot[(size_t)(w + 1) * K + p]];
+                    if (q >= nmiss && q < size && !sh_fill[q]) {  // a hit of this wave
+                        sh_fill[q] = 1;
+                        emit(w, q, 0);
+                    }
                 }
             }
+            for (int q = nmiss; q < size; ++q)
+                if (!sh_fill[q]) emit(w, q, 0);
+            for (int q = 0; q < nmiss; ++q) emit(w, q, 1);
         }
         sh_G = g;
         P.counts[3] = g;
         P.counts[4] = np;
         P.ctl[0] = 0;  // GEMM ticket
         P.ctl[1] = 0;  // abort word
+        P.ctl[2] = 0;  // link CTAs registered
+        P.ctl[3] = 0;  // GEMM CTAs registered
     }
     __syncthreads();
     const int G = sh_G;
@@ -285,7 +306,7 @@ __global__ void __launch_bounds__(256) prefill_gather_kernel(const __nv_bfloat16
 
 // ---------------------------------------------------------------- link role
 
-// One 72 KiB item (a multiple of 16 bytes, possibly shorter at the row end).
+// One 64 KiB item (a multiple of 16 bytes, possibly shorter at the row end).
 __device__ __forceinline__ void link_copy(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t bytes) {
     const int4* sp = reinterpret_cast<const int4*>(src);
     int4* dp = reinterpret_cast<int4*>(dst);
@@ -389,7 +410,7 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmA, const CUten
     }
 }
 
-// Converters (warps 2..7): decode the tile's weight codes into the
+// Converters (warps 2..11): decode the tile's weight codes into the
 // swizzled bf16 B tile of each stage, applying the scales.
 template <int EPI, int FMT>
 __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float* scale, __half* scale4,
@@ -494,7 +515,7 @@ __device__ __forceinline__ void mma_tile(StepShared& S, uint8_t* ring, const Til
     }
 }
 
-// Epilogue (warps 8..11): warp w reads TMEM lanes 32*(w%4).. of the
+// Epilogue (warps 12..15): warp w reads TMEM lanes 32*(w%4).. of the
 // accumulator buffer; in row half hf, lane l owns tile row hf*128 + 32*(w%4) + l.
 template <int EPI>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, const PrefillDev& P, const LayerDev& L,
@@ -560,14 +581,37 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     __shared__ StepShared S;
     __shared__ float sh_scale[FMT == PE_FP8_BLOCK128 ? 2 * kMaxScaleCols : 1];
     __shared__ __align__(16) __half sh_scale4[FMT == PE_INT4_GPTQ ? BN * kMaxScaleCols : 8];
-    __shared__ int sh_ok;
+    __shared__ int sh_ok, sh_rank, sh_nlink;
     pdl_wait();
-    pdl_trigger();
-    if (blockIdx.x % kLinkEvery == 0) {
+    // Roles follow the SM (every kLinkEvery-th SM streams the link), so they
+    // stay spread over the GPU wherever the CTAs were placed.  Each CTA takes
+    // a rank in its role; the link CTAs need their number.
+    if (threadIdx.x == 0) {
+        unsigned smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        const bool link = smid % kLinkEvery == 0;
+        int rank = (int)atomicAdd(&P.ctl[link ? 2 : 3], 1u);
+        int nlink = 0;
+        for (uint32_t i = 0; i < kSpin; ++i) {  // every CTA of the grid is resident: registration ends
+            if (ld_acquire(&P.ctl[2]) + ld_acquire(&P.ctl[3]) >= gridDim.x) break;
+            __nanosleep(64);
+        }
+        nlink = (int)ld_acquire(&P.ctl[2]);
+        if (nlink == 0 && !link && rank == 0) {  // no SM of the link's kind: the first GEMM CTA streams it
+            nlink = 1;
+            rank = 0;
+            sh_rank = 0;
+        } else {
+            sh_rank = link ? rank : -1;
+        }
+        sh_nlink = nlink == 0 ? 1 : nlink;
+    }
+    __syncthreads();
+    if (sh_rank >= 0) {
         // a link CTA joins the GEMM queue once its share of the page-ins is
         // done (it then depends only on work queued before its next tile)
-        link_role(P, s, host_layer, slots_all + (size_t)slot_base * s.stride, blockIdx.x / kLinkEvery,
-                  (gridDim.x + kLinkEvery - 1) / kLinkEvery, nchunk, err, &sh_ok);
+        link_role(P, s, host_layer, slots_all + (size_t)slot_base * s.stride, sh_rank, sh_nlink, nchunk, err,
+                  &sh_ok);
         __syncthreads();
     }
 
@@ -693,6 +737,9 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+    // The next kernel is released only now: launched early, its CTAs were
+    // measured to slow this multi-millisecond step down by about 10 %.
+    pdl_trigger();
 }
 
 int step_n1(const Shape& s) { return s.I / (BN / 2); }

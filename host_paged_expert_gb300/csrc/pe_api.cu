@@ -203,7 +203,7 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         pre.landed = cv.take<unsigned>(E);
         pre.gu_done = cv.take<unsigned>(tiles);
         pre.slot_done = cv.take<unsigned>(K);
-        pre.ctl = cv.take<unsigned>(2);
+        pre.ctl = cv.take<unsigned>(4);
         pre.counts = cv.take<int32_t>(8);
         pre.max_rows = (int)rows;
         pre.max_tiles = (int)tiles;

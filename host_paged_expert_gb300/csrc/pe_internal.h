@@ -69,7 +69,7 @@ struct PrefillDev {
     unsigned* landed;       // [E]            landed page-in chunks per member
     unsigned* gu_done;      // [max_tiles]    finished gate/up tiles per row tile
     unsigned* slot_done;    // [K]            finished GEMM tiles per slot in this step
-    unsigned* ctl;          // [2]            GEMM ticket, abort word
+    unsigned* ctl;          // [4]            GEMM ticket, abort word, link / GEMM CTAs registered
     int32_t* counts;        // [8]            tiles, rows, items, members, page-ins
     int max_rows, max_tiles, max_items;
 };
