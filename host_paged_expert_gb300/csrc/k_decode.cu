@@ -178,6 +178,10 @@ __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2
 // chunks past the row are skipped,
 // so the arithmetic is that of the exact chunk counts.
 constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
+// int4 rows are short (H/2 and I/2 bytes), so an int4 down item takes
+// kRowsD4 rows to keep enough bytes in flight (a gate/up item stays one row
+// pair: two spill registers); the per-row arithmetic is unchanged.
+constexpr int kRowsG4 = 1, kRowsD4 = 8;
 // FMT: the expert format (PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ).
 template <int EPL, int FMT>
 __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
@@ -262,13 +266,16 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
 
     const int nchunk = s.H >> 3;
     const size_t row_bytes = (size_t)s.H * 2;
-    const long long miss_rows = (long long)count * s.I;
+    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;  // gate/up row pairs per item
+    constexpr int RD = FMT == PE_INT4_GPTQ ? kRowsD4 : kRowsD;  // down rows per item
+    const int ipe = s.I / RPI;  // gate/up items per expert
+    const long long miss_rows = (long long)count * ipe;
     const size_t tail_bytes = s.copy_bytes - s.tail_off;
     const long long copies_per = (long long)((tail_bytes + kCopyItem - 1) / kCopyItem);
     const long long link_items = miss_rows + (long long)count * copies_per;
-    const long long hbm_items = (long long)(size - count) * s.I;
+    const long long hbm_items = (long long)(size - count) * ipe;
     const int G = gridDim.x;
-    const int row_blocks = (s.H + kRowsD - 1) / kRowsD;
+    const int row_blocks = (s.H + RD - 1) / RD;
     // roles: registration is complete long before the plan is (bounded wait)
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < kSpinLimit; ++i) {
@@ -313,25 +320,30 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                     }
                     continue;
                 }
-                const int mq = as_link ? (int)(item / s.I) : count + (int)(item / s.I);
-                const int n = (int)(item % s.I);
+                const int mq = as_link ? (int)(item / ipe) : count + (int)(item / ipe);
+                const int n = (int)(item % ipe) * RPI;  // first row pair of the item
                 const int slot = sh_mslot[mq];
                 if constexpr (FMT == PE_INT4_GPTQ) {
                     uint8_t* slot_base = slots + (size_t)slot * s.stride;
                     const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
                     const int nch4 = s.H >> 5;
-                    int4 gv[CPLH4], uv[CPLH4];
-                    float sg[CPLH4], su[CPLH4];
-                    load_row_pair_int4<CPLH4>(rbase, s, n, lane, nch4, as_link, false, gv, uv, sg, su);
-                    if (as_link) {
-                        uint8_t* gd = slot_base + s.w13_off + (size_t)n * (s.H / 2);
-                        uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
+                    int4 gv[RPI][CPLH4], uv[RPI][CPLH4];
+                    float sg[RPI][CPLH4], su[RPI][CPLH4];
 #pragma unroll
-                        for (int c = 0; c < CPLH4; ++c) {
-                            const int idx = lane + 32 * c;
-                            if (idx < nch4) {
-                                *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[c];
-                                *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[c];
+                    for (int r = 0; r < RPI; ++r)
+                        load_row_pair_int4<CPLH4>(rbase, s, n + r, lane, nch4, as_link, false, gv[r], uv[r], sg[r], su[r]);
+                    if (as_link) {
+#pragma unroll
+                        for (int r = 0; r < RPI; ++r) {
+                            uint8_t* gd = slot_base + s.w13_off + (size_t)(n + r) * (s.H / 2);
+                            uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
+#pragma unroll
+                            for (int c = 0; c < CPLH4; ++c) {
+                                const int idx = lane + 32 * c;
+                                if (idx < nch4) {
+                                    *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[r][c];
+                                    *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[r][c];
+                                }
                             }
                         }
                     }
@@ -341,9 +353,12 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                         while (mask) {
                             const int ei = b0 + __ffs(mask) - 1;
                             mask &= mask - 1;
-                            const float hval = row_pair_h_int4<CPLH4>(gv, uv, sg, su,
-                                                                      xbase + (size_t)(ei / s.k) * s.H * 2, lane, nch4);
-                            if (lane == 0) hbuf[(size_t)ei * s.I + n] = hval;
+                            const uint8_t* xr = xbase + (size_t)(ei / s.k) * s.H * 2;
+#pragma unroll
+                            for (int r = 0; r < RPI; ++r) {
+                                const float hval = row_pair_h_int4<CPLH4>(gv[r], uv[r], sg[r], su[r], xr, lane, nch4);
+                                if (lane == 0) hbuf[(size_t)ei * s.I + n + r] = hval;
+                            }
                         }
                     }
                     continue;
@@ -437,7 +452,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
         const float we = __ldcg(L.topk_w + e);
         if constexpr (FMT == PE_INT4_GPTQ)
-            down_rows_int4<CPLI4, kRowsD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
+            down_rows_int4<CPLI4, RD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
                                           hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true, merged + (size_t)e * s.H,
                                           nullptr, lane);
         else if constexpr (FMT == PE_FP8_BLOCK128)
@@ -454,7 +469,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         const long long items = (long long)sh_nhit * row_blocks;
         for (long long it = (long long)rank * kWp + warp; it < items; it += (long long)hbm_ctas * kWp) {
             const int e = sh_hit_list[it / row_blocks];
-            const int m0 = (int)(it % row_blocks) * kRowsD;
+            const int m0 = (int)(it % row_blocks) * RD;
             down_entry(e, m0);
         }
     }
@@ -464,7 +479,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         const long long items = (long long)sh_nmiss * row_blocks;
         for (long long it = (long long)blockIdx.x * kWp + warp; it < items; it += (long long)G * kWp) {
             const int e = sh_miss_list[it / row_blocks];
-            const int m0 = (int)(it % row_blocks) * kRowsD;
+            const int m0 = (int)(it % row_blocks) * RD;
             down_entry(e, m0);
         }
     }

@@ -145,15 +145,35 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
     __shared__ int sh_t0[kMaxExperts + 1], sh_i0[kMaxExperts], sh_d0[kMaxExperts];  // tiles, gate/up and down queue bases
     __shared__ int sh_cum[kMaxSlots];
     __shared__ int sh_G;
+    // the plan's member and page-in lists, copied in parallel so that the
+    // serial passes below read shared memory only: [Wmax] member counts,
+    // [Wmax] page-in counts, [Wmax*K] member experts, member slots, page-in slots
+    extern __shared__ int sh_plan[];
+    int* sh_mcount = sh_plan;
+    int* sh_pcount = sh_mcount + s.Wmax;
+    int* sh_mexp = sh_pcount + s.Wmax;
+    int* sh_mslot = sh_mexp + s.Wmax * s.K;
+    int* sh_pslot = sh_mslot + s.Wmax * s.K;
     pdl_wait();
     pdl_trigger();
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int nent = T * s.k, K = s.K;
+    const int nW = min(*L.num_waves, s.Wmax);
     for (int e = tid; e < s.E; e += nthr) sh_g_of_e[e] = -1;
     for (int i = tid; i < K; i += nthr) {
         sh_cum[i] = 0;
         P.slot_done[i] = 0;
     }
+    for (int w = tid; w < nW; w += nthr) {
+        sh_mcount[w] = L.member_count[w];
+        sh_pcount[w] = L.plan_count[w];
+    }
+    for (int i = tid; i < nW * K; i += nthr) {
+        sh_mexp[i] = L.member_expert[i];
+        sh_mslot[i] = L.member_slot[i];
+        sh_pslot[i] = L.plan_slot[i];
+    }
+    __syncthreads();
     if (tid == 0) {
         // Members in queue order, wave by wave.  In each wave: first the hits
         // whose slots the next wave's page-ins evict, in the order those
@@ -161,10 +181,9 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         // the other hits; then the page-ins in plan order (the order they
         // land).  sh_off and sh_fill serve here as slot -> member-list index
         // and as "queued" flags; both are set afresh below.
-        const int nW = min(*L.num_waves, s.Wmax);
         int g = 0, np = 0;
         auto emit = [&](int w, int q, int paged) {
-            const int e = L.member_expert[(size_t)w * K + q], slot = L.member_slot[(size_t)w * K + q];
+            const int e = sh_mexp[w * K + q], slot = sh_mslot[w * K + q];
             sh_me[g] = e;
             sh_ms[g] = slot;
             sh_wp[g] = (w << 1) | paged;
@@ -173,16 +192,16 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             ++g;
         };
         for (int w = 0; w < nW; ++w) {
-            const int size = L.member_count[w], nmiss = L.plan_count[w];
+            const int size = sh_mcount[w], nmiss = sh_pcount[w];
             for (int i = 0; i < K; ++i) sh_off[i] = -1;
             for (int q = 0; q < size; ++q) {
-                sh_off[L.member_slot[(size_t)w * K + q]] = q;
+                sh_off[sh_mslot[w * K + q]] = q;
                 sh_fill[q] = 0;
             }
             if (w + 1 < nW) {
-                const int next = L.plan_count[w + 1];
+                const int next = sh_pcount[w + 1];
                 for (int p = 0; p < next; ++p) {
-                    const int q = sh_off[L.plan_slot[(size_t)(w + 1) * K + p]];
+                    const int q = sh_off[sh_pslot[(w + 1) * K + p]];
                     if (q >= nmiss && q < size && !sh_fill[q]) {  // a hit of this wave
                         sh_fill[q] = 1;
                         emit(w, q, 0);
@@ -745,11 +764,14 @@ __global__ void __launch_bounds__(kStepThreads, 1)
 int step_n1(const Shape& s) { return s.I / (BN / 2); }
 int step_n2(const Shape& s) { return s.H / BN; }
 unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkChunk - 1) / kLinkChunk); }
+size_t align_smem(const Shape& s) { return sizeof(int) * ((size_t)2 * s.Wmax + (size_t)3 * s.Wmax * s.K); }
+constexpr size_t kAlignMaxSmem = 160 * 1024;  // dynamic shared memory the align kernel may use
 
 }  // namespace
 
 bool prefill_tc_supported(const Shape& s) {
     if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128 && s.dtype != PE_INT4_GPTQ) return false;
+    if (align_smem(s) > kAlignMaxSmem) return false;
     if (s.dtype != PE_BF16 && (s.H > kMaxScaleCols * 128 || s.I > kMaxScaleCols * 128)) return false;
     return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
@@ -764,7 +786,9 @@ size_t prefill_max_rows(int max_entries, int E) {
 size_t prefill_max_items(const Shape& s, size_t max_tiles) { return max_tiles * (size_t)(step_n1(s) + step_n2(s)); }
 
 cudaError_t prefill_setup_kernels() {
-    cudaError_t e = cudaFuncSetAttribute(prefill_step_kernel<PE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_align_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kAlignMaxSmem);
+    if (!e) e = cudaFuncSetAttribute(prefill_step_kernel<PE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Tile<PE_BF16>::SMEM);
     if (!e)
         e = cudaFuncSetAttribute(prefill_step_kernel<PE_FP8_BLOCK128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -779,8 +803,8 @@ cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const Prefil
                                  int slot_base, int T, int num_sms, cudaStream_t st) {
     // down tiles trail their gate/up tiles by two rounds of the GEMM CTAs
     const int gemm_ctas = num_sms - (num_sms + kLinkEvery - 1) / kLinkEvery;
-    cudaError_t e = launch_pdl(prefill_align_kernel, 1, 1024, 0, st, L, s, P, slot_base, T, step_n1(s), step_n2(s),
-                               step_nchunk(s), 2 * (gemm_ctas > 1 ? gemm_ctas : 1));
+    cudaError_t e = launch_pdl(prefill_align_kernel, 1, 1024, align_smem(s), st, L, s, P, slot_base, T, step_n1(s),
+                               step_n2(s), step_nchunk(s), 2 * (gemm_ctas > 1 ? gemm_ctas : 1));
     if (e) return e;
     return launch_pdl(prefill_gather_kernel, num_sms * 4, 256, 0, st, x, P, s.H, s.k);
 }
