@@ -182,7 +182,8 @@ def measured_peaks():
 # The sources each timed kernel is compiled from: a DRAM-traffic record is
 # reported only while these still hash to the value it was captured on.
 KERNEL_SOURCES = {
-    "decode_step": ("k_decode.cu", "plan_block.cuh", "pe_device.cuh", "fp8_device.cuh", "pe_internal.h"),
+    "decode_step": ("k_decode.cu", "plan_block.cuh", "pe_device.cuh", "fp8_device.cuh", "int4_device.cuh",
+                    "pe_internal.h"),
     "prefill_step": ("k_prefill.cu", "tc_sm100.cuh", "pe_device.cuh", "fp8_device.cuh", "pe_internal.h"),
 }
 

@@ -130,6 +130,42 @@ __device__ __forceinline__ int spin_geq(const unsigned* p, unsigned target, unsi
 
 // ---------------------------------------------------------------- align
 
+// Exclusive prefix sum of v over the threads of the block, in thread order;
+// every thread calls it and gets the block total in *total.  sh: 32 ints.
+__device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nw ? sh[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += y;
+        }
+        sh[lane] = t;
+    }
+    __syncthreads();
+    const int base = warp > 0 ? sh[warp - 1] : 0;
+    *total = sh[nw - 1];
+    __syncthreads();  // sh may be reused
+    return base + x - v;
+}
+
+// Lays out one prefill step (one CTA of 1024 threads; E, K <= 1024, so thread
+// i owns member i, slot i or page-in i in each pass).
+//
+// Members in queue order, wave by wave.  In each wave: first the hits whose
+// slots the next wave's page-ins evict, in the order those page-ins run (so
+// the link can go on to the next wave early); then the other hits; then the
+// page-ins in plan order (the order they land).
+//
 // The GEMM queue, wave by wave: each member's gate/up tiles in member order,
 // and its down tiles `lag` items later (so that a CTA taking a down tile
 // rarely waits for the member's gate/up tiles), never past the end of the
@@ -144,10 +180,10 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
     __shared__ int sh_cnt[kMaxExperts], sh_off[kMaxExperts], sh_fill[kMaxExperts];
     __shared__ int sh_t0[kMaxExperts + 1], sh_i0[kMaxExperts], sh_d0[kMaxExperts];  // tiles, gate/up and down queue bases
     __shared__ int sh_cum[kMaxSlots];
-    __shared__ int sh_G;
-    // the plan's member and page-in lists, copied in parallel so that the
-    // serial passes below read shared memory only: [Wmax] member counts,
-    // [Wmax] page-in counts, [Wmax*K] member experts, member slots, page-in slots
+    __shared__ int sh_scan[32];
+    // the plan's member and page-in lists, copied in parallel: [Wmax] member
+    // counts, [Wmax] page-in counts, [Wmax*K] member experts, member slots,
+    // page-in slots
     extern __shared__ int sh_plan[];
     int* sh_mcount = sh_plan;
     int* sh_pcount = sh_mcount + s.Wmax;
@@ -173,55 +209,61 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         sh_mslot[i] = L.member_slot[i];
         sh_pslot[i] = L.plan_slot[i];
     }
-    __syncthreads();
     if (tid == 0) {
-        // Members in queue order, wave by wave.  In each wave: first the hits
-        // whose slots the next wave's page-ins evict, in the order those
-        // page-ins run (so the link can go on to the next wave early); then
-        // the other hits; then the page-ins in plan order (the order they
-        // land).  sh_off and sh_fill serve here as slot -> member-list index
-        // and as "queued" flags; both are set afresh below.
-        int g = 0, np = 0;
-        auto emit = [&](int w, int q, int paged) {
-            const int e = sh_mexp[w * K + q], slot = sh_mslot[w * K + q];
-            sh_me[g] = e;
-            sh_ms[g] = slot;
-            sh_wp[g] = (w << 1) | paged;
-            P.members[g] = make_int4(e, slot, w, paged);
-            if (paged) P.pin_member[np++] = g;
-            ++g;
-        };
-        for (int w = 0; w < nW; ++w) {
-            const int size = sh_mcount[w], nmiss = sh_pcount[w];
-            for (int i = 0; i < K; ++i) sh_off[i] = -1;
-            for (int q = 0; q < size; ++q) {
-                sh_off[sh_mslot[w * K + q]] = q;
-                sh_fill[q] = 0;
-            }
-            if (w + 1 < nW) {
-                const int next = sh_pcount[w + 1];
-                for (int p = 0; p < next; ++p) {
-                    const int q = sh_off[sh_pslot[(w + 1) * K + p]];
-                    if (q >= nmiss && q < size && !sh_fill[q]) {  // a hit of this wave
-                        sh_fill[q] = 1;
-                        emit(w, q, 0);
-                    }
-                }
-            }
-            for (int q = nmiss; q < size; ++q)
-                if (!sh_fill[q]) emit(w, q, 0);
-            for (int q = 0; q < nmiss; ++q) emit(w, q, 1);
-        }
-        sh_G = g;
-        P.counts[3] = g;
-        P.counts[4] = np;
         P.ctl[0] = 0;  // GEMM ticket
         P.ctl[1] = 0;  // abort word
         P.ctl[2] = 0;  // link CTAs registered
         P.ctl[3] = 0;  // GEMM CTAs registered
     }
     __syncthreads();
-    const int G = sh_G;
+
+    // ---- members in queue order (sh_off: slot -> member-list index of the
+    // wave, sh_fill: next-wave page-in rank of a hit, sh_cnt: queue position
+    // of the needed hits by that rank; all three are set afresh below)
+    int gbase = 0, npbase = 0;
+    for (int w = 0; w < nW; ++w) {
+        const int size = sh_mcount[w], nmiss = sh_pcount[w], next = w + 1 < nW ? sh_pcount[w + 1] : 0;
+        for (int i = tid; i < K; i += nthr) sh_off[i] = -1;
+        if (tid < size) sh_fill[tid] = -1;
+        __syncthreads();
+        if (tid < size) sh_off[sh_mslot[w * K + tid]] = tid;
+        __syncthreads();
+        int q_of_p = -1;
+        if (tid < next) {
+            const int q = sh_off[sh_pslot[(w + 1) * K + tid]];
+            if (q >= nmiss && q < size) {  // the next wave evicts this wave's hit q
+                q_of_p = q;
+                sh_fill[q] = tid;
+            }
+        }
+        int n_needed;
+        const int pos_needed = block_excl_scan(q_of_p >= 0 ? 1 : 0, sh_scan, &n_needed);
+        if (q_of_p >= 0) sh_cnt[tid] = pos_needed;
+        __syncthreads();
+        const bool hit = tid >= nmiss && tid < size;
+        const bool other = hit && sh_fill[tid] < 0;
+        int n_other;
+        const int pos_other = block_excl_scan(other ? 1 : 0, sh_scan, &n_other);
+        if (tid < size) {
+            const int q = tid, paged = q < nmiss;
+            const int pos = paged ? n_needed + n_other + q : other ? n_needed + pos_other : sh_cnt[sh_fill[q]];
+            const int g = gbase + pos;
+            const int e = sh_mexp[w * K + q], slot = sh_mslot[w * K + q];
+            sh_me[g] = e;
+            sh_ms[g] = slot;
+            sh_wp[g] = (w << 1) | paged;
+            P.members[g] = make_int4(e, slot, w, paged);
+            if (paged) P.pin_member[npbase + q] = g;
+        }
+        gbase += size;
+        npbase += nmiss;
+        __syncthreads();
+    }
+    const int G = gbase;
+    if (tid == 0) {
+        P.counts[3] = G;
+        P.counts[4] = npbase;
+    }
     for (int g = tid; g < G; g += nthr) {
         sh_g_of_e[sh_me[g]] = g;
         sh_cnt[g] = 0;
@@ -234,21 +276,36 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             if (g >= 0) atomicAdd(&sh_cnt[g], 1);
         }
     __syncthreads();
-    if (tid == 0) {
-        int off = 0, nt = 0;
-        for (int g = 0; g < G; ++g) {
-            const int c = sh_cnt[g], slot = sh_ms[g];
-            sh_off[g] = off;
-            sh_t0[g] = nt;
-            for (int r = 0; r < c && nt < P.max_tiles; r += MT)
-                P.tiles[nt++] = make_int4(off + r, slot_base + slot, min(MT, c - r), g);
-            const int work = (nt - sh_t0[g]) * (n1 + n2);
-            // GEMM tiles of this slot's earlier occupants (members are in wave order)
-            P.slot_need[g] = sh_cum[slot];
-            sh_cum[slot] += work;
-            off += (c + BM - 1) / BM * BM;
+
+    // ---- row ranges and tiles: member g's rows are padded to 128, its tiles
+    // hold up to 256 rows
+    const int c = tid < G ? sh_cnt[tid] : 0;
+    const int mt = (c + MT - 1) / MT;
+    int rows_total, nt;
+    const int off = block_excl_scan((c + BM - 1) / BM * BM, sh_scan, &rows_total);
+    const int t0 = block_excl_scan(mt, sh_scan, &nt);
+    if (tid < G) {
+        sh_off[tid] = off;
+        sh_t0[tid] = t0;
+        for (int i = 0; i < mt && t0 + i < P.max_tiles; ++i)
+            P.tiles[t0 + i] = make_int4(off + i * MT, slot_base + sh_ms[tid], min(MT, c - i * MT), tid);
+    }
+    if (tid == 0) sh_t0[G] = nt;
+    // GEMM tiles of each slot's earlier occupants: members are in wave order
+    // and a slot holds one member per wave
+    {
+        int wb = 0;
+        for (int w = 0; w < nW; ++w) {
+            const int size = sh_mcount[w];
+            const bool mine = tid >= wb && tid < wb + size;
+            if (mine) P.slot_need[tid] = sh_cum[sh_ms[tid]];
+            __syncthreads();
+            if (mine) sh_cum[sh_ms[tid]] += mt * (n1 + n2);
+            __syncthreads();
+            wb += size;
         }
-        sh_t0[G] = nt;
+    }
+    if (tid == 0) {
         // queue bases: gate/up blocks in member order, each down block once
         // `lag` more items have been queued, flushed at every wave's end
         int ni = 0, head = 0;
@@ -270,7 +327,7 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             ni += (sh_t0[head + 1] - sh_t0[head]) * n2;
         }
         P.counts[0] = nt;
-        P.counts[1] = off <= P.max_rows ? off : P.max_rows;
+        P.counts[1] = rows_total <= P.max_rows ? rows_total : P.max_rows;
         P.counts[2] = ni <= P.max_items ? ni : P.max_items;
     }
     __syncthreads();
@@ -286,7 +343,7 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
                 if (j < P.max_items) P.items[j] = make_int2(t, 0x10000 | n);
         P.landed[g] = (sh_wp[g] & 1) ? 0u : nchunk;  // a hit is ready at once
     }
-    for (int t = tid; t < sh_t0[G]; t += nthr) P.gu_done[t] = 0;
+    for (int t = tid; t < nt; t += nthr) P.gu_done[t] = 0;
     for (int i = tid; i < nent; i += nthr)
         if (L.entry_wave[i] >= 0) {
             const int g = sh_g_of_e[L.topk_id[i]];
@@ -294,9 +351,11 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             const int row = sh_off[g] + atomicAdd(&sh_fill[g], 1);
             if (row < P.max_rows) P.perm[row] = i;
         }
-    for (int g = 0; g < G; ++g) {
-        const int c = sh_cnt[g], padded = (c + BM - 1) / BM * BM;
-        for (int r = c + tid; r < padded; r += nthr)
+    // padding rows: one warp per member
+    const int lane = tid & 31;
+    for (int g = tid >> 5; g < G; g += nthr >> 5) {
+        const int cg = sh_cnt[g], padded = (cg + BM - 1) / BM * BM;
+        for (int r = cg + lane; r < padded; r += 32)
             if (sh_off[g] + r < P.max_rows) P.perm[sh_off[g] + r] = -1;
     }
 }
