@@ -29,7 +29,7 @@ EXPORTS = [
     "pe_create_shared",
     "pe_load_host_expert", "pe_host_row", "pe_forward", "pe_stats", "pe_read_plan", "pe_read_residency",
     "pe_read_slot", "pe_reset_residency", "pe_probe_host_link", "pe_profile_enable", "pe_profile_read",
-    "pe_destroy", "pe_last_error", "pe_expert_mlp_noalloc",
+    "pe_destroy", "pe_last_error", "pe_expert_mlp_noalloc", "pe_selftest_bounded_waits",
 ]
 
 
@@ -124,6 +124,16 @@ def make_config(shape: MoEShape, max_tokens: int, device: int = 0) -> PEConfig:
 def required_device_bytes(shape: MoEShape, max_tokens: int) -> int:
     cfg = make_config(shape, max_tokens)
     return int(lib().pe_required_device_bytes(byref(cfg)))
+
+
+def selftest_bounded_waits(poll_limit: int = 1 << 16) -> list[int]:
+    """Error words of the three bounded-wait kinds run on never-true
+    conditions (each must read PE_DEVERR_TIMEOUT)."""
+    out = (ctypes.c_uint32 * 3)()
+    st = lib().pe_selftest_bounded_waits(ctypes.c_uint32(poll_limit), out)
+    if st != PE_OK:
+        raise PEError(st, lib().pe_last_error(None).decode())
+    return [int(v) for v in out]
 
 
 def slots_for_budget(shape: MoEShape, max_tokens: int, budget_bytes: int) -> int:

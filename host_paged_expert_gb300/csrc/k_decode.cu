@@ -73,10 +73,11 @@ __device__ __forceinline__ void cta_arrive(unsigned* ctr) {
 
 // Wait (thread 0 polls, the CTA waits at the barrier) until *ctr >= target.
 // Gives up after kSpinLimit polls, records PE_DEVERR_TIMEOUT and returns false.
-__device__ __forceinline__ bool cta_wait(const unsigned* ctr, unsigned target, uint32_t* err, int* flag_sh) {
+__device__ __forceinline__ bool cta_wait(const unsigned* ctr, unsigned target, uint32_t* err, int* flag_sh,
+                                         uint32_t limit = kSpinLimit) {
     if (threadIdx.x == 0) {
         int ok = 0;
-        for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        for (uint32_t i = 0; i < limit; ++i) {
             if (ld_acquire_u32(ctr) >= target) {
                 ok = 1;
                 break;
@@ -509,7 +510,18 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     }
 }
 
+// Self-test: a phase wait on a counter nothing increments must give up.
+__global__ void decode_wait_selftest_kernel(const unsigned* never, uint32_t* err, uint32_t limit) {
+    __shared__ int sh_flag;
+    cta_wait(never, 1u, err, &sh_flag, limit);
+}
+
 }  // namespace
+
+cudaError_t selftest_decode_wait(const unsigned* never, uint32_t* err, uint32_t limit, cudaStream_t st) {
+    decode_wait_selftest_kernel<<<1, 128, 0, st>>>(never, err, limit);
+    return cudaGetLastError();
+}
 
 int decode_fused_sync_words() { return S_NUM; }
 

@@ -117,8 +117,9 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 // Thread-level bounded wait for *p >= target.  Gives up at once when the
 // step's abort word is set; running out of polls records the timeout and
 // sets the abort word.
-__device__ __forceinline__ int spin_geq(const unsigned* p, unsigned target, unsigned* abort_w, uint32_t* err) {
-    for (uint32_t i = 0; i < kSpin; ++i) {
+__device__ __forceinline__ int spin_geq(const unsigned* p, unsigned target, unsigned* abort_w, uint32_t* err,
+                                        uint32_t limit = kSpin) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (ld_acquire(p) >= target) return 1;
         if (*reinterpret_cast<volatile unsigned*>(abort_w)) return 0;
         __nanosleep(128);
@@ -820,6 +821,21 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     pdl_trigger();
 }
 
+// Self-tests: a counter wait on a word nothing sets, and an mbarrier wait on
+// a barrier nobody arrives on, must give up (and the counter wait must raise
+// the abort word, after which a second wait gives up at once).
+__global__ void prefill_wait_selftest_kernel(const unsigned* never, unsigned* abort_w, uint32_t* err_counter,
+                                             uint32_t* err_mbar, uint32_t limit) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        spin_geq(never, 1u, abort_w, err_counter, limit);
+        spin_geq(never, 1u, abort_w, err_counter, 4 * limit);  // the abort word ends it at once
+        tc::mbar_init(&bar, 1);
+        tc::fence_barrier_init();
+        tc::mbar_wait(&bar, 0, err_mbar, PE_DEVERR_TIMEOUT, limit);
+    }
+}
+
 int step_n1(const Shape& s) { return s.I / (BN / 2); }
 int step_n2(const Shape& s) { return s.H / BN; }
 unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkChunk - 1) / kLinkChunk); }
@@ -856,6 +872,12 @@ cudaError_t prefill_setup_kernels() {
         e = cudaFuncSetAttribute(prefill_step_kernel<PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Tile<PE_INT4_GPTQ>::SMEM);
     return e;
+}
+
+cudaError_t selftest_prefill_waits(const unsigned* never, unsigned* abort_w, uint32_t* err_counter,
+                                   uint32_t* err_mbar, uint32_t limit, cudaStream_t st) {
+    prefill_wait_selftest_kernel<<<1, 32, 0, st>>>(never, abort_w, err_counter, err_mbar, limit);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const PrefillDev& P, const __nv_bfloat16* x,

@@ -774,6 +774,31 @@ pe_status pe_reset_residency(pe_handle* h, void* stream) {
     return reset_state(h, static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+// Words of the bounded-wait self-test: a word nothing ever sets, the abort
+// word, and one error word per wait kind.
+__device__ unsigned g_selftest_words[8];
+}  // namespace
+
+pe_status pe_selftest_bounded_waits(uint32_t poll_limit, uint32_t* out3) {
+    if (!out3 || poll_limit == 0) return fail(nullptr, PE_ERR_INVALID, "out3 must not be NULL and poll_limit > 0");
+    unsigned* w = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&w), g_selftest_words);
+    if (!e) e = cudaMemset(w, 0, sizeof(unsigned) * 8);
+    // w[0]: never set; w[1]: abort word; w[2..4]: error words
+    if (!e) e = selftest_prefill_waits(w, w + 1, w + 2, w + 3, poll_limit, 0);
+    if (!e) e = selftest_decode_wait(w, w + 4, poll_limit, 0);
+    if (!e) e = cudaDeviceSynchronize();
+    unsigned host[8] = {};
+    if (!e) e = cudaMemcpy(host, w, sizeof(host), cudaMemcpyDeviceToHost);
+    if (e) return fail(nullptr, PE_ERR_CUDA, std::string("bounded-wait self-test: ") + cudaGetErrorString(e));
+    out3[0] = host[2];  // prefill step counter wait
+    out3[1] = host[3];  // mbarrier wait
+    out3[2] = host[4];  // decode step phase wait
+    if (host[1] != 1u) out3[0] |= 0x80000000u;  // the abort word must have been raised
+    return PE_OK;
+}
+
 pe_status pe_probe_host_link(pe_handle* h, void* dev_dst, size_t bytes, int32_t iters, void* stream,
                              double* copy_engine_gbs, double* kernel_gbs) {
     if (!h || !dev_dst || iters < 1) return PE_ERR_INVALID;

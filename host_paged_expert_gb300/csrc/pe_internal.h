@@ -99,6 +99,12 @@ cudaError_t launch_prefill_step(const LayerDev& L, const Shape& s, const Prefill
                                 const uint8_t* host_layer, uint8_t* slots_all, int slot_base, float* merged,
                                 uint32_t* err, int num_sms, cudaStream_t st);
 
+// Self-tests of the bounded waits (each wait runs on a condition that never
+// becomes true and must give up after `limit` polls, recording the timeout).
+cudaError_t selftest_decode_wait(const unsigned* never, uint32_t* err, uint32_t limit, cudaStream_t st);
+cudaError_t selftest_prefill_waits(const unsigned* never, unsigned* abort_w, uint32_t* err_counter,
+                                   uint32_t* err_mbar, uint32_t limit, cudaStream_t st);
+
 // Records the message pe_last_error(NULL) returns in this thread.
 void set_thread_error(const char* msg);
 

@@ -53,9 +53,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the barrier phase with the given parity; gives up after a bounded
-// number of polls (about 2 s), records `err_bit` in *err and returns false.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t err_bit) {
-    for (uint32_t i = 0; i < (1u << 26); ++i) {
+// number of polls (about 2 s by default), records `err_bit` in *err and
+// returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err, uint32_t err_bit,
+                                          uint32_t limit = 1u << 26) {
+    for (uint32_t i = 0; i < limit; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i >= 16) __nanosleep(32);
     }

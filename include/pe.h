@@ -232,6 +232,20 @@ pe_status pe_read_slot(pe_handle* h, int32_t layer, int32_t slot, void* host_dst
  * error word are kept), asynchronously on `stream`. */
 pe_status pe_reset_residency(pe_handle* h, void* stream);
 
+/* Self-test of failure detection, without a GPU fault.  Every wait inside
+ * the kernels is bounded: on running out it records PE_DEVERR_TIMEOUT in an
+ * error word and returns, so the context stays usable.  This runs, on the
+ * current device, each kind of wait the kernels use on a condition that
+ * never becomes true, with `poll_limit` polls (about 0.1-1 us each):
+ *   out3[0]  the prefill step's counter wait (bit 31 set if it did not also
+ *            raise the step's abort word, which must end a second wait at once);
+ *   out3[1]  an mbarrier wait (the tensor-core pipeline's);
+ *   out3[2]  the decode step's phase wait.
+ * Each word must read PE_DEVERR_TIMEOUT.  Returns PE_ERR_INVALID for a NULL
+ * out3 or a zero limit, PE_ERR_CUDA if a launch failed.  Synchronises the
+ * device. */
+pe_status pe_selftest_bounded_waits(uint32_t poll_limit, uint32_t* out3);
+
 /* Measure the host link: copy `bytes` of the host store to `dev_dst`
  * (caller-owned device memory) `iters` times with cudaMemcpyAsync and with
  * the page-in kernel's device-side loads, timed with CUDA events on
