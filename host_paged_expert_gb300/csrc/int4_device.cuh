@@ -28,8 +28,8 @@ __device__ __forceinline__ float i4_bf_hi(uint32_t v) { return __uint_as_float(v
 __device__ __forceinline__ float dot32_int4_bf16(int4 w, const int4 (&x)[4]) {
     const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
     float p = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {  // kept rolled: a smaller loop body stays in the instruction cache
         const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
