@@ -24,20 +24,28 @@ __device__ __forceinline__ float i4_val(uint32_t w, int i) {
 __device__ __forceinline__ float i4_bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float i4_bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// sum_{e<32} (q_e - 8) * x_e in input order: 32 codes against 32 bf16 values.
-__device__ __forceinline__ float dot32_int4_bf16(int4 w, const int4 (&x)[4]) {
-    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
-    float p = 0.f;
+// Gate and up dot products of one 32-code chunk against the same 32 bf16
+// values: pg = sum_e (g_e - 8) x_e and pu likewise.  Each is accumulated as
+// an even-input and an odd-input partial sum (in input order within each)
+// added at the end, so the four chains run side by side.
+__device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (&x)[4], float& pg, float& pu) {
+    const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
+    const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
+    float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {  // kept rolled: a smaller loop body stays in the instruction cache
         const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            p = fmaf(i4_val(wv[q], 2 * i), i4_bf_lo(xv[i]), p);
-            p = fmaf(i4_val(wv[q], 2 * i + 1), i4_bf_hi(xv[i]), p);
+            const float xl = i4_bf_lo(xv[i]), xh = i4_bf_hi(xv[i]);
+            ge = fmaf(i4_val(gv[q], 2 * i), xl, ge);
+            go = fmaf(i4_val(gv[q], 2 * i + 1), xh, go);
+            ue = fmaf(i4_val(uv[q], 2 * i), xl, ue);
+            uo = fmaf(i4_val(uv[q], 2 * i + 1), xh, uo);
         }
     }
-    return p;
+    pg = __fadd_rn(ge, go);
+    pu = __fadd_rn(ue, uo);
 }
 
 // sum_{e<32} (q_e - 8) * h_e in input order: 32 codes against 32 fp32 values.
@@ -78,8 +86,10 @@ __device__ __forceinline__ float row_pair_h_int4(const int4 (&gv)[CPL], const in
             int4 x[4];
 #pragma unroll
             for (int v = 0; v < 4; ++v) x[v] = *reinterpret_cast<const int4*>(xr + 64 * (size_t)idx + 16 * v);
-            ag = fmaf(sg[c], dot32_int4_bf16(gv[c], x), ag);
-            au = fmaf(su[c], dot32_int4_bf16(uv[c], x), au);
+            float pg, pu;
+            dot32x2_int4_bf16(gv[c], uv[c], x, pg, pu);
+            ag = fmaf(sg[c], pg, ag);
+            au = fmaf(su[c], pu, au);
         }
     }
     ag = warp_sum(ag);
