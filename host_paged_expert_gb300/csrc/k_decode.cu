@@ -49,7 +49,7 @@ constexpr int kDynBudget = 48 * 1024;
 constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a second
 
 // Per-layer counters: role registration, completion counts and barriers.
-enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, S_EXIT, S_NUM };
+enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, H_TICKET, S_EXIT, S_NUM };
 constexpr int kPlanCap = 256;    // planner capacity inside this kernel: E, K <= 256
 constexpr int kLinkSmEvery = 3;  // CTAs on SMs with %smid % 3 == 0 stream the host link
 
@@ -464,14 +464,25 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     };
 
     // ---- phase 2: down projections ----
-    if (hbm_cta) {
-        // resident experts: as soon as every resident expert's h is done
+    // Resident experts: as soon as every resident expert's h is done.  Items
+    // go out eight at a time (one per warp) from a per-step ticket, so link
+    // CTAs that finish their page-ins early (small or few page-ins) help.
+    if (hbm_cta || hbm_items > 0) {
         cta_wait(&sync[D_HITS], (unsigned)hbm_ctas, err, &sh_flag);
         const long long items = (long long)sh_nhit * row_blocks;
-        for (long long it = (long long)rank * kWp + warp; it < items; it += (long long)hbm_ctas * kWp) {
-            const int e = sh_hit_list[it / row_blocks];
-            const int m0 = (int)(it % row_blocks) * RD;
-            down_entry(e, m0);
+        __shared__ unsigned sh_ticket;
+        for (;;) {
+            if (threadIdx.x == 0) sh_ticket = atomicAdd(&sync[H_TICKET], (unsigned)kWp);
+            __syncthreads();
+            const long long base = sh_ticket;
+            __syncthreads();  // every warp has read it before thread 0 takes the next
+            if (base >= items) break;
+            const long long it = base + warp;
+            if (it < items) {
+                const int e = sh_hit_list[it / row_blocks];
+                const int m0 = (int)(it % row_blocks) * RD;
+                down_entry(e, m0);
+            }
         }
     }
     // paged experts: once the link is drained (their h and their w2 rows)
