@@ -6,9 +6,10 @@
 // on the GPU.  Once the plan is written, what bounds that step is the host
 // link: the missing experts' bytes must cross it.  This kernel keeps every
 // other part of the step underneath that transfer.
-//   planner    the first CTA to start routes the tokens and plans the wave
-//              (plan_block, the same code as the standalone planner); every
-//              other CTA stages its inputs meanwhile and waits for the plan;
+//   planner    every CTA routes the tokens and plans the wave itself
+//              (plan_block, the same code as the standalone planner), so no
+//              CTA waits for a plan to travel through global memory; the
+//              last CTA to have read the old LRU state writes the new one;
 //   link SMs   stream the page-ins' gate/up rows from the host store (writing
 //              them to their slots and computing h from them on the way) and
 //              copy the rest of each paged row;
@@ -49,9 +50,16 @@ constexpr int kDynBudget = 48 * 1024;
 constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a second
 
 // Per-layer counters: role registration, completion counts and barriers.
-enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_TICKET, P_READY, H_TICKET, S_EXIT, S_NUM };
+enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_READ, H_TICKET, S_EXIT, S_NUM };
 constexpr int kPlanCap = 256;    // planner capacity inside this kernel: E, K <= 256
 constexpr int kLinkSmEvery = 3;  // CTAs on SMs with %smid % 3 == 0 stream the host link
+
+// 32-bit words of the per-CTA plan in dynamic shared memory: member experts
+// and slots [K each], then entry slot, member index and router weight
+// [kFusedMaxEntries each]; staged x follows, 16-byte aligned.
+__host__ __device__ __forceinline__ int decode_meta_words(const Shape& s) {
+    return (2 * s.K + 3 * kFusedMaxEntries + 3) & ~3;
+}
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
@@ -200,49 +208,41 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     int32_t* sh_mslot = sh_mexp + s.K;
     int32_t* sh_ekey = sh_mslot + s.K;  // entry's slot (-1 if not in the wave)
     int32_t* sh_eq = sh_ekey + kFusedMaxEntries;  // entry's member index
-    __shared__ int sh_planner;
+    float* sh_ew = reinterpret_cast<float*>(sh_eq + kFusedMaxEntries);  // entry's router weight
+    __shared__ int sh_count, sh_size;
     const int nent = T * s.k;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     pdl_wait();
 
-    // the first CTA to arrive plans the step; the others stage x meanwhile.
-    // Every CTA also registers the role its SM suggests and gets a rank in it.
+    // Every CTA registers the role its SM suggests and gets a rank in it,
+    // stages x, and plans the step into its own shared memory.
     __shared__ int sh_link_sm, sh_role_rank;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == kThr - 32) {  // a warp that routes no token of a small step: it waits for the atomic
         unsigned smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
         sh_link_sm = (smid % kLinkSmEvery) == 0;
         sh_role_rank = (int)atomicAdd(&sync[sh_link_sm ? R_LINK : R_HBM], 1u);
-        sh_planner = atomicAdd(&sync[P_TICKET], 1u) == 0;
     }
-    __syncthreads();
-    if (sh_planner) {
-        plan_block<EPL, kPlanCap>(L, s, logits, T, 1, err);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicExch(&sync[P_READY], 1u);
-        }
-    }
+    // x is copied to shared memory asynchronously, underneath the planning
     const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
     if (stage_x) {
-        int4* sx = reinterpret_cast<int4*>(sh_mexp + ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3));
+        int4* sx = reinterpret_cast<int4*>(sh_mexp + decode_meta_words(s));
         const int nvec = T * s.H / 8;
-        for (int i = threadIdx.x; i < nvec; i += blockDim.x) sx[i] = ldg16(xbase + 16 * (size_t)i);
+        for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
+            const unsigned dst = (unsigned)__cvta_generic_to_shared(sx + i);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(xbase + 16 * (size_t)i) : "memory");
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
         xbase = reinterpret_cast<const uint8_t*>(sx);
     }
-    cta_wait(&sync[P_READY], 1u, err, &sh_flag);
-
-    // the plan (written by the planner CTA in this kernel: read past L1)
-    const int size = __ldcg(L.member_count);
-    const int count = __ldcg(L.plan_count);
-    for (int i = threadIdx.x; i < size; i += blockDim.x) {
-        sh_mexp[i] = __ldcg(L.member_expert + i);
-        sh_mslot[i] = __ldcg(L.member_slot + i);
+    {
+        const PlanOut po{sh_mexp, sh_mslot, sh_ekey, sh_ew, &sh_count, &sh_size};
+        plan_block<EPL, kPlanCap>(L, s, logits, T, 1, err, &po, &sync[P_READ], gridDim.x);
     }
-    for (int i = threadIdx.x; i < nent; i += blockDim.x)
-        sh_ekey[i] = __ldcg(L.entry_wave + i) == 0 ? __ldcg(L.entry_slot + i) : -1;
+    if (stage_x) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
+    const int size = sh_size;
+    const int count = sh_count;
     if (threadIdx.x < nent) {  // member of each entry (nent <= kFusedMaxEntries <= kThr)
         int q = -1;
         for (int j = 0; j < size; ++j)
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     // down projection rows m0.. of entry e into the merged buffer
     auto down_entry = [&](int e, int m0) {
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
-        const float we = __ldcg(L.topk_w + e);
+        const float we = sh_ew[e];
         if constexpr (FMT == PE_INT4_GPTQ)
             down_rows_int4<CPLI4, RD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
                                           hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true, merged + (size_t)e * s.H,
@@ -541,8 +541,7 @@ bool decode_fused_supported(const Shape& s, int T) {
                       : s.dtype == PE_INT4_GPTQ ? (s.H <= 32 * 32 * CPLH4 && s.I <= 32 * 32 * CPLI4)
                                                 : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
     return (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K && s.E <= kPlanCap &&
-           s.K <= kPlanCap && dims &&
-           (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3) <= (size_t)kDynBudget;
+           s.K <= kPlanCap && dims && (size_t)4 * decode_meta_words(s) <= (size_t)kDynBudget;
 }
 
 cudaError_t decode_setup_kernels() {
@@ -560,7 +559,7 @@ cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* 
                                 const uint8_t* host_layer, uint8_t* slots_layer, int T, float* hbuf, float* merged,
                                 __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st) {
     const int grid = num_sms * 2;  // two CTAs per SM: every CTA is resident at once
-    const size_t meta = (size_t)4 * ((2 * s.K + 2 * kFusedMaxEntries + 3) & ~3);
+    const size_t meta = (size_t)4 * decode_meta_words(s);
     const size_t xbytes = (size_t)T * s.H * 2;
     const int stage = meta + xbytes <= (size_t)kDynBudget;
     const size_t smem = meta + (stage ? xbytes : 0);

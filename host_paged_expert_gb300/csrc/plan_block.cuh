@@ -102,14 +102,33 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
     out_w = lane < k ? __fdiv_rn(ex, sum) : 0.f;
 }
 
+// Where each CTA that plans a single-wave step side by side with others keeps
+// the plan (shared memory of the caller).
+struct PlanOut {
+    int32_t* mexp;  // [K] members: the page-ins in plan order, then the hits
+    int32_t* mslot; // [K] their slots
+    int32_t* ekey;  // [T*k] slot of each entry, -1 if its expert is not in the wave
+    float* ew;      // [T*k] router weight of each entry
+    int* count;     // page-ins
+    int* size;      // members
+};
+
 // One CTA plans every wave of a step (every thread of the block calls this).
+// With read_ctr set, `readers` CTAs plan the same step side by side (from the
+// same inputs, so to the same plan), each keeping wave 0 in `out`; each counts
+// itself in *read_ctr once it holds the old LRU state in shared memory, and
+// the CTA that counts last - when no CTA still reads the old state - writes
+// the routing, the plan, the new state and the counters to global memory.
+// That needs the routed ids in shared memory (T * k <= CAP).  Without
+// read_ctr the calling CTA alone plans and writes everything.
 // blockDim.x is a multiple of 32 and at least E (thread e owns expert e in the
 // scans) and K (thread s owns slot s); CAP >= max(E, K) sizes the shared
 // arrays, and an inline-routed step keeps its ids in shared memory when
 // T * k <= CAP.  EPL = ceil(E / 32) logits per lane.
 template <int EPL, int CAP>
 __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logits, int T, int route_inline,
-                           uint32_t* err) {
+                           uint32_t* err, const PlanOut* out = nullptr, unsigned* read_ctr = nullptr,
+                           unsigned readers = 0) {
     __shared__ int32_t sh_slot_expert[CAP];
     __shared__ uint32_t sh_tick[CAP];
     __shared__ int32_t sh_expert_slot[CAP];
@@ -122,33 +141,42 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
     __shared__ uint8_t sh_loaded[CAP];
     __shared__ unsigned long long sh_vkey[CAP];  // (tick, slot) of victim slots, ~0 otherwise
     __shared__ int sh_wr[32], sh_wm[32];
-    __shared__ int sh_nR, sh_nM, sh_cold, sh_bad, sh_nan;
+    __shared__ int sh_nR, sh_nM, sh_cold, sh_bad, sh_nan, sh_pub;
+    __shared__ uint32_t sh_clock;
 
     const int tid = threadIdx.x, nthr = blockDim.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = nthr >> 5;
     const int E = s.E, K = s.K, k = s.k;
     const int nent = T * k;
     const bool ids_in_smem = route_inline && nent <= CAP;
+    const bool shared_plan = read_ctr != nullptr;
 
-    // every global load of the planner is issued here, before routing
-    for (int i = tid; i < K; i += nthr) {
-        sh_slot_expert[i] = L.slot_expert[i];
-        sh_tick[i] = L.slot_tick[i];
+    // The old LRU state is loaded into registers (thread s owns slot s, thread
+    // e expert e) and moved to shared memory only after routing: a store of a
+    // loaded value waits for its load, so storing first would put one memory
+    // round trip per array in front of routing.  This way the state's loads,
+    // the logits' loads and the routing overlap.
+    int32_t r_slot_expert = -1, r_expert_slot = -1;
+    uint32_t r_tick = 0, r_clock = 0;
+    uint8_t r_loaded = 0;
+    if (tid < K) {
+        r_slot_expert = L.slot_expert[tid];
+        r_tick = L.slot_tick[tid];
     }
-    for (int e = tid; e < E; e += nthr) {
-        sh_expert_slot[e] = L.expert_slot[e];
-        sh_loaded[e] = L.loaded[e];
-        sh_used[e] = 0;
-        sh_inwave[e] = 0;
-        sh_wave_of[e] = -1;
-        sh_slot_in_wave[e] = -1;
+    if (tid < E) {
+        r_expert_slot = L.expert_slot[tid];
+        r_loaded = L.loaded[tid];
+        sh_used[tid] = 0;
+        sh_inwave[tid] = 0;
+        sh_wave_of[tid] = -1;
+        sh_slot_in_wave[tid] = -1;
     }
     if (tid == 0) {
+        r_clock = *L.clock;
         sh_cold = 0;
         sh_bad = 0;
         sh_nan = 0;
     }
-    uint32_t clock = *L.clock;
     if (route_inline) {
         for (int t = warp; t < T; t += nwarps) {
             int id;
@@ -156,14 +184,35 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
             bool nan_seen = false;
             route_token_warp<EPL>(logits + (size_t)t * E, E, k, id, w, nan_seen);
             if (lane < k) {
-                L.topk_id[(size_t)t * k + lane] = id;
-                L.topk_w[(size_t)t * k + lane] = w;
+                if (!shared_plan) {
+                    L.topk_id[(size_t)t * k + lane] = id;
+                    L.topk_w[(size_t)t * k + lane] = w;
+                }
                 if (ids_in_smem) sh_ids[t * k + lane] = id;
+                if (out) out->ew[t * k + lane] = w;
             }
             if (nan_seen) sh_nan = 1;
         }
     }
+    if (tid < K) {
+        sh_slot_expert[tid] = r_slot_expert;
+        sh_tick[tid] = r_tick;
+    }
+    if (tid < E) {
+        sh_expert_slot[tid] = r_expert_slot;
+        sh_loaded[tid] = r_loaded;
+    }
+    if (tid == 0) sh_clock = r_clock;
     __syncthreads();  // routing, state and flags are in shared memory from here on
+    // this CTA no longer reads the old state; the last one to say so publishes
+    // (the count returned is first used at the end, so nothing waits for it)
+    unsigned readers_before = 0;
+    if (shared_plan && tid == 0)
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                     : "=r"(readers_before)
+                     : "l"(read_ctr)
+                     : "memory");
+    uint32_t clock = sh_clock;
 
     for (int i = tid; i < nent; i += nthr) {
         const int e = ids_in_smem ? sh_ids[i] : L.topk_id[i];
@@ -232,8 +281,14 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
                 const int slot = sh_expert_slot[m];
                 sh_tick[slot] = clock;
                 // hits follow the page-ins in the member list
-                L.member_expert[(size_t)w * K + nmiss + i] = m;
-                L.member_slot[(size_t)w * K + nmiss + i] = slot;
+                if (!shared_plan) {
+                    L.member_expert[(size_t)w * K + nmiss + i] = m;
+                    L.member_slot[(size_t)w * K + nmiss + i] = slot;
+                }
+                if (out && w == 0) {
+                    out->mexp[nmiss + i] = m;
+                    out->mslot[nmiss + i] = slot;
+                }
             }
         }
         __syncthreads();
@@ -265,11 +320,17 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
             sh_expert_slot[m] = slot;
             sh_tick[slot] = clock;
             const size_t q = (size_t)w * K + my_rank;
-            L.plan_expert[q] = m;
-            L.plan_slot[q] = slot;
-            L.member_expert[q] = m;
-            L.member_slot[q] = slot;
-            if (!sh_loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
+            if (!shared_plan) {
+                L.plan_expert[q] = m;
+                L.plan_slot[q] = slot;
+                L.member_expert[q] = m;
+                L.member_slot[q] = slot;
+                if (!sh_loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
+            }
+            if (out && w == 0) {
+                out->mexp[my_rank] = m;
+                out->mslot[my_rank] = slot;
+            }
         }
         __syncthreads();
         for (int i = tid; i < size; i += nthr) {
@@ -279,11 +340,47 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
             sh_inwave[m] = 0;
         }
         if (tid == 0) {
-            L.plan_count[w] = nmiss;
-            L.member_count[w] = size;
+            if (!shared_plan) {
+                L.plan_count[w] = nmiss;
+                L.member_count[w] = size;
+            }
+            if (out && w == 0) {
+                *out->count = nmiss;
+                *out->size = size;
+            }
         }
         total_miss += nmiss;
         __syncthreads();
+    }
+    if (out && nW == 0 && tid == 0) {
+        *out->count = 0;
+        *out->size = 0;
+    }
+    if (shared_plan) {  // a single wave (T * k <= K): its plan is in `out`
+        if (tid == 0) sh_pub = readers_before == readers - 1;
+        __syncthreads();
+        if (!sh_pub) {
+            for (int i = tid; i < nent; i += nthr) {
+                const int m = sh_ids[i];
+                out->ekey[i] = m >= 0 && m < E && sh_wave_of[m] == 0 ? sh_slot_in_wave[m] : -1;
+            }
+            return;
+        }
+        const int nmiss = *out->count, size = *out->size;
+        for (int i = tid; i < size; i += nthr) {
+            const int m = out->mexp[i];
+            L.member_expert[i] = m;
+            L.member_slot[i] = out->mslot[i];
+            if (i < nmiss) {
+                L.plan_expert[i] = m;
+                L.plan_slot[i] = out->mslot[i];
+                if (!sh_loaded[m]) atomicOr(err, PE_DEVERR_NOT_LOADED);
+            }
+        }
+        if (tid == 0 && nW > 0) {
+            L.plan_count[0] = nmiss;
+            L.member_count[0] = size;
+        }
     }
     for (int w = nW + tid; w < s.Wmax; w += nthr) {
         L.plan_count[w] = 0;
@@ -295,6 +392,11 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
         const bool ok = m >= 0 && m < E;
         L.entry_wave[i] = ok ? sh_wave_of[m] : -1;
         L.entry_slot[i] = ok ? sh_slot_in_wave[m] : 0;
+        if (shared_plan) {
+            L.topk_id[i] = m;
+            L.topk_w[i] = out->ew[i];
+        }
+        if (out) out->ekey[i] = ok && sh_wave_of[m] == 0 ? sh_slot_in_wave[m] : -1;
     }
     for (int i = tid; i < K; i += nthr) {
         L.slot_expert[i] = sh_slot_expert[i];
