@@ -24,10 +24,72 @@ __device__ __forceinline__ float i4_val(uint32_t w, int i) {
 __device__ __forceinline__ float i4_bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float i4_bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// (q - 8) for the nibbles at bits 0 and 16 of w as a bf16 pair, exactly: the
+// bf16 with bits 0x4300 | q is 128 + q, and 128 + q - 136 is representable.
+__device__ __forceinline__ uint32_t i4_pair_bf16(uint32_t w) {
+    const uint32_t t = (w & 0x000F000Fu) | 0x43004300u;
+    const __nv_bfloat162 d = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&t), __float2bfloat162_rn(136.f));
+    return *reinterpret_cast<const uint32_t*>(&d);
+}
+
+// c + a * b for bf16 a, b (the low or high halves of two 32-bit registers)
+// with one rounding to fp32: the mixed-precision fma of sm_100 and later,
+// equal to fmaf(float(a), float(b), c).
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hl(uint32_t a, uint32_t b, float c) {  // a high, b low
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_lh(uint32_t a, uint32_t b, float c) {  // a low, b high
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bh, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hh(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+// One row's even-input and odd-input partial sums over the 8 codes of word w
+// against the 8 bf16 inputs in xv[0..3] (xv[i] holds inputs 2i, 2i+1): each
+// chain takes its inputs in ascending order.  The codes are decoded two at a
+// time: nibbles (0,4), (1,5), (2,6), (3,7).
+__device__ __forceinline__ void dot8_int4_bf16(uint32_t w, const uint32_t (&xv)[4], float& ev, float& od) {
+    const uint32_t p04 = i4_pair_bf16(w), p15 = i4_pair_bf16(w >> 4);
+    const uint32_t p26 = i4_pair_bf16(w >> 8), p37 = i4_pair_bf16(w >> 12);
+    ev = fma_bf16_lo(p04, xv[0], ev);  // input 0
+    od = fma_bf16_lh(p15, xv[0], od);  // input 1
+    ev = fma_bf16_lo(p26, xv[1], ev);  // input 2
+    od = fma_bf16_lh(p37, xv[1], od);  // input 3
+    ev = fma_bf16_hl(p04, xv[2], ev);  // input 4
+    od = fma_bf16_hh(p15, xv[2], od);  // input 5
+    ev = fma_bf16_hl(p26, xv[3], ev);  // input 6
+    od = fma_bf16_hh(p37, xv[3], od);  // input 7
+}
+
 // Gate and up dot products of one 32-code chunk against the same 32 bf16
 // values: pg = sum_e (g_e - 8) x_e and pu likewise.  Each is accumulated as
 // an even-input and an odd-input partial sum (in input order within each)
-// added at the end, so the four chains run side by side.
+// added at the end, so the four chains run side by side.  The products are
+// exact and each step rounds once, as fmaf on the values widened to fp32.
 __device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (&x)[4], float& pg, float& pu) {
     const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
     const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
@@ -35,14 +97,8 @@ __device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {  // kept rolled: a smaller loop body stays in the instruction cache
         const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float xl = i4_bf_lo(xv[i]), xh = i4_bf_hi(xv[i]);
-            ge = fmaf(i4_val(gv[q], 2 * i), xl, ge);
-            go = fmaf(i4_val(gv[q], 2 * i + 1), xh, go);
-            ue = fmaf(i4_val(uv[q], 2 * i), xl, ue);
-            uo = fmaf(i4_val(uv[q], 2 * i + 1), xh, uo);
-        }
+        dot8_int4_bf16(gv[q], xv, ge, go);
+        dot8_int4_bf16(uv[q], xv, ue, uo);
     }
     pg = __fadd_rn(ge, go);
     pu = __fadd_rn(ue, uo);
