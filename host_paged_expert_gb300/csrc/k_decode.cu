@@ -190,7 +190,7 @@ constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
 // int4 rows are short (H/2 and I/2 bytes), so an int4 down item takes
 // kRowsD4 rows to keep enough bytes in flight (a gate/up item stays one row
 // pair: two spill registers); the per-row arithmetic is unchanged.
-constexpr int kRowsG4 = 1, kRowsD4 = 8;
+constexpr int kRowsG4 = 2, kRowsD4 = 8;
 // FMT: the expert format (PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ).
 template <int EPL, int FMT>
 __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
@@ -267,10 +267,12 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
 
     const int nchunk = s.H >> 3;
     const size_t row_bytes = (size_t)s.H * 2;
-    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;  // gate/up row pairs per item
+    // gate/up row pairs per resident-expert item (a page-in item takes one:
+    // the link wants many warps with host reads in flight)
+    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;
     constexpr int RD = FMT == PE_INT4_GPTQ ? kRowsD4 : kRowsD;  // down rows per item
-    const int ipe = s.I / RPI;  // gate/up items per expert
-    const long long miss_rows = (long long)count * ipe;
+    const int ipe = s.I / RPI;  // gate/up items per resident expert
+    const long long miss_rows = (long long)count * s.I;
     const size_t tail_bytes = s.copy_bytes - s.tail_off;
     const long long copies_per = (long long)((tail_bytes + kCopyItem - 1) / kCopyItem);
     const long long link_items = miss_rows + (long long)count * copies_per;
@@ -321,8 +323,9 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                     }
                     continue;
                 }
-                const int mq = as_link ? (int)(item / ipe) : count + (int)(item / ipe);
-                const int n = (int)(item % ipe) * RPI;  // first row pair of the item
+                const int mq = as_link ? (int)(item / s.I) : count + (int)(item / ipe);
+                const int n = as_link ? (int)(item % s.I) : (int)(item % ipe) * RPI;  // first row pair of the item
+                const int nr = as_link ? 1 : RPI;                                       // row pairs of the item
                 const int slot = sh_mslot[mq];
                 if constexpr (FMT == PE_INT4_GPTQ) {
                     uint8_t* slot_base = slots + (size_t)slot * s.stride;
@@ -332,10 +335,12 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                     float sg[RPI][CPLH4], su[RPI][CPLH4];
 #pragma unroll
                     for (int r = 0; r < RPI; ++r)
-                        load_row_pair_int4<CPLH4>(rbase, s, n + r, lane, nch4, as_link, false, gv[r], uv[r], sg[r], su[r]);
+                        if (r < nr)
+                            load_row_pair_int4<CPLH4>(rbase, s, n + r, lane, nch4, as_link, false, gv[r], uv[r], sg[r],
+                                                      su[r]);
                     if (as_link) {
 #pragma unroll
-                        for (int r = 0; r < RPI; ++r) {
+                        for (int r = 0; r < 1; ++r) {
                             uint8_t* gd = slot_base + s.w13_off + (size_t)(n + r) * (s.H / 2);
                             uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
 #pragma unroll
@@ -357,6 +362,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                             const uint8_t* xr = xbase + (size_t)(ei / s.k) * s.H * 2;
 #pragma unroll
                             for (int r = 0; r < RPI; ++r) {
+                                if (r >= nr) break;
                                 const float hval = row_pair_h_int4<CPLH4>(gv[r], uv[r], sg[r], su[r], xr, lane, nch4);
                                 if (lane == 0) hbuf[(size_t)ei * s.I + n + r] = hval;
                             }
