@@ -15,15 +15,6 @@
 
 namespace pe {
 
-// q - 8 for nibble i of a 32-bit word, exactly: 2^23 + q as a float, minus
-// 2^23 + 8.
-__device__ __forceinline__ float i4_val(uint32_t w, int i) {
-    return __int_as_float(0x4B000000u | ((w >> (4 * i)) & 0xFu)) - 8388616.0f;
-}
-
-__device__ __forceinline__ float i4_bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
-__device__ __forceinline__ float i4_bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-
 // (q - 8) for the nibbles at bits 0 and 16 of w as a bf16 pair, exactly: the
 // bf16 with bits 0x4300 | q is 128 + q, and 128 + q - 136 is representable.
 __device__ __forceinline__ uint32_t i4_pair_bf16(uint32_t w) {
@@ -104,21 +95,27 @@ __device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (
     pu = __fadd_rn(ue, uo);
 }
 
+// (q - 8) of the low / high code of a pair from i4_pair_bf16, as fp32.
+__device__ __forceinline__ float i4_lo_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
+__device__ __forceinline__ float i4_hi_f32(uint32_t pair) { return __uint_as_float(pair & 0xffff0000u); }
+
 // sum_{e<32} (q_e - 8) * h_e in input order: 32 codes against 32 fp32 values.
 __device__ __forceinline__ float dot32_int4_f32(int4 w, const float4 (&h)[8]) {
     const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
     float p = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
+        const uint32_t p04 = i4_pair_bf16(wv[q]), p15 = i4_pair_bf16(wv[q] >> 4);
+        const uint32_t p26 = i4_pair_bf16(wv[q] >> 8), p37 = i4_pair_bf16(wv[q] >> 12);
         const float4 a = h[2 * q], b = h[2 * q + 1];
-        p = fmaf(i4_val(wv[q], 0), a.x, p);
-        p = fmaf(i4_val(wv[q], 1), a.y, p);
-        p = fmaf(i4_val(wv[q], 2), a.z, p);
-        p = fmaf(i4_val(wv[q], 3), a.w, p);
-        p = fmaf(i4_val(wv[q], 4), b.x, p);
-        p = fmaf(i4_val(wv[q], 5), b.y, p);
-        p = fmaf(i4_val(wv[q], 6), b.z, p);
-        p = fmaf(i4_val(wv[q], 7), b.w, p);
+        p = fmaf(i4_lo_f32(p04), a.x, p);
+        p = fmaf(i4_lo_f32(p15), a.y, p);
+        p = fmaf(i4_lo_f32(p26), a.z, p);
+        p = fmaf(i4_lo_f32(p37), a.w, p);
+        p = fmaf(i4_hi_f32(p04), b.x, p);
+        p = fmaf(i4_hi_f32(p15), b.y, p);
+        p = fmaf(i4_hi_f32(p26), b.z, p);
+        p = fmaf(i4_hi_f32(p37), b.w, p);
     }
     return p;
 }

@@ -73,6 +73,7 @@
 #include <cuda_fp16.h>
 
 #include "fp8_device.cuh"
+#include "int4_device.cuh"
 #include "pe_device.cuh"
 #include "pe_internal.h"
 #include "tc_sm100.cuh"
@@ -547,14 +548,19 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
                 const float scl = __half2float(scale4[r * ng + (kb * BK) / kInt4Group]);
                 const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {  // codes 2t, 2t+1 of the chunk
-                    const uint32_t w = t < 4 ? cv.x : cv.y;
-                    const int sh = 8 * (t & 3);
-                    // q - 8 exactly: 2^23 + q as a float, minus 2^23 + 8
-                    const float v0 = __int_as_float(0x4B000000u | ((w >> sh) & 0xFu)) - 8388616.0f;
-                    const float v1 = __int_as_float(0x4B000000u | ((w >> (sh + 4)) & 0xFu)) - 8388616.0f;
-                    const __nv_bfloat162 pv = __floats2bfloat162_rn(v0 * scl, v1 * scl);
-                    packed[t] = *reinterpret_cast<const uint32_t*>(&pv);
+                for (int h = 0; h < 2; ++h) {  // codes 8h .. 8h+7 of the chunk: one word
+                    const uint32_t w = h ? cv.y : cv.x;
+                    // q - 8 exactly, two codes at a time: nibbles (0,4), (1,5), (2,6), (3,7)
+                    const uint32_t p04 = i4_pair_bf16(w), p15 = i4_pair_bf16(w >> 4);
+                    const uint32_t p26 = i4_pair_bf16(w >> 8), p37 = i4_pair_bf16(w >> 12);
+                    const __nv_bfloat162 c01 = __floats2bfloat162_rn(i4_lo_f32(p04) * scl, i4_lo_f32(p15) * scl);
+                    const __nv_bfloat162 c23 = __floats2bfloat162_rn(i4_lo_f32(p26) * scl, i4_lo_f32(p37) * scl);
+                    const __nv_bfloat162 c45 = __floats2bfloat162_rn(i4_hi_f32(p04) * scl, i4_hi_f32(p15) * scl);
+                    const __nv_bfloat162 c67 = __floats2bfloat162_rn(i4_hi_f32(p26) * scl, i4_hi_f32(p37) * scl);
+                    packed[4 * h] = *reinterpret_cast<const uint32_t*>(&c01);
+                    packed[4 * h + 1] = *reinterpret_cast<const uint32_t*>(&c23);
+                    packed[4 * h + 2] = *reinterpret_cast<const uint32_t*>(&c45);
+                    packed[4 * h + 3] = *reinterpret_cast<const uint32_t*>(&c67);
                 }
             }
             // bf16 columns 16j..16j+15 are the 16-byte chunks 2j, 2j+1 of row r, swizzled by r % 8
