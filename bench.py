@@ -184,7 +184,8 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "decode_step": ("k_decode.cu", "plan_block.cuh", "pe_device.cuh", "fp8_device.cuh", "int4_device.cuh",
                     "pe_internal.h"),
-    "prefill_step": ("k_prefill.cu", "tc_sm100.cuh", "pe_device.cuh", "fp8_device.cuh", "pe_internal.h"),
+    "prefill_step": ("k_prefill.cu", "tc_sm100.cuh", "pe_device.cuh", "fp8_device.cuh", "int4_device.cuh",
+                     "pe_internal.h"),
 }
 
 
