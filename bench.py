@@ -505,7 +505,9 @@ def run_prefill(args):
     line = {"metric": "paged-MoE prefill tok/s (48 layers, K resident)", "value": round(tok_s, 1), "unit": "tok/s",
             "n_gpus": 1, "steps": K, "warmup": W, "ms_per_step": round(ms / K, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": shape.dtype, "data": "synthetic",
-            "config": {"workload": f"{args.workload}: {desc}", "chunks_cycled": nchunk},
+            "config": {"workload": f"{args.workload}: {desc}", "chunks_cycled": nchunk,
+                       "l2": f"inputs larger than L2: each chunk reads ~{d['distinct'] / K * payload / 1e9:.1f} GB "
+                             "of expert weights"},
             "clocks": clk.summary(),
             "page_in": {"per_layer_step": round(d["page_ins"] / (K * L), 2), "link_probe_gbs": [round(ce_gbs, 1), round(kn_gbs, 1)],
                         "waves_per_layer_step": round(d["waves"] / (K * L), 2),
@@ -514,6 +516,16 @@ def run_prefill(args):
                                "definition": "sum over layer-steps of max(distinct*expert_bytes/HBM, page_ins*expert_bytes/link) "
                                              "divided by the summed kernel time of the trace pass"},
             "kernels": kernels}
+    if "prefill_step" in kernels:  # the dominant kernel: page-ins over the link with the GEMMs underneath
+        kd = kernels["prefill_step"]
+        line["roofline"] = {"kernel": "prefill_step", "bound": "host_link", "achieved": kd["achieved_gbs"],
+                            "peak": kd["peak_gbs"], "unit": "GB/s", "frac": kd["frac"],
+                            "traffic": ncu_traffic("prefill_step", args.workload),
+                            "peak_src": "same-run host-link probe (best of copy engine and device loads)",
+                            "bytes_per_launch": round(d["page_ins"] * payload / kd["launches"]),
+                            "tensor": {"achieved": kd["gemm_tflops_over_step"], "peak": peaks["bf16_tflops"],
+                                       "unit": "TFLOP/s", "frac": kd["gemm_frac_of_bf16_peak"]}}
+    line["gpu_launches"] = sum(v["launches"] for v in prof.values())  # the trace pass runs the same K chunks
     print(json.dumps(line), flush=True)
     model.close()
 
