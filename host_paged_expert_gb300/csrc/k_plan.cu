@@ -59,6 +59,8 @@ cudaError_t launch_plan(const LayerDev& L, const Shape& s, const float* logits, 
                         int route_inline, uint32_t* err, cudaStream_t st) {
     int threads = s.E > s.K ? s.E : s.K;
     if (route_inline && threads < 32 * T) threads = 32 * T;  // one warp per token
+    // a large step's entry loops want many threads more than a small barrier
+    if ((long long)T * s.k > 4LL * threads) threads = kPlanMaxThreads;
     threads = (threads + 31) / 32 * 32;
     if (threads > kPlanMaxThreads) threads = kPlanMaxThreads;
     switch (epl_for(s.E)) {

@@ -175,6 +175,19 @@ __device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
 // the queue (its own member's gate/up tiles, the page-in of its expert, and
 // through that page-in the tiles of earlier waves that used its slot), which
 // keeps the persistent pipeline free of deadlock.
+// Wave and expert of entries i0, i0 + stride, ... (kAlignBatch of them; -1
+// waves past nent), all loads issued before any is used.
+constexpr int kAlignBatch = 8;
+__device__ __forceinline__ void load_entries(const LayerDev& L, int i0, int stride, int nent, int (&ew)[kAlignBatch],
+                                             int (&id)[kAlignBatch]) {
+#pragma unroll
+    for (int u = 0; u < kAlignBatch; ++u) {
+        const int i = i0 + u * stride;
+        ew[u] = i < nent ? L.entry_wave[i] : -1;
+        id[u] = i < nent ? L.topk_id[i] : 0;
+    }
+}
+
 __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s, PrefillDev P, int slot_base, int T,
                                                              int n1, int n2, unsigned nchunk, int lag) {
     __shared__ int sh_g_of_e[kMaxExperts];  // expert -> member
@@ -272,11 +285,17 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         sh_fill[g] = 0;
     }
     __syncthreads();
-    for (int i = tid; i < nent; i += nthr)
-        if (L.entry_wave[i] >= 0) {
-            const int g = sh_g_of_e[L.topk_id[i]];
-            if (g >= 0) atomicAdd(&sh_cnt[g], 1);
-        }
+    // entries' members, loaded kAlignBatch per thread at a time so their loads overlap
+    for (int i0 = tid; i0 < nent; i0 += kAlignBatch * nthr) {
+        int ew[kAlignBatch], id[kAlignBatch];
+        load_entries(L, i0, nthr, nent, ew, id);
+#pragma unroll
+        for (int u = 0; u < kAlignBatch; ++u)
+            if (ew[u] >= 0) {
+                const int g = sh_g_of_e[id[u]];
+                if (g >= 0) atomicAdd(&sh_cnt[g], 1);
+            }
+    }
     __syncthreads();
 
     // ---- row ranges and tiles: member g's rows are padded to 128, its tiles
@@ -346,13 +365,18 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
         P.landed[g] = (sh_wp[g] & 1) ? 0u : nchunk;  // a hit is ready at once
     }
     for (int t = tid; t < nt; t += nthr) P.gu_done[t] = 0;
-    for (int i = tid; i < nent; i += nthr)
-        if (L.entry_wave[i] >= 0) {
-            const int g = sh_g_of_e[L.topk_id[i]];
-            if (g < 0) continue;
-            const int row = sh_off[g] + atomicAdd(&sh_fill[g], 1);
-            if (row < P.max_rows) P.perm[row] = i;
-        }
+    for (int i0 = tid; i0 < nent; i0 += kAlignBatch * nthr) {
+        int ew[kAlignBatch], id[kAlignBatch];
+        load_entries(L, i0, nthr, nent, ew, id);
+#pragma unroll
+        for (int u = 0; u < kAlignBatch; ++u)
+            if (ew[u] >= 0) {
+                const int g = sh_g_of_e[id[u]];
+                if (g < 0) continue;
+                const int row = sh_off[g] + atomicAdd(&sh_fill[g], 1);
+                if (row < P.max_rows) P.perm[row] = i0 + u * nthr;
+            }
+    }
     // padding rows: one warp per member
     const int lane = tid & 31;
     for (int g = tid >> 5; g < G; g += nthr >> 5) {

@@ -102,6 +102,18 @@ __device__ __forceinline__ void route_token_warp(const float* __restrict__ row, 
     out_w = lane < k ? __fdiv_rn(ex, sum) : 0.f;
 }
 
+// Routed ids of entries i0, i0 + stride, ... (kPlanBatch of them, kNoEntry
+// past nent), all loads issued before any is used.
+constexpr int kPlanBatch = 8;
+constexpr int kNoEntry = -0x7fffffff;
+__device__ __forceinline__ void load_ids(const int32_t* ids, int i0, int stride, int nent, int (&id)[kPlanBatch]) {
+#pragma unroll
+    for (int u = 0; u < kPlanBatch; ++u) {
+        const int i = i0 + u * stride;
+        id[u] = i < nent ? ids[i] : kNoEntry;
+    }
+}
+
 // Where each CTA that plans a single-wave step side by side with others keeps
 // the plan (shared memory of the caller).
 struct PlanOut {
@@ -214,12 +226,18 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
                      : "memory");
     uint32_t clock = sh_clock;
 
-    for (int i = tid; i < nent; i += nthr) {
-        const int e = ids_in_smem ? sh_ids[i] : L.topk_id[i];
-        if (e >= 0 && e < E)
-            sh_used[e] = 1;
-        else
-            sh_bad = 1;
+    for (int i0 = tid; i0 < nent; i0 += kPlanBatch * nthr) {
+        int id[kPlanBatch];
+        load_ids(ids_in_smem ? sh_ids : L.topk_id, i0, nthr, nent, id);
+#pragma unroll
+        for (int u = 0; u < kPlanBatch; ++u) {
+            const int e = id[u];
+            if (e == kNoEntry) continue;
+            if (e >= 0 && e < E)
+                sh_used[e] = 1;
+            else
+                sh_bad = 1;
+        }
     }
     __syncthreads();
 
@@ -387,16 +405,22 @@ __device__ void plan_block(const LayerDev& L, const Shape& s, const float* logit
         L.member_count[w] = 0;
     }
 
-    for (int i = tid; i < nent; i += nthr) {
-        const int m = ids_in_smem ? sh_ids[i] : L.topk_id[i];
-        const bool ok = m >= 0 && m < E;
-        L.entry_wave[i] = ok ? sh_wave_of[m] : -1;
-        L.entry_slot[i] = ok ? sh_slot_in_wave[m] : 0;
-        if (shared_plan) {
-            L.topk_id[i] = m;
-            L.topk_w[i] = out->ew[i];
+    for (int i0 = tid; i0 < nent; i0 += kPlanBatch * nthr) {
+        int id[kPlanBatch];
+        load_ids(ids_in_smem ? sh_ids : L.topk_id, i0, nthr, nent, id);
+#pragma unroll
+        for (int u = 0; u < kPlanBatch; ++u) {
+            const int m = id[u], i = i0 + u * nthr;
+            if (m == kNoEntry) continue;
+            const bool ok = m >= 0 && m < E;
+            L.entry_wave[i] = ok ? sh_wave_of[m] : -1;
+            L.entry_slot[i] = ok ? sh_slot_in_wave[m] : 0;
+            if (shared_plan) {
+                L.topk_id[i] = m;
+                L.topk_w[i] = out->ew[i];
+            }
+            if (out) out->ekey[i] = ok && sh_wave_of[m] == 0 ? sh_slot_in_wave[m] : -1;
         }
-        if (out) out->ekey[i] = ok && sh_wave_of[m] == 0 ? sh_slot_in_wave[m] : -1;
     }
     for (int i = tid; i < K; i += nthr) {
         L.slot_expert[i] = sh_slot_expert[i];
