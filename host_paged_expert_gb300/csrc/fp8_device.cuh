@@ -20,21 +20,32 @@ __device__ __forceinline__ float2 e4m3x2(uint32_t two_codes) {
 __device__ __forceinline__ float bf_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-// sum_{e<16} w_e * x_e in element order: 16 E4M3 codes against 16 bf16 values.
-__device__ __forceinline__ float dot16_e4m3_bf16(int4 w, int4 x0, int4 x1) {
-    const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
+// Gate and up dot products of one 16-code chunk each against the same 16
+// bf16 values: pg = sum_{e<16} g_e x_e and pu likewise, each summed in
+// element order from zero; the x values are widened once for both rows.
+__device__ __forceinline__ void dot16x2_e4m3_bf16(int4 wg, int4 wu, int4 x0, int4 x1, float& pg, float& pu) {
+    const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
+    const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
     const uint32_t xv[8] = {(uint32_t)x0.x, (uint32_t)x0.y, (uint32_t)x0.z, (uint32_t)x0.w,
                             (uint32_t)x1.x, (uint32_t)x1.y, (uint32_t)x1.z, (uint32_t)x1.w};
-    float p = 0.f;
+    float g = 0.f, u = 0.f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        const float2 a = e4m3x2(wv[q]), b = e4m3x2(wv[q] >> 16);
-        p = fmaf(a.x, bf_lo(xv[2 * q]), p);
-        p = fmaf(a.y, bf_hi(xv[2 * q]), p);
-        p = fmaf(b.x, bf_lo(xv[2 * q + 1]), p);
-        p = fmaf(b.y, bf_hi(xv[2 * q + 1]), p);
+        const float x0l = bf_lo(xv[2 * q]), x0h = bf_hi(xv[2 * q]);
+        const float x1l = bf_lo(xv[2 * q + 1]), x1h = bf_hi(xv[2 * q + 1]);
+        const float2 ga = e4m3x2(gv[q]), gb = e4m3x2(gv[q] >> 16);
+        const float2 ua = e4m3x2(uv[q]), ub = e4m3x2(uv[q] >> 16);
+        g = fmaf(ga.x, x0l, g);
+        u = fmaf(ua.x, x0l, u);
+        g = fmaf(ga.y, x0h, g);
+        u = fmaf(ua.y, x0h, u);
+        g = fmaf(gb.x, x1l, g);
+        u = fmaf(ub.x, x1l, u);
+        g = fmaf(gb.y, x1h, g);
+        u = fmaf(ub.y, x1h, u);
     }
-    return p;
+    pg = g;
+    pu = u;
 }
 
 // sum_{e<16} w_e * h_e in element order: 16 E4M3 codes against 16 fp32 values.
@@ -64,8 +75,10 @@ __device__ __forceinline__ float row_pair_h_fp8(const int4 (&gv)[CPL], const int
         if (idx < nchunk) {
             const int4 x0 = *reinterpret_cast<const int4*>(xr + 32 * (size_t)idx);
             const int4 x1 = *reinterpret_cast<const int4*>(xr + 32 * (size_t)idx + 16);
-            ag = fmaf(sg[c], dot16_e4m3_bf16(gv[c], x0, x1), ag);
-            au = fmaf(su[c], dot16_e4m3_bf16(uv[c], x0, x1), au);
+            float pg, pu;
+            dot16x2_e4m3_bf16(gv[c], uv[c], x0, x1, pg, pu);
+            ag = fmaf(sg[c], pg, ag);
+            au = fmaf(su[c], pu, au);
         }
     }
     ag = warp_sum(ag);

@@ -275,14 +275,26 @@ __global__ void topk_sum_kernel(const float* __restrict__ merged, __nv_bfloat16*
                                 int T, int k, int H) {
     pdl_wait();
     pdl_trigger();
-    const long long total = (long long)T * H;
-    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total;
+    // four consecutive outputs per thread (H is a multiple of 8): 16-byte
+    // loads, each output summed over j = 0..k-1 from zero as before
+    const long long total4 = (long long)T * H / 4;
+    for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total4;
          q += (long long)gridDim.x * blockDim.x) {
-        const int t = (int)(q / H);
-        const int m = (int)(q - (long long)t * H);
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j) acc = __fadd_rn(acc, merged[((size_t)t * k + j) * H + m]);
-        out[q] = __float2bfloat16_rn(acc);
+        const int t = (int)(4 * q / H);
+        const int m = (int)(4 * q - (long long)t * H);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int j = 0; j < k; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(merged + ((size_t)t * k + j) * H + m);
+            acc.x = __fadd_rn(acc.x, v.x);
+            acc.y = __fadd_rn(acc.y, v.y);
+            acc.z = __fadd_rn(acc.z, v.z);
+            acc.w = __fadd_rn(acc.w, v.w);
+        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 packed;
+        packed.x = *reinterpret_cast<const uint32_t*>(&lo);
+        packed.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(out + 4 * q) = packed;
     }
 }
 
@@ -347,7 +359,7 @@ cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_
 
 cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
                             cudaStream_t st) {
-    const long long total = (long long)T * s.H;
+    const long long total = (long long)T * s.H / 4;
     const int grid = (int)((total + 255) / 256 < 4096 ? (total + 255) / 256 : 4096);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(topk_sum_kernel, grid, 256, 0, st, merged, out, T, s.k, s.H);
