@@ -52,7 +52,13 @@ constexpr uint32_t kSpinLimit = 1u << 23;  // polls (>= 128 ns apart): about a s
 // Per-layer counters: role registration, completion counts and barriers.
 enum SyncSlot { R_LINK = 0, R_HBM, D_LINK, D_HITS, S_DOWN, P_READ, H_TICKET, S_EXIT, S_NUM };
 constexpr int kPlanCap = 256;    // planner capacity inside this kernel: E, K <= 256
-constexpr int kLinkSmEvery = 3;  // CTAs on SMs with %smid % 3 == 0 stream the host link
+// CTAs on SMs with %smid % link_every == 0 stream the host link: every third
+// SM, or every sixth for int4 steps of two or more tokens.  An int4 page-in is
+// a quarter of a bf16 one while the resident experts' GEMVs take about as
+// long, and with more tokens those GEMVs are the longer side (measured: at
+// batch 4 every sixth SM is 6 % faster than every third, at batch 1 1 %
+// slower).
+constexpr int kLinkSmEvery = 3, kLinkSmEveryInt4Batch = 6;
 
 // 32-bit words of the per-CTA plan in dynamic shared memory: member experts
 // and slots [K each], then entry slot, member index and router weight
@@ -220,7 +226,8 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     if (threadIdx.x == kThr - 32) {  // a warp that routes no token of a small step: it waits for the atomic
         unsigned smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        sh_link_sm = (smid % kLinkSmEvery) == 0;
+        const unsigned link_every = FMT == PE_INT4_GPTQ && T > 1 ? kLinkSmEveryInt4Batch : kLinkSmEvery;
+        sh_link_sm = (smid % link_every) == 0;
         sh_role_rank = (int)atomicAdd(&sync[sh_link_sm ? R_LINK : R_HBM], 1u);
     }
     // x is copied to shared memory asynchronously, underneath the planning
