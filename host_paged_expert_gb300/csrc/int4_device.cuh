@@ -95,6 +95,34 @@ __device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (
     pu = __fadd_rn(ue, uo);
 }
 
+// (q - 8) for the nibbles at bits 0 and 16 of w as an fp16 pair, exactly: the
+// fp16 with bits 0x6400 | q is 1024 + q, and 1024 + q - 1032 is representable.
+__device__ __forceinline__ uint32_t i4_pair_f16(uint32_t w) {
+    const uint32_t t = (w & 0x000F000Fu) | 0x64006400u;
+    const __half2 d = __hsub2(*reinterpret_cast<const __half2*>(&t), __float2half2_rn(1032.f));
+    return *reinterpret_cast<const uint32_t*>(&d);
+}
+
+// a * s in fp32 for the low / high fp16 half a of a pair and the fp16 scale s
+// (bits in the low half of s16): the mixed-precision fma of sm_100 with a
+// -0 addend, i.e. the exact product rounded once, as float(a) * float(s).
+__device__ __forceinline__ float i4_lo_times(uint32_t pair, uint32_t s16) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, sl, sh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {sl, sh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, al, sl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(pair), "r"(s16), "f"(-0.0f));
+    return d;
+}
+__device__ __forceinline__ float i4_hi_times(uint32_t pair, uint32_t s16) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, sl, sh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {sl, sh}, %2;\n\t"
+        "fma.rn.f32.f16 %0, ah, sl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(pair), "r"(s16), "f"(-0.0f));
+    return d;
+}
+
 // (q - 8) of the low / high code of a pair from i4_pair_bf16, as fp32.
 __device__ __forceinline__ float i4_lo_f32(uint32_t pair) { return __uint_as_float(pair << 16); }
 __device__ __forceinline__ float i4_hi_f32(uint32_t pair) { return __uint_as_float(pair & 0xffff0000u); }

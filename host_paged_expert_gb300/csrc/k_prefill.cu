@@ -569,18 +569,19 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
                     packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
                 }
             } else {
-                const float scl = __half2float(scale4[r * ng + (kb * BK) / kInt4Group]);
+                // the fp16 scale's bits; each weight is the exact product (q - 8) * s rounded to bf16
+                const uint32_t s16 = reinterpret_cast<const unsigned short*>(scale4)[r * ng + (kb * BK) / kInt4Group];
                 const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // codes 8h .. 8h+7 of the chunk: one word
                     const uint32_t w = h ? cv.y : cv.x;
                     // q - 8 exactly, two codes at a time: nibbles (0,4), (1,5), (2,6), (3,7)
-                    const uint32_t p04 = i4_pair_bf16(w), p15 = i4_pair_bf16(w >> 4);
-                    const uint32_t p26 = i4_pair_bf16(w >> 8), p37 = i4_pair_bf16(w >> 12);
-                    const __nv_bfloat162 c01 = __floats2bfloat162_rn(i4_lo_f32(p04) * scl, i4_lo_f32(p15) * scl);
-                    const __nv_bfloat162 c23 = __floats2bfloat162_rn(i4_lo_f32(p26) * scl, i4_lo_f32(p37) * scl);
-                    const __nv_bfloat162 c45 = __floats2bfloat162_rn(i4_hi_f32(p04) * scl, i4_hi_f32(p15) * scl);
-                    const __nv_bfloat162 c67 = __floats2bfloat162_rn(i4_hi_f32(p26) * scl, i4_hi_f32(p37) * scl);
+                    const uint32_t p04 = i4_pair_f16(w), p15 = i4_pair_f16(w >> 4);
+                    const uint32_t p26 = i4_pair_f16(w >> 8), p37 = i4_pair_f16(w >> 12);
+                    const __nv_bfloat162 c01 = __floats2bfloat162_rn(i4_lo_times(p04, s16), i4_lo_times(p15, s16));
+                    const __nv_bfloat162 c23 = __floats2bfloat162_rn(i4_lo_times(p26, s16), i4_lo_times(p37, s16));
+                    const __nv_bfloat162 c45 = __floats2bfloat162_rn(i4_hi_times(p04, s16), i4_hi_times(p15, s16));
+                    const __nv_bfloat162 c67 = __floats2bfloat162_rn(i4_hi_times(p26, s16), i4_hi_times(p37, s16));
                     packed[4 * h] = *reinterpret_cast<const uint32_t*>(&c01);
                     packed[4 * h + 1] = *reinterpret_cast<const uint32_t*>(&c23);
                     packed[4 * h + 2] = *reinterpret_cast<const uint32_t*>(&c45);
