@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -189,6 +190,15 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """Source text without its // and /* */ comments or blank lines, so that
+    a comment-only edit keeps a kernel's hash (no string literal in these
+    sources holds a comment marker)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(kernel: str):
     files = KERNEL_SOURCES.get(kernel)
     if not files:
@@ -196,7 +206,7 @@ def kernel_source_hash(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "host_paged_expert_gb300", "csrc")
     for n in files:
-        h.update(open(os.path.join(csrc, n), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, n)).read()).encode())
     return h.hexdigest()[:16]
 
 

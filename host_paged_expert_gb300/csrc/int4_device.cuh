@@ -4,8 +4,10 @@
 // its output row and group of 128 inputs.  A 16-byte chunk holds 32 codes of
 // one row (input 2j in the low nibble of byte j) and never crosses a group,
 // so each lane decodes its chunk, forms the chunk's dot product and adds it
-// scaled by the chunk's group scale.  Every int4 kernel computes a value with
-// these functions in the same order, so all paths agree bit for bit.
+// scaled by the chunk's group scale.  Every int4 GEMV kernel computes a value
+// with these functions in the same order, so the GEMV paths agree bit for
+// bit; the prefill converters use the pair decoding to build the bf16
+// tensor-core operand.
 #pragma once
 
 #include <cuda_fp16.h>
