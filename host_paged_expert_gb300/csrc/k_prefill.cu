@@ -268,7 +268,10 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
             sh_ms[g] = slot;
             sh_wp[g] = (w << 1) | paged;
             P.members[g] = make_int4(e, slot, w, paged);
-            if (paged) P.pin_member[npbase + q] = g;
+            if (paged) {
+                P.pin_member[npbase + q] = g;
+                sh_i0[npbase + q] = g;  // the page-in list, until the queue bases take sh_i0 over
+            }
         }
         gbase += size;
         npbase += nmiss;
@@ -308,24 +311,77 @@ __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s
     if (tid < G) {
         sh_off[tid] = off;
         sh_t0[tid] = t0;
-        for (int i = 0; i < mt && t0 + i < P.max_tiles; ++i)
-            P.tiles[t0 + i] = make_int4(off + i * MT, slot_base + sh_ms[tid], min(MT, c - i * MT), tid);
     }
     if (tid == 0) sh_t0[G] = nt;
-    // GEMM tiles of each slot's earlier occupants: members are in wave order
-    // and a slot holds one member per wave
+    // Which members have an earlier occupant of their slot in this step
+    // (sh_d0, for the staging choice below): members are in wave order and a
+    // slot holds one member per wave.  sh_cum: slot -> occupants so far.
     {
+        int wb = 0;
+        for (int w = 0; w < nW; ++w) {
+            const int size = sh_mcount[w];
+            const bool mine = tid >= wb && tid < wb + size;
+            if (mine) sh_d0[tid] = sh_cum[sh_ms[tid]];
+            __syncthreads();
+            if (mine) sh_cum[sh_ms[tid]] += 1;
+            __syncthreads();
+            wb += size;
+        }
+    }
+    // Staging: a page-in whose slot still has an earlier occupant in this step
+    // goes to a staging row (the first stage_rows such, in plan order), so the
+    // link need not wait for that occupant's tiles; its tiles read the staging
+    // row, and the row is copied into the slot once the slot is free if the
+    // member is the slot's last occupant.  sh_d0: member -> staging row or -1.
+    {
+        const int np = npbase;
+        int want = 0, gp = -1;
+        if (tid < np) {
+            gp = sh_i0[tid];
+            want = sh_d0[gp] > 0;
+        }
+        int nwant;
+        const int spos = block_excl_scan(want, sh_scan, &nwant);
+        if (tid < G) sh_d0[tid] = -1;
+        __syncthreads();
+        if (want && spos < P.stage_rows) sh_d0[gp] = spos;
+        __syncthreads();
+        // GEMM tiles of each slot's earlier occupants that read the slot
+        // itself (a staged member reads its staging row and is not counted),
+        // then each slot's last occupant (sh_cum: slot -> member)
+        for (int i = tid; i < K; i += nthr) sh_cum[i] = 0;
+        __syncthreads();
         int wb = 0;
         for (int w = 0; w < nW; ++w) {
             const int size = sh_mcount[w];
             const bool mine = tid >= wb && tid < wb + size;
             if (mine) P.slot_need[tid] = sh_cum[sh_ms[tid]];
             __syncthreads();
-            if (mine) sh_cum[sh_ms[tid]] += mt * (n1 + n2);
+            if (mine && sh_d0[tid] < 0) sh_cum[sh_ms[tid]] += mt * (n1 + n2);
             __syncthreads();
             wb += size;
         }
+        wb = 0;
+        for (int w = 0; w < nW; ++w) {
+            const int size = sh_mcount[w];
+            if (tid >= wb && tid < wb + size) sh_cum[sh_ms[tid]] = tid;
+            __syncthreads();
+            wb += size;
+        }
+        const bool commit = tid < G && sh_d0[tid] >= 0 && sh_cum[sh_ms[tid]] == tid;
+        int ncommit;
+        const int cpos = block_excl_scan(commit ? 1 : 0, sh_scan, &ncommit);
+        if (commit) P.commit_member[cpos] = tid;
+        if (tid == 0) P.counts[5] = ncommit;
     }
+    if (tid < G) {
+        const int st = sh_d0[tid];
+        P.stage_of[tid] = st;
+        const int slot_index = st >= 0 ? P.stage_base + st : slot_base + sh_ms[tid];
+        for (int i = 0; i < mt && t0 + i < P.max_tiles; ++i)
+            P.tiles[t0 + i] = make_int4(off + i * MT, slot_index, min(MT, c - i * MT), tid);
+    }
+    __syncthreads();  // sh_i0 and sh_d0 are the queue bases' from here on
     if (tid == 0) {
         // queue bases: gate/up blocks in member order, each down block once
         // `lag` more items have been queued, flushed at every wave's end
@@ -428,34 +484,88 @@ __device__ __forceinline__ void link_copy(const uint8_t* __restrict__ src, uint8
     }
 }
 
+// A copy of `bytes` (a multiple of 16, at most kLinkChunk) within HBM,
+// between rows written in this kernel: read through L2.
+__device__ __forceinline__ void hbm_copy(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, size_t bytes) {
+    const int4* sp = reinterpret_cast<const int4*>(src);
+    int4* dp = reinterpret_cast<int4*>(dst);
+    const int nvec = (int)(bytes >> 4);
+    int4 v[kLinkUnroll];
+#pragma unroll
+    for (int u = 0; u < kLinkUnroll; ++u) {
+        const int i = threadIdx.x + u * kStepThreads;
+        if (i < nvec) v[u] = __ldcg(sp + i);
+    }
+#pragma unroll
+    for (int u = 0; u < kLinkUnroll; ++u) {
+        const int i = threadIdx.x + u * kStepThreads;
+        if (i < nvec) dp[i] = v[u];
+    }
+}
+
 // Link CTA `rank` of `nL`: items (page-in p, chunk c) in plan order, round
-// robin, so the experts land one after another.
+// robin, so the experts land one after another.  A page-in whose slot is
+// still in use goes to its staging row if it has one, else it waits until
+// the slot's earlier occupants' tiles are done.  Then the commit items copy
+// each staged last occupant from its staging row into its slot, once the
+// slot is free.
 __device__ void link_role(const PrefillDev& P, const Shape& s, const uint8_t* __restrict__ host_layer,
-                          uint8_t* __restrict__ slots_layer, int rank, int nL, unsigned nchunk, uint32_t* err,
-                          int* ok_sh) {
-    const int np = P.counts[4];
-    const size_t total = (size_t)np * nchunk;
-    int last_p = -1, ok = 1;
+                          uint8_t* __restrict__ slots_layer, uint8_t* __restrict__ slots_all, int rank, int nL,
+                          unsigned nchunk, uint32_t* err, int* ok_sh) {
+    const int np = P.counts[4], ncommit = P.counts[5];
+    const size_t nstream = (size_t)np * nchunk, total = nstream + (size_t)ncommit * nchunk;
+    int last_p = -1, last_ci = -1, ok = 1;
     for (size_t it = rank; it < total; it += nL) {
-        const int p = (int)(it / nchunk);
-        const size_t c = it - (size_t)p * nchunk;
-        const int g = P.pin_member[p];
-        const int4 m = P.members[g];
-        if (p != last_p) {  // the slot's earlier occupants in this step must be done with it
-            last_p = p;
-            if (threadIdx.x == 0) *ok_sh = spin_geq(&P.slot_done[m.y], (unsigned)P.slot_need[g], &P.ctl[1], err);
+        if (it < nstream) {
+            const int p = (int)(it / nchunk);
+            const size_t c = it - (size_t)p * nchunk;
+            const int g = P.pin_member[p];
+            const int4 m = P.members[g];
+            const int st = P.stage_of[g];
+            if (p != last_p) {  // without a staging row the slot's earlier occupants must be done with it
+                last_p = p;
+                if (st < 0) {
+                    if (threadIdx.x == 0)
+                        *ok_sh = spin_geq(&P.slot_done[m.y], (unsigned)P.slot_need[g], &P.ctl[1], err);
+                    __syncthreads();
+                    ok = *ok_sh;
+                } else {
+                    ok = 1;
+                }
+            }
+            const size_t off = c * kLinkChunk;
+            uint8_t* row = st >= 0 ? slots_all + (size_t)(P.stage_base + st) * s.stride
+                                   : slots_layer + (size_t)m.y * s.stride;
+            if (ok) {
+                const size_t n = s.copy_bytes - off < kLinkChunk ? s.copy_bytes - off : kLinkChunk;
+                link_copy(host_layer + (size_t)m.x * s.stride + off, row + off, n);
+            }
             __syncthreads();
-            ok = *ok_sh;
-        }
-        const size_t off = c * kLinkChunk;
-        if (ok) {
-            const size_t n = s.copy_bytes - off < kLinkChunk ? s.copy_bytes - off : kLinkChunk;
-            link_copy(host_layer + (size_t)m.x * s.stride + off, slots_layer + (size_t)m.y * s.stride + off, n);
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            __threadfence();
-            atomicAdd(&P.landed[g], 1u);
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(&P.landed[g], 1u);
+            }
+        } else {
+            const int ci = (int)((it - nstream) / nchunk);
+            const size_t c = (it - nstream) - (size_t)ci * nchunk;
+            const int g = P.commit_member[ci];
+            const int4 m = P.members[g];
+            const int st = P.stage_of[g];
+            if (ci != last_ci) {  // the staging row has landed and the slot is free
+                last_ci = ci;
+                if (threadIdx.x == 0)
+                    *ok_sh = spin_geq(&P.landed[g], nchunk, &P.ctl[1], err) &&
+                             spin_geq(&P.slot_done[m.y], (unsigned)P.slot_need[g], &P.ctl[1], err);
+                __syncthreads();
+                ok = *ok_sh;
+            }
+            const size_t off = c * kLinkChunk;
+            if (ok && st >= 0 && st < P.stage_rows) {
+                const size_t n = s.copy_bytes - off < kLinkChunk ? s.copy_bytes - off : kLinkChunk;
+                hbm_copy(slots_all + (size_t)(P.stage_base + st) * s.stride + off,
+                         slots_layer + (size_t)m.y * s.stride + off, n);
+            }
+            __syncthreads();
         }
     }
 }
@@ -720,7 +830,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     if (sh_rank >= 0) {
         // a link CTA joins the GEMM queue once its share of the page-ins is
         // done (it then depends only on work queued before its next tile)
-        link_role(P, s, host_layer, slots_all + (size_t)slot_base * s.stride, sh_rank, sh_nlink, nchunk, err,
+        link_role(P, s, host_layer, slots_all + (size_t)slot_base * s.stride, slots_all, sh_rank, sh_nlink, nchunk, err,
                   &sh_ok);
         __syncthreads();
     }
@@ -836,7 +946,8 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                 if (warp == 2 + kConvWarps && lane == 0) {
                     __threadfence();
                     if (I.kind == 0) atomicAdd(&P.gu_done[I.t], 1u);
-                    atomicAdd(&P.slot_done[I.ti.y - slot_base], 1u);
+                    // tiles that read the slot itself (not a staging row)
+                    if (I.ti.y < P.stage_base) atomicAdd(&P.slot_done[I.ti.y - slot_base], 1u);
                 }
             }
         }

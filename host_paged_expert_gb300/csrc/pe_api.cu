@@ -182,13 +182,17 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
     const int L = c.num_layers, E = c.num_experts, K = c.num_slots;
     const size_t maxTk = (size_t)c.max_tokens * c.top_k;
     const int W = max_waves(c, c.max_tokens);
-    uint8_t* slots = cv.take<uint8_t>((size_t)L * K * r.row_stride);
+    const bool tc = tc_enabled(c, r);
+    // The prefill step pages an expert of a later wave into a staging row when
+    // its slot is still in use, so the link need not wait: K rows right after
+    // the slot table, so the weight tensor maps address them as slots.
+    const int stage_rows = tc && W >= 2 ? K : 0;
+    uint8_t* slots = cv.take<uint8_t>(((size_t)L * K + stage_rows) * r.row_stride);
     uint8_t* loaded = cv.take<uint8_t>((size_t)L * E);
     uint32_t* err = cv.take<uint32_t>(1);
     float* hbuf = cv.take<float>(maxTk * c.intermediate);
     float* merged = cv.take<float>(maxTk * c.hidden);
     PrefillDev pre = {};
-    const bool tc = tc_enabled(c, r);
     if (tc) {
         const size_t rows = prefill_max_rows((int)maxTk, E), tiles = rows / 128;
         const size_t items = prefill_max_items(make_shape(c, r), tiles);
@@ -205,6 +209,10 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
         pre.slot_done = cv.take<unsigned>(K);
         pre.ctl = cv.take<unsigned>(4);
         pre.counts = cv.take<int32_t>(8);
+        pre.stage_of = cv.take<int32_t>(E);
+        pre.commit_member = cv.take<int32_t>(E);
+        pre.stage_base = L * K;
+        pre.stage_rows = stage_rows;
         pre.max_rows = (int)rows;
         pre.max_tiles = (int)tiles;
         pre.max_items = (int)items;
@@ -296,7 +304,7 @@ pe_status setup_prefill(pe_handle* h) {
     const pe_config& c = h->cfg;
     const PrefillDev& P = h->pre;
     const cuuint64_t H = (cuuint64_t)c.hidden, I = (cuuint64_t)c.intermediate, rows = (cuuint64_t)P.max_rows;
-    const cuuint64_t nslots = (cuuint64_t)c.num_layers * c.num_slots, stride = h->row.row_stride;
+    const cuuint64_t nslots = (cuuint64_t)c.num_layers * c.num_slots + h->pre.stage_rows, stride = h->row.row_stride;
     bool ok = true;
     {
         const cuuint64_t d[2] = {H, rows}, st[1] = {H * 2};

@@ -70,8 +70,12 @@ struct PrefillDev {
     unsigned* gu_done;      // [max_tiles]    finished gate/up tiles per row tile
     unsigned* slot_done;    // [K]            finished GEMM tiles per slot in this step
     unsigned* ctl;          // [4]            GEMM ticket, abort word, link / GEMM CTAs registered
-    int32_t* counts;        // [8]            tiles, rows, items, members, page-ins
+    int32_t* counts;        // [8]            tiles, rows, items, members, page-ins, staged members to commit
+    int32_t* stage_of;      // [E]            staging row of a member paged in through staging, else -1
+    int32_t* commit_member; // [E]            staged members that are their slot's last occupant in the step
     int max_rows, max_tiles, max_items;
+    int stage_base;         // whole-table slot index of staging row 0 (the rows follow the L*K slots)
+    int stage_rows;         // staging rows (0: no staging)
 };
 
 // TMA descriptors of the prefill path, encoded once at creation.
