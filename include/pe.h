@@ -138,7 +138,10 @@ typedef struct pe_handle pe_handle;
 
 /* Device bytes the caller must provide to pe_create for this config: the
  * L*K slot table, per-layer LRU state and plans, and the forward workspace
- * for up to max_tokens tokens.  Returns 0 for an invalid config.  Pure. */
+ * for up to max_tokens tokens (with the tensor-core prefill path and steps
+ * of two or more waves, also K staging rows after the slot table, where a
+ * later wave's page-in lands while its slot is still in use).  Returns 0 for
+ * an invalid config.  Pure. */
 size_t pe_required_device_bytes(const pe_config* cfg);
 
 /* Slot count for a device-memory budget.  "Paged Experts" (SGLang docs),
