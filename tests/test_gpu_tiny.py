@@ -350,3 +350,41 @@ def test_prefill_tiles_over_128_rows():
         assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"], T
     b.close()
     a.close()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "int4"])
+def test_consecutive_multiwave_prefills_keep_slots_exact(dtype):
+    """Prefill steps of three waves in a row (K = 6 of 16 experts): a later
+    wave's page-ins go through the staging rows while their slots are still in
+    use (the second wave's fill them, the third wave's wait), and the slots'
+    last occupants are copied in from there.  Every step equals K = E bit for
+    bit, plans and residency equal the oracle's, and every resident slot
+    holds its expert's host row byte for byte."""
+    _lib = _need_gpu()
+    s = synth.MoEShape(1, 16, 2, 6, 256, 256, dtype)
+    w = synth.ExpertWeights(s, seed=3)
+    a = _lib.PagedMoE(s, max_tokens=65)
+    gu.load_stack(a, w)
+    b = _lib.PagedMoE(s.with_slots(s.num_experts), max_tokens=65, store_owner=a)
+    o = omlp.PagedLayer(s.num_experts, s.num_slots, s.top_k, gu.expert_fn(w, 0))
+    waves = []
+    for i, T in enumerate((64, 65, 64, 48)):
+        xb = synth.hidden_states((T,), s.hidden, seed=T, tag=9 + i)
+        lg = synth.prefill_logits(1, s.num_experts, T, seed=T + i)[0]
+        x, l = gu.to_dev_bf16(xb), gu.to_dev_f32(lg)
+        ya, yb = a.forward(0, x, l), b.forward(0, x, l)
+        out, _, plan, ids, wts = o.step(xb, lg)
+        waves.append(len(plan.waves))
+        gu.check_plan(a.read_plan(0, T), plan, ids, wts)
+        gu.check_residency(a.read_residency(0), o.sim)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), (dtype, i)
+        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2[dtype], (dtype, i)
+        for slot, e in enumerate(a.read_residency(0)["slot_expert"].tolist()):
+            if e >= 0:
+                got = a.read_slot(0, slot, a.layout["payload_bytes"])
+                want = a.host_row(0, e)[: a.layout["payload_bytes"]]
+                assert np.array_equal(got, want), (dtype, i, slot, e)
+    assert max(waves) >= 3, waves
+    assert a.stats(0)["error_word"] == 0
+    a.close()
+    b.close()
