@@ -14,9 +14,10 @@
 // After the planner, a layer step is three kernels:
 //   align   (one CTA) lays out every member of every wave: a packed row range
 //           per member (padded to 128 rows), the row -> entry map, a tile
-//           table, the GEMM work queue, the page-in list, and for each
-//           member how many GEMM tiles of its slot's earlier occupants in
-//           this step must finish before its page-in may overwrite the slot;
+//           table, the GEMM work queue, the page-in list, the staging rows
+//           (below), and for each member how many GEMM tiles of its slot's
+//           earlier occupants in this step must finish before the slot may
+//           be overwritten;
 //   gather  copies each entry's token row of x into the packed A operand;
 //   step    one persistent CTA per SM.  The CTA on every fourth SM streams
 //           the host link: it copies 64 KiB chunks of the planned experts, in plan
@@ -29,9 +30,14 @@
 //           down tile once all gate/up tiles of its rows are done.  So the
 //           resident experts compute while the misses page in, every paged
 //           expert computes as soon as it has landed, and wave w+1's page-in
-//           runs under wave w's GEMMs, slot by slot.
-// The waves stay exactly the planner's: a page-in never overwrites a slot
-// before the GEMMs of the slot's previous expert are done with it.
+//           runs under wave w's GEMMs.
+// A page-in whose slot an earlier wave's expert still uses streams into one
+// of K staging rows after the slot table instead of waiting (the first K
+// such, in plan order; the others wait for the slot): its tiles read the
+// staging row, and if it is the slot's last occupant in the step, a link CTA
+// copies the row into the slot once every tile that reads the slot is done.
+// The waves, the residency after the step and the results stay exactly the
+// planner's: nothing overwrites a slot before the GEMMs that read it are done.
 //
 // A GEMM tile is up to 256 rows of one expert x 128 output columns.  A GEMM
 // CTA is a pipeline of warp roles that hand tiles on through mbarriers:
