@@ -143,3 +143,24 @@ def test_slots_for_budget(L):
         if k < s.num_experts:
             assert _lib.required_device_bytes(s.with_slots(k + 1), T) > budget
         assert abs(k - sizing.slots_for_budget(budget, fixed, per_slot, s.num_experts, s.top_k)) <= 1
+
+
+def test_prefill_arena_holds_one_staging_row_per_slot(L):
+    """With the tensor-core prefill path and steps of two or more waves, the
+    arena adds K staging rows after the slot table: one slot more costs one
+    expert row per layer plus one staging row, against one row per layer at
+    decode sizes (the other per-slot buffers are a few hundred bytes)."""
+    s = synth.STACK48
+    stride = _lib.row_layout(s)["row_stride"]
+    assert _lib.max_waves(s, 2048) >= 2
+    per_slot_prefill = _lib.required_device_bytes(s, 2048) - _lib.required_device_bytes(s.with_slots(31), 2048)
+    per_slot_decode = _lib.required_device_bytes(s, 8) - _lib.required_device_bytes(s.with_slots(31), 8)
+    assert abs(per_slot_decode - s.num_layers * stride) < 64 * 1024
+    assert abs(per_slot_prefill - per_slot_decode - stride) < 64 * 1024
+    # one wave at most (K = E): no staging rows, so the arena beyond the slot
+    # table is K rows smaller than at K = 32
+    full = s.with_slots(s.num_experts)
+    assert _lib.max_waves(full, 2048) == 1
+    beyond_full = _lib.required_device_bytes(full, 2048) - s.num_layers * s.num_experts * stride
+    beyond_32 = _lib.required_device_bytes(s, 2048) - s.num_layers * s.num_slots * stride
+    assert abs(beyond_32 - beyond_full - s.num_slots * stride) < 256 * 1024
