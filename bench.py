@@ -190,6 +190,14 @@ KERNEL_SOURCES = {
 }
 
 
+def max_miss_rate_for_rate(link_gbs: float, tok_s: float, layers: int, top_k: int, expert_bytes: int) -> float:
+    """The largest per-entry miss rate a token rate allows over a link of
+    link_gbs if every missed entry moved a whole expert row: the link's bytes
+    per token over the bytes of a token whose every routed expert missed
+    ("¿Por qué es rápido…?": the pages' bound on the unmeasured miss rate)."""
+    return link_gbs * 1e9 / tok_s / (layers * top_k * expert_bytes)
+
+
 def _code_only(text: str) -> str:
     """Source text without its // and /* */ comments or blank lines, so that
     a comment-only edit keeps a kernel's hash (no string literal in these
@@ -645,11 +653,9 @@ def main():
                     "miss_rate_per_distinct": round(d["page_ins"] / max(1, d["distinct"]), 4),
                     "bytes_per_token": int(d["page_ins"] / args.steps * r["payload"]),
                     "random_routing_miss_rate": round(1.0 - shape.num_slots / shape.num_experts, 4),
-                    # the largest per-entry miss rate this run's token rate allows over the probed
-                    # link if every missed entry moved a whole expert (the pages' upper bound)
-                    "max_miss_rate_for_rate": round(
-                        max(r["link"]["copy_engine_gbs"], r["link"]["kernel_gbs"]) * 1e9 / (r["tok_s"] / world)
-                        / (L * shape.top_k * r["payload"]), 4),
+                    "max_miss_rate_for_rate": round(max_miss_rate_for_rate(
+                        max(r["link"]["copy_engine_gbs"], r["link"]["kernel_gbs"]), r["tok_s"] / world, L,
+                        shape.top_k, r["payload"]), 4),
                     "link_probe_gbs": r["link"]},
         "setup_s": round(r["t_load"], 1),
     }

@@ -29,3 +29,20 @@ def test_reference_arm_prints_one_contract_line():
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("decode48")
+
+
+def test_reported_miss_rate_bound_is_the_pages_arithmetic():
+    """bench.py's max_miss_rate_for_rate is the oracle's bound: with the
+    pages' worked numbers (50 GB/s, 87.7 tok/s, 48 layers, top-8, the 4.72 MB
+    block-FP8 expert) both give the pages' 31 %."""
+    import importlib.util
+
+    from oracle import sizing
+
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    fp8 = sizing.expert_bytes(2048, 768, "fp8")
+    got = bench.max_miss_rate_for_rate(50.0, 87.7, 48, 8, fp8)
+    assert abs(got - sizing.max_miss_rate(50e9, 87.7, 48, 8, fp8)) < 1e-12
+    assert round(got, 2) == 0.31
