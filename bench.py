@@ -32,6 +32,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -91,6 +92,9 @@ def parse():
     p.add_argument("--probe-bytes", type=int, default=2 << 30)
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: run a shorter stack of the same layer shape")
+    p.add_argument("--repeats", type=int, default=3,
+                   help="timed passes of the value and e2e measurements (median reported)")
+    p.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args()
 
 
@@ -123,11 +127,11 @@ class ClockSampler:
     def __init__(self, device):
         self.device = device
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"pe_clocks_dev{device}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.device), f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
@@ -147,6 +151,15 @@ class ClockSampler:
             self.f.close()
 
     def summary(self):
+        try:
+            return self._summary()
+        finally:
+            try:
+                os.unlink(self.path)
+            except OSError:
+                pass
+
+    def _summary(self):
         if not self.proc or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm, mx, reasons = [], [], set()
@@ -305,30 +318,40 @@ def run_ours(args, rep):
     def barrier():
         replicas.barrier(rep)
 
-    # ---- value pass
-    with torch.cuda.stream(stream):
-        model.reset_residency(stream)
-        for t in range(W):
-            step(t)
-        s0 = model.stats(-1)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        stream.synchronize()
-        barrier()
-        torch.cuda.synchronize()
-        with ClockSampler(dev) as clk:
+    # ---- value pass: `repeats` timed passes of K tokens, each from empty slots
+    def value_pass():
+        with torch.cuda.stream(stream):
+            model.reset_residency(stream)
+            for t in range(W):
+                step(t)
+            s0 = model.stats(-1)
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            stream.synchronize()
+            barrier()
+            torch.cuda.synchronize()
             ev0.record(stream)
             for t in range(W, S):
                 step(t)
             ev1.record(stream)
             stream.synchronize()
-        torch.cuda.synchronize()
-        barrier()
-        ms = ev0.elapsed_time(ev1)
-        s1 = model.stats(-1)
+            torch.cuda.synchronize()
+            barrier()
+            s1 = model.stats(-1)
+        return ev0.elapsed_time(ev1), s0, s1
+
+    runs = []
+    with ClockSampler(dev) as clk:
+        for _ in range(max(1, args.repeats)):
+            runs.append(value_pass())
     clocks = clk.summary()
-    ms = replicas.max_over_replicas(rep, ms, device=dev)
+    run_ms = [replicas.max_over_replicas(rep, r_[0], device=dev) for r_ in runs]
+    ms = statistics.median(run_ms)
+    s0, s1 = runs[0][1], runs[0][2]
     tok_s = replicas.job_rate(K * B, world, ms)
-    log(f"value pass: {ms:.1f} ms for {K} steps -> {tok_s:.1f} tok/s")
+    spread = {"runs_tok_s": [round(replicas.job_rate(K * B, world, m), 2) for m in run_ms],
+              "min": round(replicas.job_rate(K * B, world, max(run_ms)), 2),
+              "max": round(replicas.job_rate(K * B, world, min(run_ms)), 2)}
+    log(f"value pass: median {ms:.1f} ms for {K} steps -> {tok_s:.1f} tok/s (runs {spread['runs_tok_s']})")
     d = {n: s1[n] - s0[n] for n in ("steps", "waves", "entries", "distinct", "hits", "page_ins")}
 
     # ---- e2e pass: host buffers, copies inside the timed region
@@ -337,32 +360,37 @@ def run_ours(args, rep):
         hs_pin = torch.from_numpy(hs_h.view(np.int16)).view(torch.bfloat16).pin_memory()
         lg_pin = torch.from_numpy(lg_h).pin_memory()
         y_pin = torch.empty((S, L, B, H), dtype=torch.bfloat16).pin_memory()
-        with torch.cuda.stream(stream):
-            model.reset_residency(stream)
 
-            def step_host(t):
-                x_st.copy_(hs_pin[t], non_blocking=True)
-                l_st.copy_(lg_pin[t], non_blocking=True)
-                if graph is not None:
-                    graph.replay()
-                else:
-                    launch_token()
-                y_pin[t].copy_(y_st, non_blocking=True)
+        def step_host(t):
+            x_st.copy_(hs_pin[t], non_blocking=True)
+            l_st.copy_(lg_pin[t], non_blocking=True)
+            if graph is not None:
+                graph.replay()
+            else:
+                launch_token()
+            y_pin[t].copy_(y_st, non_blocking=True)
 
-            for t in range(W):
-                step_host(t)
-            stream.synchronize()
-            barrier()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            for t in range(W, S):
-                step_host(t)
-            b.record(stream)
-            stream.synchronize()
-            e_ms = a.elapsed_time(b)
-        e_ms = replicas.max_over_replicas(rep, e_ms, device=dev)
+        e_runs = []
+        for _ in range(max(1, args.repeats)):
+            with torch.cuda.stream(stream):
+                model.reset_residency(stream)
+                for t in range(W):
+                    step_host(t)
+                stream.synchronize()
+                barrier()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for t in range(W, S):
+                    step_host(t)
+                b.record(stream)
+                stream.synchronize()
+                e_runs.append(replicas.max_over_replicas(rep, a.elapsed_time(b), device=dev))
+        e_ms = statistics.median(e_runs)
         e2e = {"value": round(replicas.job_rate(K * B, world, e_ms), 2), "unit": "tok/s",
-               "h2d_bytes_per_step": L * B * (H * 2 + E * 4), "d2h_bytes_per_step": L * B * H * 2}
+               "h2d_bytes_per_step": L * B * (H * 2 + E * 4), "d2h_bytes_per_step": L * B * H * 2,
+               "runs_tok_s": [round(replicas.job_rate(K * B, world, m), 2) for m in e_runs],
+               "timed": f"median of {len(e_runs)} passes of {K} steps"}
+        log(f"e2e pass: {e2e['value']} tok/s (runs {e2e['runs_tok_s']})")
 
     # ---- trace pass: per-kernel events, per-layer counters, layer-step latency
     trace = None
@@ -397,7 +425,7 @@ def run_ours(args, rep):
             model.profile_enable(False)
         trace = {"prof": prof, "roof_s": roof_s, "lat_us": lat, "peaks": peaks}
 
-    out = {"tok_s": tok_s, "ms": ms, "clocks": clocks, "d": d, "e2e": e2e, "trace": trace,
+    out = {"tok_s": tok_s, "ms": ms, "spread": spread, "clocks": clocks, "d": d, "e2e": e2e, "trace": trace,
            "link": {"copy_engine_gbs": round(ce_gbs, 1), "kernel_gbs": round(kn_gbs, 1)},
            "t_load": t_load, "shape": shape, "B": B, "desc": desc, "payload": payload,
            "layout": model.layout, "lg_h": lg_h, "hs_h": hs_h, "weights": weights}
@@ -579,10 +607,82 @@ def oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=None, n_steps=None, 
 
 
 def blas_threads():
-    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
-        if os.environ.get(k):
-            return int(os.environ[k])
-    return os.cpu_count()
+    """Threads the BLAS under numpy actually uses: threadpoolctl where it is
+    installed, else the OpenBLAS library numpy loaded, asked directly."""
+    try:
+        import threadpoolctl
+
+        n = sum(i["num_threads"] for i in threadpoolctl.threadpool_info() if i.get("user_api") == "blas")
+        if n:
+            return int(n)
+    except Exception:
+        pass
+    try:
+        import ctypes
+
+        libs = sorted({ln.split()[-1] for ln in open("/proc/self/maps") if "openblas" in ln.lower()
+                       and ln.split()[-1].startswith("/")})
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                        "openblas_get_num_threads"):
+                fn = getattr(lib, sym, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return int(fn())
+    except Exception:
+        pass
+    return None
+
+
+ONE_CORE_ENV = {"OPENBLAS_NUM_THREADS": "1", "OMP_NUM_THREADS": "1", "MKL_NUM_THREADS": "1"}
+
+
+def oracle_leg(args):
+    """The oracle on this process's cores over the workload's steady state
+    (after one whole token of warm-up); prints one JSON object.  Run by
+    oracle_one_core() in a fresh process pinned to one core."""
+    shape, B, _ = workload(args.workload)
+    weights = synth.ExpertWeights(shape, seed=0)
+    L = shape.num_layers
+    lg_h, hs_h = make_inputs(shape, B, 1 + int(args.cpu_seconds * 4 / L) + 8)
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=args.cpu_seconds, warm=L)
+    print(json.dumps({"steps": steps, "seconds": sec, "tok_s": steps / L * B / sec,
+                      "blas_threads": blas_threads(), "cores": len(os.sched_getaffinity(0))}), flush=True)
+
+
+def oracle_one_core(workload_name: str, seconds: float):
+    """The same oracle leg in a fresh interpreter confined to one core, with
+    one BLAS thread (a new process, never a fork of this CUDA process)."""
+    env = dict(os.environ, **ONE_CORE_ENV)
+    cpu = sorted(os.sched_getaffinity(0))[0]
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload", workload_name,
+           "--cpu-seconds", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=seconds * 6 + 120,
+                           preexec_fn=lambda: os.sched_setaffinity(0, {cpu}))
+        return json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as exc:  # reported, not fatal: the GPU line stands on its own
+        return {"error": f"{type(exc).__name__}: {exc}"}
+
+
+def cpu_baseline_entry(shape, B, weights, lg_h, hs_h, seconds, workload_name):
+    """cpu_baseline: the oracle at all cores and at one core, steady state."""
+    L = shape.num_layers
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=seconds, warm=L)
+    one = oracle_one_core(workload_name, seconds)
+    out = {"value": round(steps / L * B / sec, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+           "blas_threads": blas_threads(), "kind": "oracle",
+           "sample": f"{steps} layer-steps (token-major) after one whole token of warm-up, {sec:.1f} s, "
+                     "fp64 numpy"}
+    if "tok_s" in one:
+        out["one_core"] = {"value": round(one["tok_s"], 4), "unit": "tok/s", "cores": one["cores"],
+                           "blas_threads": one["blas_threads"],
+                           "sample": f"{one['steps']} layer-steps after one token of warm-up, "
+                                     f"{one['seconds']:.1f} s, one core"}
+    else:
+        out["one_core"] = one
+    return out
 
 
 def run_reference(args, rep):
@@ -590,18 +690,23 @@ def run_reference(args, rep):
         return
     shape, B, desc = workload(args.workload)
     weights = synth.ExpertWeights(shape, seed=0)
-    n_tok = max(1, -(-(args.warmup + args.steps) // shape.num_layers)) + 1
+    L = shape.num_layers
+    # steady state: one whole token (L layer-steps) of warm-up fills the
+    # slots the way a running decode has them, then W more untimed steps
+    warm = L + args.warmup
+    n_tok = -(-(warm + args.steps) // L) + 1
     lg_h, hs_h = make_inputs(shape, B, n_tok)
-    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, n_steps=args.steps, warm=args.warmup)
-    tok_s = steps / shape.num_layers * B / sec
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, n_steps=args.steps, warm=warm)
+    tok_s = steps / L * B / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tok/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": f"{args.workload}: {desc}",
                                             "step": "one layer-step of the CPU oracle; tok/s = layer-steps / 48 / s"},
-            "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": f"{steps} layer-steps after {args.warmup} warm-up layer-steps, "
-                                       "token-major over the 48 layers"},
+            "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
+                             "blas_threads": blas_threads(), "kind": "oracle",
+                             "sample": f"{steps} layer-steps after {warm} warm-up layer-steps (one whole token, "
+                                       f"then {args.warmup}), token-major over the {L} layers"},
             "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -611,6 +716,9 @@ def run_reference(args, rep):
 
 def main():
     args = parse()
+    if args.oracle_leg:
+        oracle_leg(args)
+        return
     rep = replicas.from_env()
     rank, world, local_rank = rep.rank, rep.world, rep.local_rank
     if args.impl == "reference":
@@ -647,7 +755,10 @@ def main():
                    "l2": "inputs larger than L2: each step streams ~%.1f GB of expert weights"
                          % (d["distinct"] / args.steps * r["payload"] / 1e9)},
         "clocks": r["clocks"],
-        "gpu_launches": args.steps * L * launches_per_layer_step(shape, B),
+        "value_spread": dict(r["spread"], timed=f"value = median of {len(r['spread']['runs_tok_s'])} passes, "
+                                                 f"each {args.warmup} warm-up and {args.steps} timed steps "
+                                                 "from empty slots"),
+        "gpu_launches": args.steps * L * launches_per_layer_step(shape, B),  # per timed pass of K steps
         "page_in": {"per_token": round(d["page_ins"] / args.steps, 3),
                     "miss_rate_per_entry": round(d["page_ins"] / max(1, d["entries"]), 4),
                     "miss_rate_per_distinct": round(d["page_ins"] / max(1, d["distinct"]), 4),
@@ -694,7 +805,21 @@ def main():
                             "peak_src": ("same-run host-link probe (best of copy engine and device loads)"
                                          if kd["bound"] == "host_link"
                                          else f"MEASURED_PEAKS.json hbm_gbs ({peaks['src']})"),
-                            "bytes_per_launch": kd["bytes_per_launch"]}
+                            "bytes_per_launch": kd["bytes_per_launch"],
+                            "source": "eager trace pass (per-kernel CUDA events)"}
+        if dom == "decode_step" and not args.no_graph and launches_per_layer_step(shape, B) == 1:
+            # one kernel per layer-step: in the graph-timed value pass its
+            # average duration is at most the pass time / (K*L), gaps included
+            avg_us = r["ms"] * 1e3 / (args.steps * L)
+            ach = d["page_ins"] * r["payload"] / (r["ms"] * 1e-3) / 1e9
+            line["roofline"].update({"achieved": round(ach, 1), "frac": round(ach / kd["peak_gbs"], 4),
+                                     "bytes_per_launch": round(d["page_ins"] * r["payload"] / (args.steps * L)),
+                                     "avg_launch_us": round(avg_us, 2),
+                                     "source": "graph-replayed value pass (median pass): one decode_step launch "
+                                               "per layer-step, average duration = pass time / (steps x layers), "
+                                               "launch gaps included",
+                                     "eager_trace": {"achieved": kd["achieved_gbs"], "frac": kd["frac"],
+                                                     "avg_launch_us": kd["avg_us"]}})
         line["kernels"] = kernels
         lat = sorted(tr["lat_us"])
         line["layer_step_us"] = {"p50": round(lat[len(lat) // 2], 1), "p99": round(lat[int(len(lat) * 0.99)], 1),
@@ -706,11 +831,8 @@ def main():
                           "divided by the graph-timed value pass",
             "hbm_gbs": peaks["hbm_gbs"], "link_gbs": link}
     if world == 1 and not args.no_cpu_baseline:
-        steps, sec = oracle_layer_steps(shape, r["weights"], r["lg_h"], r["hs_h"], budget_s=args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(steps / L * B / sec, 4), "unit": "tok/s", "cores": blas_threads(),
-                                "kind": "oracle",
-                                "sample": f"first {steps} layer-steps (token-major) of this workload, "
-                                          f"{sec:.1f} s, fp64 numpy"}
+        line["cpu_baseline"] = cpu_baseline_entry(shape, B, r["weights"], r["lg_h"], r["hs_h"], args.cpu_seconds,
+                                                  args.workload)
     print(json.dumps(line), flush=True)
     replicas.finish(rep)
 

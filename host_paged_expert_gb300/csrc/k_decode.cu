@@ -288,10 +288,14 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     const int row_blocks = (s.H + RD - 1) / RD;
     // roles: registration is complete long before the plan is (bounded wait)
     if (threadIdx.x == 0) {
-        for (uint32_t i = 0; i < kSpinLimit; ++i) {
-            if (ld_acquire_u32(&sync[R_LINK]) + ld_acquire_u32(&sync[R_HBM]) >= (unsigned)G) break;
-            __nanosleep(64);
+        bool all = false;
+        for (uint32_t i = 0; i < kSpinLimit && !all; ++i) {
+            all = ld_acquire_u32(&sync[R_LINK]) + ld_acquire_u32(&sync[R_HBM]) >= (unsigned)G;
+            if (!all) __nanosleep(64);
         }
+        // CTAs that were not all resident would split the work inconsistently:
+        // name the cause here rather than in a later phase wait
+        if (!all) atomicOr(err, PE_DEVERR_TIMEOUT);
     }
     __syncthreads();
     const int nL = (int)__ldcg(&sync[R_LINK]), nH = G - nL;
@@ -568,10 +572,38 @@ cudaError_t decode_setup_kernels() {
     return e;
 }
 
+cudaError_t decode_ctas_per_sm(int dtype, int* out) {
+    // The phase counters need every CTA of the grid resident at once, so the
+    // grid is (resident CTAs per SM, at most 2) x SMs, taken at the largest
+    // dynamic shared memory a launch may ask for and over every instantiation
+    // of the format.
+    int best = 2;
+    cudaError_t e = cudaSuccess;
+#define PE_OCC(N, F)                                                                                              \
+    if (!e) {                                                                                                     \
+        int n = 0;                                                                                                \
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_step_kernel<N, F>, kThr, kDynBudget);        \
+        if (!e && n < best) best = n;                                                                             \
+    }
+#define PE_OCC_F(F) PE_OCC(1, F) PE_OCC(2, F) PE_OCC(4, F) PE_OCC(8, F)
+    if (dtype == PE_FP8_BLOCK128) {
+        PE_OCC_F(PE_FP8_BLOCK128)
+    } else if (dtype == PE_INT4_GPTQ) {
+        PE_OCC_F(PE_INT4_GPTQ)
+    } else {
+        PE_OCC_F(PE_BF16)
+    }
+#undef PE_OCC_F
+#undef PE_OCC
+    *out = e ? 0 : best;
+    return e;
+}
+
 cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* logits, const __nv_bfloat16* x,
                                 const uint8_t* host_layer, uint8_t* slots_layer, int T, float* hbuf, float* merged,
-                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st) {
-    const int grid = num_sms * 2;  // two CTAs per SM: every CTA is resident at once
+                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, int ctas_per_sm,
+                                cudaStream_t st) {
+    const int grid = num_sms * ctas_per_sm;  // every CTA is resident at once (decode_ctas_per_sm)
     const size_t meta = (size_t)4 * decode_meta_words(s);
     const size_t xbytes = (size_t)T * s.H * 2;
     const int stage = meta + xbytes <= (size_t)kDynBudget;

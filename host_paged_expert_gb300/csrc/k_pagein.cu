@@ -1,13 +1,13 @@
 // Page-in: copy the experts a wave planned from the host store into slots.
 //
-// "Paged Experts" (SGLang docs), "Captured decode": a kernel copies the
-// planned experts of every paged tensor from the pinned host store into
-// their slots, reading host memory directly through its unified address and
-// taking the count from device memory, so each graph replay moves exactly the
-// experts it decided on.  Here one expert row holds every paged tensor of the
-// expert (w13, w2 and, for FP8, both scale grids), so copying the row pages
-// all of them together: a slot can never hold one expert's weights with
-// another expert's scales.
+// "Paged Experts" (SGLang docs), "Captured decode".  The copy is done by
+// GPU threads that load the host store's rows directly (the store is pinned
+// and mapped, so it has a device-visible address); how many rows to move is
+// read from the plan in device memory, so a replayed graph copies whatever
+// that replay's plan chose, with no host involvement.  One expert row holds
+// all of an expert's paged tensors (w13, w2 and any scale tensors), so one
+// row copy moves them together and a slot never pairs one expert's weights
+// with another expert's scales.
 //
 // The grid is fixed from shapes (a few CTAs per SM); CTAs stride over
 // (planned expert, 16 KiB chunk) items and stop at the device-side count.

@@ -818,9 +818,17 @@ __global__ void __launch_bounds__(kStepThreads, 1)
         const bool link = smid % kLinkEvery == 0;
         int rank = (int)atomicAdd(&P.ctl[link ? 2 : 3], 1u);
         int nlink = 0;
-        for (uint32_t i = 0; i < kSpin; ++i) {  // every CTA of the grid is resident: registration ends
-            if (ld_acquire(&P.ctl[2]) + ld_acquire(&P.ctl[3]) >= gridDim.x) break;
-            __nanosleep(64);
+        bool all = false;
+        for (uint32_t i = 0; i < kSpin && !all; ++i) {  // every CTA of the grid is resident: registration ends
+            all = ld_acquire(&P.ctl[2]) + ld_acquire(&P.ctl[3]) >= gridDim.x;
+            if (!all) __nanosleep(64);
+        }
+        if (!all) {
+            // CTAs could read different link-CTA counts and split the page-ins
+            // inconsistently: record the cause and abort the step, so every
+            // wait gives up at once and the kernel ends
+            atomicOr(err, PE_DEVERR_TIMEOUT);
+            atomicExch(&P.ctl[1], 1u);
         }
         nlink = (int)ld_acquire(&P.ctl[2]);
         if (nlink == 0 && !link && rank == 0) {  // no SM of the link's kind: the first GEMM CTA streams it
@@ -1019,6 +1027,20 @@ cudaError_t prefill_setup_kernels() {
     if (!e)
         e = cudaFuncSetAttribute(prefill_step_kernel<PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Tile<PE_INT4_GPTQ>::SMEM);
+    return e;
+}
+
+cudaError_t prefill_step_ctas_per_sm(int dtype, int* out) {
+    int n = 0;
+    cudaError_t e = dtype == PE_FP8_BLOCK128
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_FP8_BLOCK128>,
+                                                                        kStepThreads, Tile<PE_FP8_BLOCK128>::SMEM)
+                    : dtype == PE_INT4_GPTQ
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_INT4_GPTQ>,
+                                                                        kStepThreads, Tile<PE_INT4_GPTQ>::SMEM)
+                        : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_BF16>, kStepThreads,
+                                                                        Tile<PE_BF16>::SMEM);
+    *out = e ? 0 : n;
     return e;
 }
 

@@ -152,6 +152,7 @@ struct pe_handle {
     PrefillDev pre = {};
     PrefillMaps maps;
     int num_sms = 0;
+    int decode_ctas_per_sm = 0;  // resident CTAs per SM of the decode step kernel (1 or 2)
     std::string last_error;
     // per-kernel timing
     bool prof_on = false;
@@ -406,14 +407,32 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
         return fail(nullptr, PE_ERR_CUDA, std::string("device attribute: ") + cudaGetErrorString(ce));
     }
     ce = decode_setup_kernels();
+    if (!ce) ce = decode_ctas_per_sm(cfg->dtype, &h->decode_ctas_per_sm);
     if (ce) {
         delete h;
         return fail(nullptr, PE_ERR_CUDA, std::string("decode kernel attributes: ") + cudaGetErrorString(ce));
+    }
+    // The one-kernel decode step and the prefill step order their phases
+    // with counters that every CTA of the grid must reach, so all of a grid's
+    // CTAs have to be resident at once; refuse a device where they cannot be.
+    if (h->decode_ctas_per_sm < 1) {
+        delete h;
+        return fail(nullptr, PE_ERR_CUDA, "the decode step kernel cannot be resident on this device (occupancy 0)");
     }
     if (h->tc_ok && setup_prefill(h) != PE_OK) {
         const std::string msg = h->last_error;
         delete h;
         return fail(nullptr, PE_ERR_CUDA, msg);
+    }
+    if (h->tc_ok) {
+        int n = 0;
+        ce = prefill_step_ctas_per_sm(cfg->dtype, &n);
+        if (ce || n < 1) {
+            delete h;
+            return fail(nullptr, PE_ERR_CUDA,
+                        ce ? std::string("prefill occupancy: ") + cudaGetErrorString(ce)
+                           : std::string("the prefill step kernel cannot be resident on this device (occupancy 0)"));
+        }
     }
 
     const size_t store_bytes = (size_t)cfg->num_layers * cfg->num_experts * r.row_stride;
@@ -625,7 +644,7 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
         // one wave of decode size: the whole step, plan included, in one kernel
         ProfScope p(h, P_DECODE, st);
         e = launch_decode_fused(L, s, router_logits, x, host_layer, slots_layer, T, h->hbuf, h->merged, y, L.dsync,
-                                h->err, h->num_sms, st);
+                                h->err, h->num_sms, h->decode_ctas_per_sm, st);
         if (e) return cuda_fail(h, e, "decode kernel");
         return PE_OK;
     }

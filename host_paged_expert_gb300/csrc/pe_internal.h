@@ -92,6 +92,10 @@ bool prefill_tc_supported(const Shape& s);
 size_t prefill_max_rows(int max_entries, int E);
 size_t prefill_max_items(const Shape& s, size_t max_tiles);
 cudaError_t prefill_setup_kernels();
+// CTAs of the prefill step kernel for this format that fit on one SM (its
+// grid is one CTA per SM, all resident at once; call after
+// prefill_setup_kernels).
+cudaError_t prefill_step_ctas_per_sm(int dtype, int* out);
 // Prefill step, part 1 (after the planner): lay out every wave's members,
 // tiles, GEMM queue and page-in list, and gather the token rows (align +
 // gather kernels).
@@ -149,9 +153,14 @@ cudaError_t launch_down(const LayerDev& L, const Shape& s, const uint8_t* slots_
 bool decode_fused_supported(const Shape& s, int T);
 int decode_fused_sync_words();
 cudaError_t decode_setup_kernels();
+// Resident CTAs per SM of the decode step kernel for this format, capped at
+// 2 (its grid is this many CTAs per SM, all resident at once; call after
+// decode_setup_kernels).  0 means it cannot run.
+cudaError_t decode_ctas_per_sm(int dtype, int* out);
 cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* logits, const __nv_bfloat16* x,
                                 const uint8_t* host_layer, uint8_t* slots_layer, int T, float* hbuf, float* merged,
-                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, cudaStream_t st);
+                                __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, int ctas_per_sm,
+                                cudaStream_t st);
 
 // Block-FP8 counterparts of the three decode kernels above.
 cudaError_t launch_gateup_pagein_fp8(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,

@@ -278,8 +278,11 @@ pe_status pe_profile_read(pe_handle* h, pe_profile_t* out);
  *   alias x.  H <= 2048 and I <= 1024, both multiples of 8.
  * The intermediate h (num_tokens * I fp32) lives in a static device array of
  * PE_NOALLOC_SCRATCH_BYTES; larger requests return PE_ERR_RANGE before any
- * launch.  The result equals pe_forward on a one-expert layer (E = K =
- * top_k = 1) with the same weights, bit for bit.
+ * launch.  For num_tokens <= 64 the result equals pe_forward on a one-expert
+ * layer (E = K = top_k = 1) with the same weights bit for bit: both run the
+ * same GEMV arithmetic.  Above 64 tokens pe_forward switches to its
+ * tensor-core path, which rounds h to bf16 and sums in another order, so
+ * there the two agree only within bf16 rounding (rel-L2 well under 1e-2).
  * The first call on a device looks up the array's device address with that
  * device current; make that first call before any stream capture.  Every
  * call shares the one array per device: calls whose kernels overlap on the

@@ -1,15 +1,16 @@
 """LRU residency simulator: waves, page-in plans, slot remap.
 
-Follows "Paged Experts" (SGLang docs), "How It Works":
-  * "The K-slot table and the host store": per layer, K slots on the GPU, all
-    E experts in the host store;
-  * "A step: waves, page-in, merge", steps 1-3: the step's distinct experts are
-    split into waves of at most K with the resident experts first; each wave
-    makes its experts resident by evicting the least recently used experts
-    outside the wave and copies the missing ones into their slots; routed ids
-    are remapped to slots;
-  * "Captured decode": decode with tokens*top_k <= K is one wave whose plan is
-    (experts, slots, count); both decode and prefill share one LRU state.
+Follows "Paged Experts" (SGLang docs), "The K-slot table and the host
+store", "A step: waves, page-in, merge" (items 1-3) and "Captured decode".
+Per layer there are K GPU slots and a host copy of all E experts.  A step
+takes the set of distinct experts its tokens routed to, puts the ones already
+in a slot first, and cuts that order into waves of at most K.  Before a wave
+runs, every expert of the wave must hold a slot: a missing one takes the slot
+of the least recently used expert that is not in the wave, and its weights
+are copied in.  Each routed id is then replaced by the slot of its expert.  A
+decode step whose entries fit in K slots is a single wave, described by the
+list of (expert, slot) copies and their count; decode and prefill steps
+update the same residency state.
 
 Readings where the pages are silent (all fixed here, and the CUDA planner
 must reproduce them bit for bit):

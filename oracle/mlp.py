@@ -1,16 +1,17 @@
 """Expert MLP, merged buffer, top-k sum and the whole paged layer step.
 
-"Paged Experts" (SGLang docs), "A step: waves, page-in, merge", steps 3-4: the
-MoE kernel runs over the wave's own entries without its final top-k sum and
-returns every routed (token, expert) output already multiplied by its router
-weight; each entry is written into one merged buffer by the one wave holding
-its expert, and the merged entries go through the same top-k sum, so the
-result does not depend on how experts were split into waves.  The paged layer
-therefore equals the plain (unpaged) MoE layer ("Why Paged Experts?",
-"Correctness").
+Follows "Paged Experts" (SGLang docs), "A step: waves, page-in, merge",
+items 3-4, and "Correctness".  Each routed (token, expert) pair yields one
+entry: the expert's gated MLP applied to the token, scaled by that pair's
+router weight, with no summation over the token's experts at that point.
+Whichever wave holds the expert fills the entry, once, in a single buffer
+shared by all waves; each token's k entries are added afterwards.  Since no
+entry depends on the wave that produced it, splitting the experts into waves
+cannot change the result, and the paged layer equals the plain MoE layer
+("Why Paged Experts?", "Correctness").
 
 Readings where the pages are silent:
-  * the expert MLP is the SiLU-gated one the spec names:
+  * the expert MLP is the SiLU-gated one the workload description names:
     h = SiLU(x Wg^T) * (x Wu^T), y = h Wd^T, with SiLU(z) = z / (1 + e^-z);
   * the gate and up projections are stacked in one [2I, H] tensor "w13":
     rows 0..I-1 are the gate, rows I..2I-1 the up projection; "w2" is the

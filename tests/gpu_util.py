@@ -62,6 +62,28 @@ def rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
+def token_rel_l2(got: np.ndarray, ref: np.ndarray) -> np.ndarray:
+    """rel-L2 of every token (row) of a [T, H] output on its own."""
+    num = np.linalg.norm(got - ref, axis=-1)
+    den = np.maximum(np.linalg.norm(ref, axis=-1), 1e-300)
+    return num / den
+
+
+def max_token_rel_l2(got: np.ndarray, ref: np.ndarray) -> float:
+    """The worst token's rel-L2: a wrong entry in one token of a long chunk
+    shows here, where the whole output's norm would dilute it."""
+    return float(token_rel_l2(got.reshape(-1, got.shape[-1]), ref.reshape(-1, ref.shape[-1])).max())
+
+
+def check_tokens(got: np.ndarray, want: np.ndarray, tol: float, what) -> float:
+    """Every token of an output within ``tol`` (rel-L2 of that token alone)
+    of the oracle; prints and returns the worst token's figure."""
+    worst = max_token_rel_l2(got, want)
+    print(f"{what}: worst token rel-L2 {worst:.3e} (whole output {rel_l2(got, want):.3e})")
+    assert worst <= tol, (what, worst)
+    return worst
+
+
 def check_plan(gpu: dict, plan, ids: np.ndarray, w: np.ndarray):
     """Bit-exact plan parity between the device planner and the oracle LRU."""
     assert np.array_equal(gpu["topk_id"], ids), "routed ids differ"

@@ -6,7 +6,9 @@ times it (one CUDA graph per token over the 48 layers).
   routed ids) is bit-exact against the oracle's LRU simulator;
 * the output of every layer-step equals the same call on a K = E handle bit
   for bit;
-* sampled layer-steps match the oracle's plain MoE layer within rel-L2 1e-2.
+* sampled layer-steps (every layer of one decode token; four layers of each
+  prefill chunk) match the oracle's plain MoE layer token by token: each
+  token's rel-L2 is within 1e-2.
 Covers the K=32 batch-1 decode workload and the K=64 graph-captured decode at
 batch 1, 2, 4 and 8 (= K // top_k) with one router-bias stream per request.
 """
@@ -102,12 +104,15 @@ def test_stack48_decode(stack48, K, B):
         gu.check_residency(model.read_residency(l), sims[l])
     st = model.stats(-1)
     assert st["error_word"] == 0 and st["steps"] == STEPS * L
-    # sampled values against the plain MoE layer
-    for t, l in [(0, 0), (0, L - 1), (STEPS - 1, 0), (STEPS - 1, L // 2), (STEPS // 2, 7)]:
-        get = gu.expert_fn(w, l)
-        want = omlp.unpaged_layer(hs[t, l], lg[t, l], k, get)
+    # sampled values against the plain MoE layer, token by token: every layer
+    # of one token, and the first and last layer-steps
+    samples = [(STEPS // 2, l) for l in range(L)] + [(0, 0), (STEPS - 1, L - 1)]
+    worst = 0.0
+    for t, l in samples:
+        want = omlp.unpaged_layer(hs[t, l], lg[t, l], k, gu.expert_fn(w, l))
         have = synth.bf16_bits_to_f32(got[t, l]).astype(np.float64)
-        assert gu.rel_l2(have, want) <= gu.REL_L2["bf16"], (t, l)
+        worst = max(worst, gu.check_tokens(have, want, gu.REL_L2["bf16"], (K, B, t, l)))
+    print(f"K={K} B={B}: worst token rel-L2 over {len(samples)} layer-steps {worst:.3e}")
     model.close()
 
 
@@ -115,8 +120,8 @@ def test_stack48_decode(stack48, K, B):
 def test_stack48_prefill(stack48, T):
     """One prefill chunk through all 48 layers at K=32: routing covers about
     100-128 experts per layer, so each layer-step runs 4 waves through the
-    pipelined prefill step; plans bit-exact, paged == K=E bit for bit, sampled values
-    within 1e-2 of the plain MoE layer."""
+    pipelined prefill step; plans bit-exact, paged == K=E bit for bit, every
+    token of four layers within 1e-2 of the plain MoE layer."""
     from host_paged_expert_gb300 import _lib
 
     s, w, owner = stack48
@@ -138,9 +143,9 @@ def test_stack48_prefill(stack48, T):
         gu.check_plan(model.read_plan(l, T), plan, ids, wts)
         got = gu.out_bits(ya)
         assert np.array_equal(got, gu.out_bits(yb)), l
-        if l in (0, L - 1):
+        if l in (0, 1, L // 2, L - 1):  # every token of four layers against the plain MoE layer
             want = omlp.unpaged_layer(hs[l], lg[l], k, gu.expert_fn(w, l))
-            assert gu.rel_l2(synth.bf16_bits_to_f32(got).astype(np.float64), want) <= gu.REL_L2["bf16"], l
+            gu.check_tokens(synth.bf16_bits_to_f32(got).astype(np.float64), want, gu.REL_L2["bf16"], (T, l))
     assert min(waves) >= 3
     prof = model.profile_read()
     assert prof["prefill_step"]["launches"] == L and prof["pagein"]["launches"] == 0

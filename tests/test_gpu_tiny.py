@@ -63,7 +63,7 @@ def test_tiny_decode_then_prefill(tiny):
         gu.check_residency(paged.read_residency(0), o_paged.sim)
         gu.check_residency(unpaged.read_residency(0), o_unpaged.sim)
         assert np.array_equal(gu.out_bits(y), gu.out_bits(y_ref)), f"paged != unpaged at step {step}"
-        err = gu.rel_l2(gu.out_f64(y), out)
+        err = gu.max_token_rel_l2(gu.out_f64(y), out)
         assert err <= gu.REL_L2["bf16"], (step, err)
         # every resident slot holds its expert's host row byte for byte
         res = paged.read_residency(0)
@@ -121,7 +121,7 @@ def test_multi_token_shapes(tiny, T):
         out, _, plan, ids, wts = o.step(xb, lg)
         gu.check_plan(a.read_plan(0, T), plan, ids, wts)
         assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb))
-        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
+        assert gu.max_token_rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
     a.close()
     b.close()
 
@@ -197,7 +197,7 @@ def test_scale_rows_are_paged_with_weights():
     ref = omlp.unpaged_layer(xb, lg, 2, lambda e: omlp.expert_weights(
         {"w13": row["w13"], "w2": w2} if e == 6 else w.row(0, e), "bf16"))
     got = synth.bf16_bits_to_f32(y1).astype(np.float64)
-    assert gu.rel_l2(got, ref) <= 1e-2
+    assert gu.max_token_rel_l2(got, ref) <= 1e-2
     m.close()
 
 
@@ -272,7 +272,7 @@ def test_graph_captured_prefill_matches_eager(tiny):
         out, _, plan, ids, wts = o.step(xb, lb)
         assert len(plan.waves) >= 2
         gu.check_plan(graphed.read_plan(0, T), plan, ids, wts)
-        assert gu.rel_l2(gu.out_f64(ye), out) <= gu.REL_L2["bf16"], c
+        assert gu.max_token_rel_l2(gu.out_f64(ye), out) <= gu.REL_L2["bf16"], c
     assert graphed.stats(0)["page_ins"] == eager.stats(0)["page_ins"]
     assert graphed.stats(0)["error_word"] == 0
     eager.close()
@@ -299,7 +299,7 @@ def test_odd_slot_and_entry_counts(E, k, K):
         out, _, plan, ids, wts = o.step(xb, lg)
         gu.check_plan(a.read_plan(0, T), plan, ids, wts)
         assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb))
-        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
+        assert gu.max_token_rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"]
     b.close()
     a.close()
 
@@ -326,6 +326,49 @@ def test_prefill_runs_on_the_tensor_core_path(tiny):
     m.close()
 
 
+def test_prefill_fallback_path_for_untiled_shapes():
+    """A prefill-sized step (T*top_k > 64) whose shapes do not tile for the
+    tensor cores (H = 136 is not a multiple of 128, I = 72 not of 64) runs the
+    plain path: per wave a page-in kernel, the weight-streaming gate/up and
+    down kernels, then the top-k sum.  Plans bit-exact against the oracle,
+    paged equal to K = E bit for bit, every token within 1e-2 of the oracle,
+    over consecutive chunks so later waves evict earlier ones."""
+    _lib = _need_gpu()
+    s = synth.MoEShape(1, 16, 2, 5, 136, 72, "bf16")
+    w = synth.ExpertWeights(s, seed=41)
+    T = 48
+    a = _lib.PagedMoE(s, max_tokens=T)
+    gu.load_stack(a, w)
+    b = _lib.PagedMoE(s.with_slots(s.num_experts), max_tokens=T, store_owner=a)
+    o = omlp.PagedLayer(s.num_experts, s.num_slots, s.top_k, gu.expert_fn(w, 0))
+    a.profile_enable(True)
+    waves = []
+    for c in range(3):
+        xb = synth.hidden_states((T,), s.hidden, seed=42, tag=c)
+        lg = synth.prefill_logits(1, s.num_experts, T, seed=43 + c)[0]
+        x, l = gu.to_dev_bf16(xb), gu.to_dev_f32(lg)
+        ya, yb = a.forward(0, x, l), b.forward(0, x, l)
+        out, _, plan, ids, wts = o.step(xb, lg)
+        waves.append(len(plan.waves))
+        gu.check_plan(a.read_plan(0, T), plan, ids, wts)
+        gu.check_residency(a.read_residency(0), o.sim)
+        assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), c
+        gu.check_tokens(gu.out_f64(ya), out, gu.REL_L2["bf16"], ("fallback", c))
+        res = a.read_residency(0)
+        for slot, e in enumerate(res["slot_expert"].tolist()):
+            if e >= 0:
+                got = a.read_slot(0, slot, a.layout["payload_bytes"])
+                assert np.array_equal(got, a.host_row(0, e)[: a.layout["payload_bytes"]]), (c, slot, e)
+    prof = a.profile_read()
+    assert min(waves) >= 3
+    assert prof["prefill_step"]["launches"] == 0 and prof["decode_step"]["launches"] == 0
+    assert prof["pagein"]["launches"] >= 3 * min(waves) and prof["gateup"]["launches"] == prof["pagein"]["launches"]
+    assert prof["topk_sum"]["launches"] == 3
+    assert a.stats(0)["error_word"] == 0
+    b.close()
+    a.close()
+
+
 def test_prefill_tiles_over_128_rows():
     """Experts with more than 128 routed rows fill both 128-row halves of a
     tensor-core tile (and, past 256 rows, several tiles); results match the
@@ -347,7 +390,7 @@ def test_prefill_tiles_over_128_rows():
         out, _, plan, ids, wts = o.step(xb, lg)
         gu.check_plan(a.read_plan(0, T), plan, ids, wts)
         assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), T
-        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"], T
+        assert gu.max_token_rel_l2(gu.out_f64(ya), out) <= gu.REL_L2["bf16"], T
     b.close()
     a.close()
 
@@ -378,7 +421,7 @@ def test_consecutive_multiwave_prefills_keep_slots_exact(dtype):
         gu.check_plan(a.read_plan(0, T), plan, ids, wts)
         gu.check_residency(a.read_residency(0), o.sim)
         assert np.array_equal(gu.out_bits(ya), gu.out_bits(yb)), (dtype, i)
-        assert gu.rel_l2(gu.out_f64(ya), out) <= gu.REL_L2[dtype], (dtype, i)
+        assert gu.max_token_rel_l2(gu.out_f64(ya), out) <= gu.REL_L2[dtype], (dtype, i)
         for slot, e in enumerate(a.read_residency(0)["slot_expert"].tolist()):
             if e >= 0:
                 got = a.read_slot(0, slot, a.layout["payload_bytes"])
