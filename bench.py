@@ -52,7 +52,19 @@ def log(msg: str) -> None:
 HBM_NOMINAL_GBS = 7900.0
 
 
+RESIDENT = "_resident"
+
+
 def workload(name: str):
+    """(shape, batch or chunk tokens, description) of a named workload.  A
+    prefill workload with the suffix "_resident" runs with K = E after a
+    warm-up that leaves every expert resident: no page-in, the expert GEMMs
+    alone."""
+    if name.endswith(RESIDENT) and "prefill48_T" in name:
+        shape, t, desc = workload(name[: -len(RESIDENT)])
+        return (shape.with_slots(shape.num_experts), t,
+                desc.split(", K=")[0] + f", K=E={shape.num_experts} (every expert resident after warm-up), "
+                + desc.split(", K=")[1].split(", ", 1)[1])
     base = synth.STACK48
     if name == "decode48":
         return base.with_slots(32), 1, "48 layers, H=2048, I=768, E=128, top-8, K=32, bf16 experts, batch 1"
@@ -71,6 +83,14 @@ def workload(name: str):
     if name.startswith("int4prefill48_T"):
         t = int(name[len("int4prefill48_T"):])
         return synth.STACK48_INT4, t, f"48 layers, H=2048, I=768, E=128, top-8, K=92, GPTQ int4 (group 128), prefill chunks of {t} tokens"
+    for fmt, shape4, label in (("mxfp4", synth.STACK48_MXFP4, "MXFP4 (E8M0 per 32)"),
+                               ("nvfp4", synth.STACK48_NVFP4, "NVFP4 (E4M3 per 16, fp32 per tensor)")):
+        if name.startswith(f"{fmt}prefill48_T"):
+            t = int(name[len(f"{fmt}prefill48_T"):])
+            return shape4, t, f"48 layers, H=2048, I=768, E=128, top-8, K=92, {label}, prefill chunks of {t} tokens"
+        if name.startswith(f"{fmt}_48_b"):
+            b = int(name[len(f"{fmt}_48_b"):])
+            return shape4, b, f"48 layers, H=2048, I=768, E=128, top-8, K=92, {label}, batch {b}"
     if name.startswith("fp8_48_b"):
         b = int(name[len("fp8_48_b"):])
         return synth.STACK48_FP8, b, f"48 layers, H=2048, I=768, E=128, top-8, K=40, block-FP8, batch {b}"
@@ -189,8 +209,9 @@ def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]), "src": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "src": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
 # The sources each timed kernel is compiled from: a DRAM-traffic record is
@@ -270,10 +291,27 @@ def run_ours(args, rep):
     t0 = time.time()
     weights = synth.ExpertWeights(shape, seed=0)
     log("weights pool ready")
-    model = _lib.PagedMoE(shape, max_tokens=B, device=dev)
-    log(f"handle created: arena {model.arena.numel() / 1e9:.2f} GB, host store "
-        f"{shape.num_layers * shape.num_experts * model.layout['row_stride'] / 1e9:.2f} GB pinned")
-    load_weights(model, weights)
+    store = None
+    if world > 1:
+        # one host store for all replicas on the host: replica 0 fills a
+        # shared mapping, every replica registers the same pages
+        from host_paged_expert_gb300 import shared_store
+
+        made = {}
+
+        def fill(st):
+            made["model"] = _lib.PagedMoE(shape, max_tokens=B, device=dev, host_store=st, filled=False)
+            load_weights(made["model"], weights)
+
+        path = shared_store.default_path(f"{os.environ.get('MASTER_PORT', '0')}_{args.workload}")
+        store = shared_store.open_for_replicas(rep, path, _lib.host_store_bytes(shape), fill)
+        model = made.get("model") or _lib.PagedMoE(shape, max_tokens=B, device=dev, host_store=store, filled=True)
+        log(f"handle created on the shared host store {path} ({store.nbytes / 1e9:.2f} GB, one copy per host)")
+    else:
+        model = _lib.PagedMoE(shape, max_tokens=B, device=dev)
+        log(f"handle created: arena {model.arena.numel() / 1e9:.2f} GB, host store "
+            f"{shape.num_layers * shape.num_experts * model.layout['row_stride'] / 1e9:.2f} GB pinned")
+        load_weights(model, weights)
     t_load = time.time() - t0
     log("experts loaded into the host store")
     payload = model.layout["payload_bytes"]
@@ -428,8 +466,12 @@ def run_ours(args, rep):
     out = {"tok_s": tok_s, "ms": ms, "spread": spread, "clocks": clocks, "d": d, "e2e": e2e, "trace": trace,
            "link": {"copy_engine_gbs": round(ce_gbs, 1), "kernel_gbs": round(kn_gbs, 1)},
            "t_load": t_load, "shape": shape, "B": B, "desc": desc, "payload": payload,
-           "layout": model.layout, "lg_h": lg_h, "hs_h": hs_h, "weights": weights}
+           "layout": model.layout, "lg_h": lg_h, "hs_h": hs_h, "weights": weights,
+           "host_store": "shared by all replicas on the host" if store is not None else "pinned by this process"}
     model.close()
+    if store is not None:
+        replicas.barrier(rep)  # every replica is done with the mapping
+        store.close()
     return out
 
 
@@ -562,7 +604,44 @@ def run_prefill(args):
                                "definition": "sum over layer-steps of max(distinct*expert_bytes/HBM, page_ins*expert_bytes/link) "
                                              "divided by the summed kernel time of the trace pass"},
             "kernels": kernels}
-    if "prefill_step" in kernels:  # the dominant kernel: page-ins over the link with the GEMMs underneath
+    resident = args.workload.endswith(RESIDENT)
+    if resident and "prefill_step" in kernels:
+        # every expert resident: the step is the expert GEMMs alone, bound by
+        # the tensor pipe or, below the ridge, by streaming the weights once
+        kd = kernels["prefill_step"]
+        if d["page_ins"]:
+            log(f"warning: {d['page_ins']} page-ins in the timed region of a resident workload")
+        sec = prof["prefill_step"]["total_ms"] * 1e-3
+        wbytes = d["distinct"] * payload  # each routed expert's weights read once per layer-step
+        tf = flops / sec / 1e12
+        hbm = wbytes / sec / 1e9
+        ai = flops / wbytes
+        ridge = peaks["bf16_tflops_sustained"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+        ceiling = min(1.0, ai / ridge)
+        tensor = {"achieved": round(tf, 1), "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                  "frac": round(tf / peaks["bf16_tflops_sustained"], 4),
+                  "peak_src": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peaks['src']})",
+                  "flops_per_launch": round(flops / kd["launches"])}
+        hbm_o = {"achieved": round(hbm, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                 "frac": round(hbm / peaks["hbm_gbs"], 4), "bytes_per_launch": round(wbytes / kd["launches"])}
+        bound = "tensor" if ceiling >= 1.0 else "hbm"
+        main = tensor if bound == "tensor" else hbm_o
+        line["roofline"] = {"kernel": "prefill_step", "bound": bound, "achieved": main["achieved"],
+                            "peak": main["peak"], "unit": main["unit"], "frac": main["frac"],
+                            "traffic": ncu_traffic("prefill_step", args.workload),
+                            "tensor": tensor, "hbm": hbm_o,
+                            "arithmetic_intensity_flop_per_byte": round(ai, 1),
+                            "ridge_flop_per_byte": round(ridge, 1),
+                            "tensor_ceiling_from_ai": round(ceiling, 4),
+                            "tensor_frac_of_ceiling": round(tensor["frac"] / ceiling, 4),
+                            "definition": "FLOP = 2*entries*H*2I + 2*entries*I*H over the prefill_step kernel's "
+                                          "CUDA-event time; bytes = distinct experts x expert bytes"}
+        line["metric"] = "paged-MoE prefill tok/s (48 layers, every expert resident)"
+        kd.update({"bound": bound, "gemm_tflops": round(tf, 1),
+                   "gemm_frac_of_bf16_sustained": tensor["frac"], "weight_gbs": round(hbm, 1)})
+        for k_ in ("achieved_gbs", "peak_gbs", "frac"):
+            kd.pop(k_, None)
+    elif "prefill_step" in kernels:  # the dominant kernel: page-ins over the link with the GEMMs underneath
         kd = kernels["prefill_step"]
         line["roofline"] = {"kernel": "prefill_step", "bound": "host_link", "achieved": kd["achieved_gbs"],
                             "peak": kd["peak_gbs"], "unit": "GB/s", "frac": kd["frac"],
@@ -731,7 +810,7 @@ def main():
     if world > 1:
         torch.cuda.set_device(local_rank)
         replicas.init(rep, "nccl", device=torch.device("cuda", local_rank))
-    if args.workload.startswith(("prefill48_T", "fp8prefill48_T", "int4prefill48_T")):
+    if "prefill48_T" in args.workload:
         if world > 1:
             raise SystemExit("prefill workloads time one replica; run them with --gpus 1")
         run_prefill(args)
@@ -751,6 +830,7 @@ def main():
         "data": "synthetic",
         "config": {"workload": f"{args.workload}: {r['desc']}", "global_batch": B * world,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "host_store": r["host_store"],
                    "graph": not args.no_graph,
                    "l2": "inputs larger than L2: each step streams ~%.1f GB of expert weights"
                          % (d["distinct"] / args.steps * r["payload"] / 1e9)},

@@ -20,12 +20,13 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libpe.so")
 
 PE_OK, PE_ERR_INVALID, PE_ERR_UNSUPPORTED_DTYPE, PE_ERR_HOST_ALLOC, PE_ERR_CUDA, PE_ERR_RANGE, PE_ERR_ARENA = range(7)
-PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ = 0, 1, 2
-_DTYPE = {"bf16": PE_BF16, "fp8": PE_FP8_BLOCK128, "int4": PE_INT4_GPTQ}
+PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4, PE_NVFP4 = 0, 1, 2, 3, 4
+_DTYPE = {"bf16": PE_BF16, "fp8": PE_FP8_BLOCK128, "int4": PE_INT4_GPTQ, "mxfp4": PE_MXFP4, "nvfp4": PE_NVFP4}
 PE_DEVERR_NAN_LOGIT, PE_DEVERR_NOT_LOADED, PE_DEVERR_PLAN = 1, 2, 4
 
 EXPORTS = [
     "pe_required_device_bytes", "pe_slots_for_budget", "pe_get_row_layout", "pe_max_waves", "pe_create",
+    "pe_create_external",
     "pe_create_shared",
     "pe_load_host_expert", "pe_host_row", "pe_forward", "pe_stats", "pe_read_plan", "pe_read_residency",
     "pe_read_slot", "pe_reset_residency", "pe_probe_host_link", "pe_profile_enable", "pe_profile_read",
@@ -84,6 +85,7 @@ def lib() -> ctypes.CDLL:
     L.pe_max_waves.restype = c_int32
     L.pe_create.argtypes = [cfgp, c_void_p, c_size_t, POINTER(c_void_p)]
     L.pe_create_shared.argtypes = [cfgp, c_void_p, c_size_t, c_void_p, POINTER(c_void_p)]
+    L.pe_create_external.argtypes = [cfgp, c_void_p, c_size_t, c_void_p, c_size_t, c_int32, POINTER(c_void_p)]
     L.pe_load_host_expert.argtypes = [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p]
     L.pe_host_row.argtypes = [c_void_p, c_int32, c_int32]
     L.pe_host_row.restype = c_void_p
@@ -142,6 +144,11 @@ def slots_for_budget(shape: MoEShape, max_tokens: int, budget_bytes: int) -> int
     return int(lib().pe_slots_for_budget(byref(cfg), c_size_t(budget_bytes)))
 
 
+def host_store_bytes(shape: MoEShape) -> int:
+    """Bytes of a host store for this shape: L * E * row_stride."""
+    return shape.num_layers * shape.num_experts * row_layout(shape)["row_stride"]
+
+
 def row_layout(shape: MoEShape) -> dict:
     cfg = make_config(shape, 1)
     r = PERowLayout()
@@ -173,7 +180,11 @@ def _stream_ptr(stream) -> int | None:
 class PagedMoE:
     """A stack of paged MoE layers on one GPU (wraps a libpe handle)."""
 
-    def __init__(self, shape: MoEShape, max_tokens: int, device: int = 0, store_owner: "PagedMoE | None" = None):
+    def __init__(self, shape: MoEShape, max_tokens: int, device: int = 0, store_owner: "PagedMoE | None" = None,
+                 host_store=None, filled: bool = False):
+        """``store_owner``: read that handle's host store.  ``host_store``: an
+        object with ``ptr`` and ``nbytes`` (e.g. a SharedHostStore) to use as
+        the host store; ``filled`` marks every expert in it loaded."""
         import torch
 
         self.shape = shape
@@ -186,7 +197,10 @@ class PagedMoE:
             raise PEError(PE_ERR_INVALID, "invalid configuration")
         self.arena = torch.empty(n, dtype=torch.uint8, device=f"cuda:{device}")
         h = c_void_p()
-        if store_owner is None:
+        if host_store is not None:
+            st = self._L.pe_create_external(byref(self.cfg), c_void_p(self.arena.data_ptr()), n,
+                                            c_void_p(host_store.ptr), host_store.nbytes, int(filled), byref(h))
+        elif store_owner is None:
             st = self._L.pe_create(byref(self.cfg), c_void_p(self.arena.data_ptr()), n, byref(h))
         else:
             st = self._L.pe_create_shared(byref(self.cfg), c_void_p(self.arena.data_ptr()), n,
@@ -194,7 +208,7 @@ class PagedMoE:
         if st != PE_OK:
             raise PEError(st, self._L.pe_last_error(None).decode())
         self.handle = h
-        self._owner = store_owner
+        self._owner = store_owner if store_owner is not None else host_store
         self.layout = row_layout(shape)
 
     # -- lifecycle
@@ -219,9 +233,23 @@ class PagedMoE:
         w2 = np.ascontiguousarray(row["w2"])
         s13 = row.get("s13")
         s2 = row.get("s2")
-        sdt = np.float16 if self.shape.dtype == "int4" else np.float32
-        s13 = None if s13 is None else np.ascontiguousarray(s13, dtype=sdt)
-        s2 = None if s2 is None else np.ascontiguousarray(s2, dtype=sdt)
+        dt = self.shape.dtype
+        if dt in ("mxfp4", "nvfp4"):
+            # byte grids; NVFP4 puts the tensor's fp32 scale in a 16-byte header first
+            def grid(sc, g):
+                sc = np.ascontiguousarray(sc, dtype=np.uint8).reshape(-1)
+                if dt == "mxfp4":
+                    return sc
+                hdr = np.zeros(16, np.uint8)
+                hdr[:4] = np.array([g], dtype=np.float32).view(np.uint8)
+                return np.concatenate([hdr, sc])
+
+            s13 = grid(s13, row.get("g13"))
+            s2 = grid(s2, row.get("g2"))
+        else:
+            sdt = np.float16 if dt == "int4" else np.float32
+            s13 = None if s13 is None else np.ascontiguousarray(s13, dtype=sdt)
+            s2 = None if s2 is None else np.ascontiguousarray(s2, dtype=sdt)
         self._check(self._L.pe_load_host_expert(
             self.handle, layer, expert, w13.ctypes.data, w2.ctypes.data,
             None if s13 is None else s13.ctypes.data, None if s2 is None else s2.ctypes.data))

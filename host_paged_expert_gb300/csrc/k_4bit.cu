@@ -1,18 +1,21 @@
-// GPTQ int4 expert MLP for decode sizes ("Paged Experts", SGLang docs,
-// "Supported Configurations and Limitations": GPTQ int4 experts).  Weights are
-// 4-bit codes with the zero point 8 and one fp16 scale per output row and
-// group of 128 inputs: W[n, k] = (q[n, k] - 8) * s[n][k / 128].  Activations
-// stay bf16 and accumulation is fp32.
+// 4-bit expert MLP for decode sizes: GPTQ int4 ("Paged Experts", SGLang docs,
+// "Supported Configurations and Limitations") and MXFP4 / NVFP4 ("SGLang
+// Paged Experts: corré MoE más grandes que tu VRAM", "¿Qué es la paginación
+// de expertos…?").  GPTQ int4: W[n, k] = (q[n, k] - 8) * s[n][k / 128] with
+// fp16 scales; MXFP4: W = e2m1(q) * 2^(e - 127) per 32 inputs; NVFP4:
+// W = e2m1(q) * e4m3(s) * g per 16 inputs.  Activations stay bf16 and
+// accumulation is fp32.
 //
 // The kernels mirror the block-FP8 ones: gate/up with the page-in fused in,
 // the same on resident slots only, and the down projection with the top-k
-// sum.  All arithmetic is in int4_device.cuh, shared with the one-kernel
-// decode step.  Scales are read from the same place as the codes (host row
-// for a page-in, slot for a hit), so a slot never pairs one expert's codes
-// with another's scales.
+// sum.  All arithmetic is in int4_device.cuh and fp4_device.cuh (Q4Ops),
+// shared with the one-kernel decode step.  Scales are read from the same
+// place as the codes (host row for a page-in, slot for a hit), so a slot
+// never pairs one expert's codes with another's scales.
 
 #include <cuda_fp16.h>
 
+#include "fp4_device.cuh"
 #include "int4_device.cuh"
 #include "pe_device.cuh"
 #include "pe_internal.h"
@@ -30,8 +33,8 @@ constexpr int kSmemBudget4 = 48 * 1024;
 // Gate/up of one wave fused with its page-in; same work split as the bf16
 // kernel (link CTAs: page-in rows used for h, then the rest of each paged row;
 // HBM CTAs: resident members' rows).
-template <int CPL>
-__global__ void __launch_bounds__(kThreads4, 2) gateup_pagein_int4_kernel(
+template <int FMT, int CPL>
+__global__ void __launch_bounds__(kThreads4, 2) gateup_pagein_q4_kernel(
     LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ host,
     uint8_t* __restrict__ slots, int wave, int T, float* __restrict__ hbuf, int stage_x) {
     extern __shared__ int4 sh_dyn4[];
@@ -99,8 +102,8 @@ __global__ void __launch_bounds__(kThreads4, 2) gateup_pagein_int4_kernel(
         uint8_t* slot_base = slots + (size_t)slot * s.stride;
         const uint8_t* base = link_cta ? host + (size_t)sh_mexp[q] * s.stride : slot_base;
         int4 gv[CPL], uv[CPL];
-        float sg[CPL], su[CPL];
-        load_row_pair_int4<CPL>(base, s, n, lane, nchunk, link_cta, false, gv, uv, sg, su);
+        typename Q4Ops<FMT>::Scale sg[CPL], su[CPL];
+        Q4Ops<FMT>::template load<CPL>(base, s, n, lane, nchunk, link_cta, false, gv, uv, sg, su);
         if (link_cta) {
             uint8_t* gd = slot_base + s.w13_off + (size_t)n * (s.H / 2);
             uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
@@ -119,7 +122,8 @@ __global__ void __launch_bounds__(kThreads4, 2) gateup_pagein_int4_kernel(
             while (mask) {
                 const int ei = b0 + __ffs(mask) - 1;
                 mask &= mask - 1;
-                const float h = row_pair_h_int4<CPL>(gv, uv, sg, su, xbase + (size_t)(ei / s.k) * xrow, lane, nchunk);
+                const float h =
+                    Q4Ops<FMT>::template h<CPL>(gv, uv, sg, su, xbase + (size_t)(ei / s.k) * xrow, lane, nchunk);
                 if (lane == 0) hbuf[(size_t)ei * s.I + n] = h;
             }
         }
@@ -128,8 +132,8 @@ __global__ void __launch_bounds__(kThreads4, 2) gateup_pagein_int4_kernel(
 
 // Gate/up of one wave from the slots only (after a separate page-in): one
 // warp per (entry, row).
-template <int CPL>
-__global__ void __launch_bounds__(kThreads4) gateup_int4_kernel(LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x,
+template <int FMT, int CPL>
+__global__ void __launch_bounds__(kThreads4) gateup_q4_kernel(LayerDev L, Shape s, const __nv_bfloat16* __restrict__ x,
                                                               const uint8_t* __restrict__ slots, int wave, int T,
                                                               float* __restrict__ hbuf) {
     pdl_wait();
@@ -144,18 +148,18 @@ __global__ void __launch_bounds__(kThreads4) gateup_int4_kernel(LayerDev L, Shap
         if (L.entry_wave[i] != wave) continue;
         const uint8_t* base = slots + (size_t)L.entry_slot[i] * s.stride;
         int4 gv[CPL], uv[CPL];
-        float sg[CPL], su[CPL];
-        load_row_pair_int4<CPL>(base, s, n, lane, nchunk, false, false, gv, uv, sg, su);
+        typename Q4Ops<FMT>::Scale sg[CPL], su[CPL];
+        Q4Ops<FMT>::template load<CPL>(base, s, n, lane, nchunk, false, false, gv, uv, sg, su);
         const uint8_t* xr = reinterpret_cast<const uint8_t*>(x + (size_t)(i / s.k) * s.H);
-        const float h = row_pair_h_int4<CPL>(gv, uv, sg, su, xr, lane, nchunk);
+        const float h = Q4Ops<FMT>::template h<CPL>(gv, uv, sg, su, xr, lane, nchunk);
         if (lane == 0) hbuf[(size_t)i * s.I + n] = h;
     }
 }
 
 // Down projection of one wave (same structure as the bf16 kernel): a CTA owns
 // token t and kDownRows4 rows, warp w the entries j = w, w + 8, ...
-template <int CPL>
-__global__ void __launch_bounds__(kThreads4) down_int4_kernel(LayerDev L, Shape s, const uint8_t* __restrict__ slots,
+template <int FMT, int CPL>
+__global__ void __launch_bounds__(kThreads4) down_q4_kernel(LayerDev L, Shape s, const uint8_t* __restrict__ slots,
                                                              int wave, int T, const float* __restrict__ hbuf,
                                                              float* __restrict__ merged, __nv_bfloat16* __restrict__ out,
                                                              int fused) {
@@ -175,9 +179,8 @@ __global__ void __launch_bounds__(kThreads4) down_int4_kernel(LayerDev L, Shape 
         }
         const uint8_t* base = slots + (size_t)L.entry_slot[i] * s.stride;
         float p[kDownRows4];
-        down_rows_int4<CPL, kDownRows4>(base + s.w2_off, reinterpret_cast<const __half*>(base + s.s2_off),
-                                        hbuf + (size_t)i * s.I, L.topk_w[i], m0, s.H, s.I, false,
-                                        fused ? nullptr : merged + (size_t)i * s.H, p, lane);
+        Q4Ops<FMT>::template down<CPL, kDownRows4>(base, s, hbuf + (size_t)i * s.I, L.topk_w[i], m0, false,
+                                                   fused ? nullptr : merged + (size_t)i * s.H, p, lane);
         if (fused && lane == 0) {
 #pragma unroll
             for (int r = 0; r < kDownRows4; ++r) sh_p[j][r] = p[r];
@@ -193,18 +196,17 @@ __global__ void __launch_bounds__(kThreads4) down_int4_kernel(LayerDev L, Shape 
     }
 }
 
-}  // namespace
 
-cudaError_t launch_gateup_pagein_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
-                                     const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T, float* hbuf,
-                                     int num_sms, cudaStream_t st) {
+template <int FMT>
+cudaError_t gateup_pagein_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* host_layer,
+                             uint8_t* slots_layer, int wave, int T, float* hbuf, int num_sms, cudaStream_t st) {
     const int grid = num_sms * 2;
     const int cpl = (s.H / 32 + 31) / 32;
     const size_t xbytes = (size_t)T * s.H * 2;
     const size_t meta = (size_t)4 * ((2 * s.K + T * s.k + 3) & ~3);
     const int stage = meta + xbytes <= (size_t)kSmemBudget4;
     const size_t smem = meta + (stage ? xbytes : 0);
-#define PE_G4(C) return launch_pdl(gateup_pagein_int4_kernel<C>, grid, kThreads4, smem, st, L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)
+#define PE_G4(C) return launch_pdl(gateup_pagein_q4_kernel<FMT, C>, grid, kThreads4, smem, st, L, s, x, host_layer, slots_layer, wave, T, hbuf, stage)
     if (cpl <= 1) PE_G4(1);
     if (cpl <= 2) PE_G4(2);
     if (cpl <= 4) PE_G4(4);
@@ -213,14 +215,15 @@ cudaError_t launch_gateup_pagein_int4(const LayerDev& L, const Shape& s, const _
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_gateup_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* slots_layer,
-                              int wave, int T, float* hbuf, int num_sms, cudaStream_t st) {
+template <int FMT>
+cudaError_t gateup_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* slots_layer, int wave,
+                      int T, float* hbuf, int num_sms, cudaStream_t st) {
     const long long warps = (long long)T * s.k * s.I;
     const long long blocks = (warps + kWarps4 - 1) / kWarps4;
     const int grid = (int)(blocks < (long long)num_sms * 4 ? blocks : (long long)num_sms * 4);
     if (grid <= 0) return cudaSuccess;
     const int cpl = (s.H / 32 + 31) / 32;
-#define PE_U4(C) return launch_pdl(gateup_int4_kernel<C>, grid, kThreads4, 0, st, L, s, x, slots_layer, wave, T, hbuf)
+#define PE_U4(C) return launch_pdl(gateup_q4_kernel<FMT, C>, grid, kThreads4, 0, st, L, s, x, slots_layer, wave, T, hbuf)
     if (cpl <= 1) PE_U4(1);
     if (cpl <= 2) PE_U4(2);
     if (cpl <= 4) PE_U4(4);
@@ -229,20 +232,45 @@ cudaError_t launch_gateup_int4(const LayerDev& L, const Shape& s, const __nv_bfl
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_down_int4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave, int T,
-                            const float* hbuf, float* merged, __nv_bfloat16* out, int fused, int num_sms,
-                            cudaStream_t st) {
-    (void)num_sms;
+template <int FMT>
+cudaError_t down_q4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave, int T, const float* hbuf,
+                    float* merged, __nv_bfloat16* out, int fused, cudaStream_t st) {
     const long long blocks = (long long)T * ((s.H + kDownRows4 - 1) / kDownRows4);
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int cpl = (s.I / 32 + 31) / 32;
-#define PE_D4(C) return launch_pdl(down_int4_kernel<C>, (int)blocks, kThreads4, 0, st, L, s, slots_layer, wave, T, hbuf, merged, out, fused)
+#define PE_D4(C) return launch_pdl(down_q4_kernel<FMT, C>, (int)blocks, kThreads4, 0, st, L, s, slots_layer, wave, T, hbuf, merged, out, fused)
     if (cpl <= 1) PE_D4(1);
     if (cpl <= 2) PE_D4(2);
     if (cpl <= 4) PE_D4(4);
 #undef PE_D4
     return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_gateup_pagein_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                    const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T, float* hbuf,
+                                    int num_sms, cudaStream_t st) {
+    if (s.dtype == PE_MXFP4) return gateup_pagein_q4<PE_MXFP4>(L, s, x, host_layer, slots_layer, wave, T, hbuf, num_sms, st);
+    if (s.dtype == PE_NVFP4) return gateup_pagein_q4<PE_NVFP4>(L, s, x, host_layer, slots_layer, wave, T, hbuf, num_sms, st);
+    return gateup_pagein_q4<PE_INT4_GPTQ>(L, s, x, host_layer, slots_layer, wave, T, hbuf, num_sms, st);
+}
+
+cudaError_t launch_gateup_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x, const uint8_t* slots_layer,
+                             int wave, int T, float* hbuf, int num_sms, cudaStream_t st) {
+    if (s.dtype == PE_MXFP4) return gateup_q4<PE_MXFP4>(L, s, x, slots_layer, wave, T, hbuf, num_sms, st);
+    if (s.dtype == PE_NVFP4) return gateup_q4<PE_NVFP4>(L, s, x, slots_layer, wave, T, hbuf, num_sms, st);
+    return gateup_q4<PE_INT4_GPTQ>(L, s, x, slots_layer, wave, T, hbuf, num_sms, st);
+}
+
+cudaError_t launch_down_q4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave, int T,
+                           const float* hbuf, float* merged, __nv_bfloat16* out, int fused, int num_sms,
+                           cudaStream_t st) {
+    (void)num_sms;
+    if (s.dtype == PE_MXFP4) return down_q4<PE_MXFP4>(L, s, slots_layer, wave, T, hbuf, merged, out, fused, st);
+    if (s.dtype == PE_NVFP4) return down_q4<PE_NVFP4>(L, s, slots_layer, wave, T, hbuf, merged, out, fused, st);
+    return down_q4<PE_INT4_GPTQ>(L, s, slots_layer, wave, T, hbuf, merged, out, fused, st);
 }
 
 }  // namespace pe

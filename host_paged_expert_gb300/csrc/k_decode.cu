@@ -32,6 +32,7 @@
 // warp sum for a down row, p = w * d, the sum over j = 0..k-1 from zero), so
 // the two paths give the same bits and the output still equals K = E.
 
+#include "fp4_device.cuh"
 #include "fp8_device.cuh"
 #include "int4_device.cuh"
 #include "pe_device.cuh"
@@ -197,7 +198,8 @@ constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
 // kRowsD4 rows to keep enough bytes in flight (a gate/up item stays one row
 // pair: two spill registers); the per-row arithmetic is unchanged.
 constexpr int kRowsG4 = 2, kRowsD4 = 8;
-// FMT: the expert format (PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ).
+// FMT: the expert format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4 or
+// PE_NVFP4; the three 4-bit formats share the int4 tiling).
 template <int EPL, int FMT>
 __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape s, const float* __restrict__ logits,
                                                                   const __nv_bfloat16* __restrict__ x,
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     if (threadIdx.x == kThr - 32) {  // a warp that routes no token of a small step: it waits for the atomic
         unsigned smid;
         asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
-        const unsigned link_every = FMT == PE_INT4_GPTQ && T > 1 ? kLinkSmEveryInt4Batch : kLinkSmEvery;
+        const unsigned link_every = is_4bit(FMT) && T > 1 ? kLinkSmEveryInt4Batch : kLinkSmEvery;
         sh_link_sm = (smid % link_every) == 0;
         sh_role_rank = (int)atomicAdd(&sync[sh_link_sm ? R_LINK : R_HBM], 1u);
     }
@@ -276,8 +278,8 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     const size_t row_bytes = (size_t)s.H * 2;
     // gate/up row pairs per resident-expert item (a page-in item takes one:
     // the link wants many warps with host reads in flight)
-    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;
-    constexpr int RD = FMT == PE_INT4_GPTQ ? kRowsD4 : kRowsD;  // down rows per item
+    constexpr int RPI = is_4bit(FMT) ? kRowsG4 : 1;
+    constexpr int RD = is_4bit(FMT) ? kRowsD4 : kRowsD;  // down rows per item
     const int ipe = s.I / RPI;  // gate/up items per resident expert
     const long long miss_rows = (long long)count * s.I;
     const size_t tail_bytes = s.copy_bytes - s.tail_off;
@@ -338,6 +340,46 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
                 const int n = as_link ? (int)(item % s.I) : (int)(item % ipe) * RPI;  // first row pair of the item
                 const int nr = as_link ? 1 : RPI;                                       // row pairs of the item
                 const int slot = sh_mslot[mq];
+                if constexpr (FMT == PE_MXFP4 || FMT == PE_NVFP4) {
+                    uint8_t* slot_base = slots + (size_t)slot * s.stride;
+                    const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
+                    const int nch4 = s.H >> 5;
+                    int4 gv[RPI][CPLH4], uv[RPI][CPLH4];
+                    float2 sg[RPI][CPLH4], su[RPI][CPLH4];
+#pragma unroll
+                    for (int r = 0; r < RPI; ++r)
+                        if (r < nr)
+                            load_row_pair_fp4<FMT, CPLH4>(rbase, s, n + r, lane, nch4, as_link, false, gv[r], uv[r],
+                                                          sg[r], su[r]);
+                    if (as_link) {
+                        uint8_t* gd = slot_base + s.w13_off + (size_t)n * (s.H / 2);
+                        uint8_t* ud = gd + (size_t)s.I * (s.H / 2);
+#pragma unroll
+                        for (int c = 0; c < CPLH4; ++c) {
+                            const int idx = lane + 32 * c;
+                            if (idx < nch4) {
+                                *reinterpret_cast<int4*>(gd + 16 * (size_t)idx) = gv[0][c];
+                                *reinterpret_cast<int4*>(ud + 16 * (size_t)idx) = uv[0][c];
+                            }
+                        }
+                    }
+                    for (int b0 = 0; b0 < nent; b0 += 32) {
+                        const int i = b0 + lane;
+                        unsigned mask = __ballot_sync(0xffffffffu, i < nent && sh_ekey[i] == slot);
+                        while (mask) {
+                            const int ei = b0 + __ffs(mask) - 1;
+                            mask &= mask - 1;
+                            const uint8_t* xr = xbase + (size_t)(ei / s.k) * s.H * 2;
+#pragma unroll
+                            for (int r = 0; r < RPI; ++r) {
+                                if (r >= nr) break;
+                                const float hval = row_pair_h_fp4<CPLH4>(gv[r], uv[r], sg[r], su[r], xr, lane, nch4);
+                                if (lane == 0) hbuf[(size_t)ei * s.I + n + r] = hval;
+                            }
+                        }
+                    }
+                    continue;
+                }
                 if constexpr (FMT == PE_INT4_GPTQ) {
                     uint8_t* slot_base = slots + (size_t)slot * s.stride;
                     const uint8_t* rbase = as_link ? host + (size_t)sh_mexp[mq] * s.stride : slot_base;
@@ -469,7 +511,10 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     auto down_entry = [&](int e, int m0) {
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
         const float we = sh_ew[e];
-        if constexpr (FMT == PE_INT4_GPTQ)
+        if constexpr (FMT == PE_MXFP4 || FMT == PE_NVFP4)
+            down_rows_fp4<FMT, CPLI4, RD>(sb + s.w2_off, sb + s.s2_off, hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true,
+                                          merged + (size_t)e * s.H, nullptr, lane);
+        else if constexpr (FMT == PE_INT4_GPTQ)
             down_rows_int4<CPLI4, RD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
                                           hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true, merged + (size_t)e * s.H,
                                           nullptr, lane);
@@ -555,7 +600,7 @@ int decode_fused_sync_words() { return S_NUM; }
 
 bool decode_fused_supported(const Shape& s, int T) {
     const bool dims = s.dtype == PE_FP8_BLOCK128 ? (s.H <= 32 * 16 * CPLH8 && s.I <= 32 * 16 * CPLI8)
-                      : s.dtype == PE_INT4_GPTQ ? (s.H <= 32 * 32 * CPLH4 && s.I <= 32 * 32 * CPLI4)
+                      : is_4bit(s.dtype) ? (s.H <= 32 * 32 * CPLH4 && s.I <= 32 * 32 * CPLI4)
                                                 : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
     return (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K && s.E <= kPlanCap &&
            s.K <= kPlanCap && dims && (size_t)4 * decode_meta_words(s) <= (size_t)kDynBudget;
@@ -566,7 +611,9 @@ cudaError_t decode_setup_kernels() {
 #define PE_ATTR(N)                                                                                                   \
     if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
     if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_FP8_BLOCK128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
-    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget); \
+    if (!e) e = cudaFuncSetAttribute(decode_step_kernel<N, PE_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kDynBudget);
     PE_ATTR(1) PE_ATTR(2) PE_ATTR(4) PE_ATTR(8)
 #undef PE_ATTR
     return e;
@@ -590,6 +637,10 @@ cudaError_t decode_ctas_per_sm(int dtype, int* out) {
         PE_OCC_F(PE_FP8_BLOCK128)
     } else if (dtype == PE_INT4_GPTQ) {
         PE_OCC_F(PE_INT4_GPTQ)
+    } else if (dtype == PE_MXFP4) {
+        PE_OCC_F(PE_MXFP4)
+    } else if (dtype == PE_NVFP4) {
+        PE_OCC_F(PE_NVFP4)
     } else {
         PE_OCC_F(PE_BF16)
     }
@@ -615,6 +666,8 @@ cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* 
 #define PE_DEC(N)                                                                                                   \
     return s.dtype == PE_FP8_BLOCK128 ? PE_DEC1(N, PE_FP8_BLOCK128)                                                 \
            : s.dtype == PE_INT4_GPTQ  ? PE_DEC1(N, PE_INT4_GPTQ)                                                    \
+           : s.dtype == PE_MXFP4      ? PE_DEC1(N, PE_MXFP4)                                                        \
+           : s.dtype == PE_NVFP4      ? PE_DEC1(N, PE_NVFP4)                                                        \
                                       : PE_DEC1(N, PE_BF16)
     if (epl <= 1) PE_DEC(1);
     if (epl <= 2) PE_DEC(2);

@@ -57,14 +57,16 @@
 // The weights come straight from the slot table (a 3-D tensor map over
 // [slot][row][k]).
 //
-// Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block) and GPTQ
+// Block-FP8 experts (E4M3 codes, one fp32 scale per 128x128 block), GPTQ
 // int4 experts (4-bit codes, zero point 8, one fp16 scale per output row and
-// 128 inputs) keep bf16 activations: TMA brings the code tile into a staging
-// buffer, ten converter warps decode it, multiply by its scale, round to bf16
-// and write it in the 128-byte-swizzled layout the MMA reads; the MMA then
-// runs as for bf16.  A tile's scales are staged in shared memory once per
-// tile (FP8: one row of blocks for each of its gate, up or down row ranges;
-// int4: every row's group scales).
+// 128 inputs) and MXFP4 / NVFP4 experts (E2M1 codes with E8M0 scales per 32
+// inputs, or E4M3 scales per 16 inputs and an fp32 tensor scale) keep bf16
+// activations: TMA brings the code tile into a staging buffer, ten converter
+// warps decode it, multiply by its scale, round to bf16 and write it in the
+// 128-byte-swizzled layout the MMA reads; the MMA then runs as for bf16.  A
+// tile's scales are staged in shared memory once per tile (FP8: one row of
+// blocks for each of its gate, up or down row ranges; the 4-bit formats:
+// every row's scales).
 //
 // Every row of an MMA tile is computed independently and always with the same
 // k order, so an entry's result does not depend on its tile-mates, its slot,
@@ -78,6 +80,7 @@
 
 #include <cuda_fp16.h>
 
+#include "fp4_device.cuh"
 #include "fp8_device.cuh"
 #include "int4_device.cuh"
 #include "pe_device.cuh"
@@ -101,15 +104,16 @@ constexpr int kLinkEvery = 4;         // the CTAs on SMs 0, 4, 8, ... stream the
 constexpr int kLinkUnroll = 8;
 constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 64 KiB per item
 constexpr int kMaxScaleCols = 64;     // FP8 / int4: K / 128 of either GEMM (H, I <= 8192)
+constexpr int kScaleStageBytes = BN * kMaxScaleCols * 2;  // a 4-bit tile's staged scales: 16 KiB
 constexpr uint32_t kSpin = 1u << 22;  // polls, >= 128 ns apart
 
-// Stage layout per weight format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ):
+// Stage layout per weight format (PE_BF16, PE_FP8_BLOCK128, the 4-bit formats):
 // [A half 0][A half 1][B tile, bf16, swizzled][quantised formats only: code
 // staging], every part 1024-aligned.
 template <int FMT>
 struct Tile {
     static constexpr int C_BYTES = FMT == PE_FP8_BLOCK128 ? BN * BK          // E4M3 codes of the B tile
-                                   : FMT == PE_INT4_GPTQ  ? BN * BK / 2      // int4 codes of the B tile
+                                   : is_4bit(FMT)         ? BN * BK / 2      // 4-bit codes of the B tile
                                                           : 0;
     static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + C_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring
@@ -618,7 +622,7 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmA, const CUten
         // bf16: the B tile itself; quantised: its codes, into the staging buffer
         uint8_t* b = QUANT ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
         // the weight map's inner coordinate counts bytes for int4 (two codes each)
-        const int kx = FMT == PE_INT4_GPTQ ? kb * (BK / 2) : kb * BK;
+        const int kx = is_4bit(FMT) ? kb * (BK / 2) : kb * BK;
         tc::tma_load_2d(a, tmA, &S.full[st], kb * BK, I.ti.x);
         if (two) tc::tma_load_2d(a + A_BYTES, tmA, &S.full[st], kb * BK, I.ti.x + BM);
         if (EPI == 0) {
@@ -652,11 +656,15 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
             scale[h * kMaxScaleCols + c] = __ldcg(reinterpret_cast<const float*>(sc) + (size_t)(h ? rb1 : rb0) * ng + c);
         }
     } else {
-        // every row has its own group scales [rows][ng] fp16; the tile's rows
-        // are one or two contiguous 16-byte-aligned ranges: copy as vectors
-        const int half_vecs = (BN / 2) * ng * 2 / 16;
-        const uint8_t* src0 = sc + (size_t)b_row<EPI>(s, I.n, 0) * ng * 2;
-        const uint8_t* src1 = sc + (size_t)b_row<EPI>(s, I.n, BN / 2) * ng * 2;
+        // every row has its own scales (int4: [rows][K/128] fp16; MXFP4 /
+        // NVFP4: [rows][K/32 or K/16] bytes after the grid's header); the
+        // tile's rows are one or two contiguous 16-byte-aligned ranges: copy
+        // as vectors
+        const int row_bytes = FMT == PE_INT4_GPTQ ? ng * 2 : Kdim / fp4_block(FMT);
+        const uint8_t* grid = sc + fp4_scale_header(FMT);
+        const int half_vecs = (BN / 2) * row_bytes / 16;
+        const uint8_t* src0 = grid + (size_t)b_row<EPI>(s, I.n, 0) * row_bytes;
+        const uint8_t* src1 = grid + (size_t)b_row<EPI>(s, I.n, BN / 2) * row_bytes;
         int4* dst = reinterpret_cast<int4*>(scale4);
         for (int i = ct; i < 2 * half_vecs; i += NCT) {
             const uint8_t* src = i < half_vecs ? src0 + 16 * (size_t)i : src1 + 16 * (size_t)(i - half_vecs);
@@ -664,6 +672,9 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
         }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
+    // NVFP4: the tensor scale (times 1/2) from the scale grid's header
+    const float g_half = FMT == PE_NVFP4 ? 0.5f * __ldcg(reinterpret_cast<const float*>(sc)) : 1.f;
+    (void)g_half;
     for (int kb = 0; kb < kblocks; ++kb) {
         const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
         if (!tc::mbar_wait(&S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) return;
@@ -683,6 +694,23 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
                     const __nv_bfloat162 p1 = __floats2bfloat162_rn(hi.x * scl, hi.y * scl);
                     packed[2 * t] = *reinterpret_cast<const uint32_t*>(&p0);
                     packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
+                }
+            } else if (FMT == PE_MXFP4 || FMT == PE_NVFP4) {
+                // 2*e2m1(q) times half the block scale (exact for MXFP4), rounded to bf16
+                const int k0 = kb * BK + j * 16;
+                const uint8_t* srow = reinterpret_cast<const uint8_t*>(scale4) + r * (Kdim / fp4_block(FMT));
+                const float scl = FMT == PE_NVFP4 ? e4m3x2(srow[k0 / kNvfp4Block]).x * g_half
+                                                  : e8m0_half(srow[k0 / kMxfp4Block]);
+                const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // codes 8h .. 8h+7 of the chunk: one word
+                    uint32_t p[4];
+                    e2m1x8_bf16x2(h ? cv.y : cv.x, p);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const __nv_bfloat162 c2 = __floats2bfloat162_rn(bf_lo(p[i]) * scl, bf_hi(p[i]) * scl);
+                        packed[4 * h + i] = *reinterpret_cast<const uint32_t*>(&c2);
+                    }
                 }
             } else {
                 // the fp16 scale's bits; each weight is the exact product (q - 8) * s rounded to bf16
@@ -741,6 +769,11 @@ __device__ __forceinline__ void mma_tile(StepShared& S, uint8_t* ring, const Til
     }
 }
 
+// SiLU for the prefill epilogue: the hardware exp2-based exponential and a
+// fast divide (relative error around 1e-7, far inside the tolerances).  Paged
+// and unpaged steps run this same code, so they still agree bit for bit.
+__device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f + __expf(-g)); }
+
 // Epilogue (warps 12..15): warp w reads TMEM lanes 32*(w%4).. of the
 // accumulator buffer; in row half hf, lane l owns tile row hf*128 + 32*(w%4) + l.
 template <int EPI>
@@ -760,8 +793,9 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, c
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float h0 = __fmul_rn(silu(__uint_as_float(g[2 * c])), __uint_as_float(u[2 * c]));
-                        const float h1 = __fmul_rn(silu(__uint_as_float(g[2 * c + 1])), __uint_as_float(u[2 * c + 1]));
+                        const float h0 = __fmul_rn(silu_fast(__uint_as_float(g[2 * c])), __uint_as_float(u[2 * c]));
+                        const float h1 =
+                            __fmul_rn(silu_fast(__uint_as_float(g[2 * c + 1])), __uint_as_float(u[2 * c + 1]));
                         const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
                         packed[c] = *reinterpret_cast<const uint32_t*>(&hv);
                     }
@@ -806,7 +840,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ StepShared S;
     __shared__ float sh_scale[FMT == PE_FP8_BLOCK128 ? 2 * kMaxScaleCols : 1];
-    __shared__ __align__(16) __half sh_scale4[FMT == PE_INT4_GPTQ ? BN * kMaxScaleCols : 8];
+    __shared__ __align__(16) __half sh_scale4[is_4bit(FMT) ? kScaleStageBytes / 2 : 8];
     __shared__ int sh_ok, sh_rank, sh_nlink;
     pdl_wait();
     // Roles follow the SM (every kLinkEvery-th SM streams the link), so they
@@ -1001,9 +1035,13 @@ constexpr size_t kAlignMaxSmem = 160 * 1024;  // dynamic shared memory the align
 }  // namespace
 
 bool prefill_tc_supported(const Shape& s) {
-    if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128 && s.dtype != PE_INT4_GPTQ) return false;
+    if (s.dtype != PE_BF16 && s.dtype != PE_FP8_BLOCK128 && !is_4bit(s.dtype)) return false;
     if (align_smem(s) > kAlignMaxSmem) return false;
     if (s.dtype != PE_BF16 && (s.H > kMaxScaleCols * 128 || s.I > kMaxScaleCols * 128)) return false;
+    // MXFP4 / NVFP4: a tile's scale rows (K / block bytes each) fit the staging buffer
+    if ((s.dtype == PE_MXFP4 || s.dtype == PE_NVFP4) &&
+        BN * (s.H > s.I ? s.H : s.I) / fp4_block(s.dtype) > kScaleStageBytes)
+        return false;
     return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
 
@@ -1013,6 +1051,8 @@ size_t prefill_max_rows(int max_entries, int E) {
     const size_t rows = (size_t)max_entries + members * (BM - 1);
     return (rows + BM - 1) / BM * BM;
 }
+
+size_t prefill_max_tiles(int max_entries, int E) { return prefill_max_rows(max_entries, E) / BM; }
 
 size_t prefill_max_items(const Shape& s, size_t max_tiles) { return max_tiles * (size_t)(step_n1(s) + step_n2(s)); }
 
@@ -1027,6 +1067,12 @@ cudaError_t prefill_setup_kernels() {
     if (!e)
         e = cudaFuncSetAttribute(prefill_step_kernel<PE_INT4_GPTQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Tile<PE_INT4_GPTQ>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_step_kernel<PE_MXFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<PE_MXFP4>::SMEM);
+    if (!e)
+        e = cudaFuncSetAttribute(prefill_step_kernel<PE_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Tile<PE_NVFP4>::SMEM);
     return e;
 }
 
@@ -1038,6 +1084,12 @@ cudaError_t prefill_step_ctas_per_sm(int dtype, int* out) {
                     : dtype == PE_INT4_GPTQ
                         ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_INT4_GPTQ>,
                                                                         kStepThreads, Tile<PE_INT4_GPTQ>::SMEM)
+                    : dtype == PE_MXFP4
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_MXFP4>,
+                                                                        kStepThreads, Tile<PE_MXFP4>::SMEM)
+                    : dtype == PE_NVFP4
+                        ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_NVFP4>,
+                                                                        kStepThreads, Tile<PE_NVFP4>::SMEM)
                         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, prefill_step_kernel<PE_BF16>, kStepThreads,
                                                                         Tile<PE_BF16>::SMEM);
     *out = e ? 0 : n;
@@ -1071,6 +1123,8 @@ cudaError_t launch_prefill_step(const LayerDev& L, const Shape& s, const Prefill
                       P, L, s, host_layer, slots_all, slot_base, n1, n2, nchunk, merged, err)
     if (s.dtype == PE_FP8_BLOCK128) PE_STEP(PE_FP8_BLOCK128);
     if (s.dtype == PE_INT4_GPTQ) PE_STEP(PE_INT4_GPTQ);
+    if (s.dtype == PE_MXFP4) PE_STEP(PE_MXFP4);
+    if (s.dtype == PE_NVFP4) PE_STEP(PE_NVFP4);
     PE_STEP(PE_BF16);
 #undef PE_STEP
 }

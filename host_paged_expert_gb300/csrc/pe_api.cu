@@ -29,7 +29,20 @@ constexpr int kRouteInlineMaxTokens = 32;  // plan CTA routes up to one token pe
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-bool dtype_ok(int d) { return d == PE_BF16 || d == PE_FP8_BLOCK128 || d == PE_INT4_GPTQ; }
+bool dtype_ok(int d) {
+    return d == PE_BF16 || d == PE_FP8_BLOCK128 || d == PE_INT4_GPTQ || d == PE_MXFP4 || d == PE_NVFP4;
+}
+
+bool is_fp4(int d) { return d == PE_MXFP4 || d == PE_NVFP4; }
+
+// Expert width as the kernels see it.  MXFP4 and NVFP4 rows carry I padded
+// to a multiple of 128 (zero codes, zero scales): the 4-bit kernels step
+// through an expert's intermediate dimension in 128-input units, and the host
+// row has exactly that padded layout, so what a page-in copies is what the
+// kernels read.  Padded features contribute exact zeros.
+int kernel_intermediate(const pe_config& c) {
+    return is_fp4(c.dtype) ? (c.intermediate + 127) / 128 * 128 : c.intermediate;
+}
 
 // Returns "" when the config is valid, else the reason.
 std::string validate(const pe_config& c) {
@@ -47,13 +60,19 @@ std::string validate(const pe_config& c) {
         return "block-FP8 needs hidden and intermediate to be multiples of 128";
     if (c.dtype == PE_INT4_GPTQ && (c.hidden % kInt4Group || c.intermediate % kInt4Group))
         return "int4 needs hidden and intermediate to be multiples of the 128-input group";
+    if (is_fp4(c.dtype) && c.hidden % 128)
+        return "MXFP4 and NVFP4 need hidden to be a multiple of 128";
+    if (c.dtype == PE_MXFP4 && c.intermediate % kMxfp4Block)
+        return "MXFP4 needs intermediate to be a multiple of its 32-input block";
+    if (c.dtype == PE_NVFP4 && c.intermediate % kNvfp4Block)
+        return "NVFP4 needs intermediate to be a multiple of its 16-input block";
     return "";
 }
 
 void row_layout(const pe_config& c, pe_row_layout* r) {
-    const uint64_t H = (uint64_t)c.hidden, I = (uint64_t)c.intermediate;
+    const uint64_t H = (uint64_t)c.hidden, I = (uint64_t)kernel_intermediate(c);
     std::memset(r, 0, sizeof(*r));
-    // bytes per 2 weights: bf16 4, E4M3 2, int4 1
+    // bytes per 2 weights: bf16 4, E4M3 2, 4-bit formats 1
     const uint64_t per2 = c.dtype == PE_BF16 ? 4 : c.dtype == PE_FP8_BLOCK128 ? 2 : 1;
     uint64_t s13 = 0, s2 = 0;
     if (c.dtype == PE_FP8_BLOCK128) {  // fp32 per 128x128 block
@@ -62,6 +81,10 @@ void row_layout(const pe_config& c, pe_row_layout* r) {
     } else if (c.dtype == PE_INT4_GPTQ) {  // fp16 per output row and 128 inputs
         s13 = 2 * (2 * I) * ((H + kInt4Group - 1) / kInt4Group);
         s2 = 2 * H * ((I + kInt4Group - 1) / kInt4Group);
+    } else if (is_fp4(c.dtype)) {  // one byte per row and block; NVFP4: a 16-byte fp32 tensor-scale header first
+        const uint64_t blk = c.dtype == PE_MXFP4 ? kMxfp4Block : kNvfp4Block, hdr = c.dtype == PE_NVFP4 ? 16 : 0;
+        s13 = hdr + (2 * I) * (H / blk);
+        s2 = hdr + H * (I / blk);
     }
     r->w13_offset = 0;
     r->w13_bytes = I * H * per2;
@@ -81,7 +104,7 @@ Shape make_shape(const pe_config& c, const pe_row_layout& r) {
     s.k = c.top_k;
     s.K = c.num_slots;
     s.H = c.hidden;
-    s.I = c.intermediate;
+    s.I = kernel_intermediate(c);
     s.Wmax = 1;
     s.dtype = c.dtype;
     s.stride = r.row_stride;
@@ -105,6 +128,36 @@ int32_t max_waves(const pe_config& c, int32_t T) {
     if (ent <= c.num_slots) return 1;
     const long long d = ent < c.num_experts ? ent : c.num_experts;
     return (int32_t)((d + c.num_slots - 1) / c.num_slots);
+}
+
+// Writes one MXFP4 / NVFP4 expert, given in its logical shape, into a host
+// row of the padded layout: gate rows 0..I-1 and up rows I..2I-1 of w13 go
+// to rows 0.. and Ip.. of the [2Ip, H/2] code block, each w2 row of I/2
+// bytes to the start of an Ip/2-byte row, and the scale grids likewise (the
+// NVFP4 tensor scale first, in the 16-byte header).  Everything else in the
+// row is zero, so the padding the kernels read is the padding the row holds.
+void load_fp4_row(const pe_config& c, const pe_row_layout& r, uint8_t* row, const uint8_t* w13, const uint8_t* w2,
+                  const uint8_t* s13, const uint8_t* s2) {
+    const size_t H = (size_t)c.hidden, I = (size_t)c.intermediate, Ip = (size_t)kernel_intermediate(c);
+    const size_t blk = c.dtype == PE_MXFP4 ? kMxfp4Block : kNvfp4Block, hdr = c.dtype == PE_NVFP4 ? 16 : 0;
+    std::memset(row, 0, r.row_stride);
+    // w13 codes and scales: logical row j -> padded row j (gate) or Ip + j - I (up)
+    const size_t cb = H / 2, sb = H / blk;
+    for (size_t j = 0; j < 2 * I; ++j) {
+        const size_t pj = j < I ? j : Ip + (j - I);
+        std::memcpy(row + r.w13_offset + pj * cb, w13 + j * cb, cb);
+        std::memcpy(row + r.s13_offset + hdr + pj * sb, s13 + hdr + j * sb, sb);
+    }
+    // w2 codes and scales: H rows, each I inputs wide inside Ip
+    const size_t cw = I / 2, cwp = Ip / 2, sw = I / blk, swp = Ip / blk;
+    for (size_t m = 0; m < H; ++m) {
+        std::memcpy(row + r.w2_offset + m * cwp, w2 + m * cw, cw);
+        std::memcpy(row + r.s2_offset + hdr + m * swp, s2 + hdr + m * sw, sw);
+    }
+    if (hdr) {  // the tensor scales
+        std::memcpy(row + r.s13_offset, s13, 4);
+        std::memcpy(row + r.s2_offset, s2, 4);
+    }
 }
 
 // Bump allocator over the arena; with base == nullptr it only measures.
@@ -141,7 +194,8 @@ struct pe_handle {
     uint8_t* slots = nullptr;
     uint8_t* store_host = nullptr;
     uint8_t* store_dev = nullptr;
-    bool owns_store = false;
+    bool owns_store = false;      // the store was pinned by this handle (cudaHostAlloc)
+    bool external_store = false;  // caller-owned memory registered by this handle (cudaHostRegister)
     std::vector<LayerDev> layers;
     uint8_t* loaded_dev = nullptr;   // [L][E]
     std::vector<uint8_t> loaded_host;
@@ -191,14 +245,14 @@ size_t carve(pe_handle* h, const pe_config& c, const pe_row_layout& r, uint8_t* 
     uint8_t* slots = cv.take<uint8_t>(((size_t)L * K + stage_rows) * r.row_stride);
     uint8_t* loaded = cv.take<uint8_t>((size_t)L * E);
     uint32_t* err = cv.take<uint32_t>(1);
-    float* hbuf = cv.take<float>(maxTk * c.intermediate);
+    float* hbuf = cv.take<float>(maxTk * kernel_intermediate(c));
     float* merged = cv.take<float>(maxTk * c.hidden);
     PrefillDev pre = {};
     if (tc) {
-        const size_t rows = prefill_max_rows((int)maxTk, E), tiles = rows / 128;
+        const size_t rows = prefill_max_rows((int)maxTk, E), tiles = prefill_max_tiles((int)maxTk, E);
         const size_t items = prefill_max_items(make_shape(c, r), tiles);
         pre.x_perm = cv.take<__nv_bfloat16>(rows * c.hidden);
-        pre.h_perm = cv.take<__nv_bfloat16>(rows * c.intermediate);
+        pre.h_perm = cv.take<__nv_bfloat16>(rows * kernel_intermediate(c));
         pre.perm = cv.take<int32_t>(rows);
         pre.tiles = cv.take<int4>(tiles);
         pre.items = cv.take<int2>(items);
@@ -288,7 +342,7 @@ bool encode_map(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint6
                 const cuuint32_t* box, bool bytes) {
     auto fn = encode_fn();
     if (!fn) return false;
-    const cuuint32_t es[3] = {1, 1, 1};
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank,
               const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
               bytes ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -304,7 +358,7 @@ bool encode_bf16(CUtensorMap* m, const void* base, cuuint32_t rank, const cuuint
 pe_status setup_prefill(pe_handle* h) {
     const pe_config& c = h->cfg;
     const PrefillDev& P = h->pre;
-    const cuuint64_t H = (cuuint64_t)c.hidden, I = (cuuint64_t)c.intermediate, rows = (cuuint64_t)P.max_rows;
+    const cuuint64_t H = (cuuint64_t)c.hidden, I = (cuuint64_t)kernel_intermediate(c), rows = (cuuint64_t)P.max_rows;
     const cuuint64_t nslots = (cuuint64_t)c.num_layers * c.num_slots + h->pre.stage_rows, stride = h->row.row_stride;
     bool ok = true;
     {
@@ -319,7 +373,7 @@ pe_status setup_prefill(pe_handle* h) {
     }
     // weight boxes: BN/2 rows of w13 (the gate or the up half of a tile), BN rows of w2
     const cuuint32_t r13 = kPrefillBN / 2, r2 = kPrefillBN;
-    if (c.dtype == PE_INT4_GPTQ) {  // packed int4 code tiles (two codes per byte), decoded in shared memory
+    if (is_4bit(c.dtype)) {  // packed 4-bit code tiles (two codes per byte), decoded in shared memory
         {
             const cuuint64_t d[3] = {H / 2, 2 * I, nslots}, st[2] = {H / 2, stride};
             const cuuint32_t b[3] = {32, r13, 1};
@@ -359,11 +413,54 @@ pe_status setup_prefill(pe_handle* h) {
     return PE_OK;
 }
 
+// An external host store: caller-owned memory (for example one shared
+// mapping that every replica process maps), registered for the handle's
+// lifetime; `filled` marks every expert loaded.
+struct ExternalStore {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+    int filled = 0;
+};
+
+// Registrations of external stores in this process, counted per start
+// address: CUDA refuses to register a range twice, and several handles may
+// share one store (a filling handle and reading handles, for instance).  The
+// range is registered by its first handle and unregistered with its last.
+std::mutex g_reg_mu;
+std::vector<std::pair<void*, std::pair<size_t, int>>> g_regs;  // (ptr, (bytes, handles))
+
+cudaError_t register_external(void* ptr, size_t bytes) {
+    std::lock_guard<std::mutex> lock(g_reg_mu);
+    for (auto& r : g_regs)
+        if (r.first == ptr) {
+            if (r.second.first < bytes) return cudaErrorInvalidValue;  // an overlapping, larger request
+            r.second.second += 1;
+            return cudaSuccess;
+        }
+    const cudaError_t e = cudaHostRegister(ptr, bytes, cudaHostRegisterMapped | cudaHostRegisterPortable);
+    if (!e) g_regs.push_back({ptr, {bytes, 1}});
+    return e;
+}
+
+void unregister_external(void* ptr) {
+    std::lock_guard<std::mutex> lock(g_reg_mu);
+    for (size_t i = 0; i < g_regs.size(); ++i)
+        if (g_regs[i].first == ptr) {
+            if (--g_regs[i].second.second == 0) {
+                cudaHostUnregister(ptr);
+                g_regs.erase(g_regs.begin() + (long)i);
+            }
+            return;
+        }
+}
+
 pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_handle* owner,
-                      pe_handle** out) {
+                      const ExternalStore* ext, pe_handle** out) {
     if (!cfg || !out) return fail(nullptr, PE_ERR_INVALID, "NULL config or output pointer");
     *out = nullptr;
-    if (!dtype_ok(cfg->dtype)) return fail(nullptr, PE_ERR_UNSUPPORTED_DTYPE, "expert dtype must be PE_BF16 or PE_FP8_BLOCK128");
+    if (!dtype_ok(cfg->dtype))
+        return fail(nullptr, PE_ERR_UNSUPPORTED_DTYPE,
+                    "expert dtype must be PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4 or PE_NVFP4");
     const std::string why = validate(*cfg);
     if (!why.empty()) return fail(nullptr, PE_ERR_INVALID, why);
     if (owner) {
@@ -372,7 +469,18 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
             o.hidden != cfg->hidden || o.intermediate != cfg->intermediate || o.dtype != cfg->dtype ||
             o.top_k != cfg->top_k || o.device != cfg->device)
             return fail(nullptr, PE_ERR_INVALID, "shared store needs the same L, E, top_k, H, I, dtype and device");
-        if (!owner->owns_store) return fail(nullptr, PE_ERR_INVALID, "store owner must own its store");
+        if (!owner->owns_store && !owner->external_store)
+            return fail(nullptr, PE_ERR_INVALID, "store owner must own or have registered its store");
+    }
+    if (ext) {  // checked before any CUDA call
+        pe_row_layout rl;
+        row_layout(*cfg, &rl);
+        const size_t need = (size_t)cfg->num_layers * cfg->num_experts * rl.row_stride;
+        if (!ext->ptr) return fail(nullptr, PE_ERR_INVALID, "external host store is NULL");
+        if (reinterpret_cast<uintptr_t>(ext->ptr) % 4096)
+            return fail(nullptr, PE_ERR_INVALID, "external host store must be 4096-byte aligned");
+        if (ext->bytes < need)
+            return fail(nullptr, PE_ERR_INVALID, "external host store too small: need " + std::to_string(need) + " bytes");
     }
     int ndev = 0;
     cudaError_t ce = cudaGetDeviceCount(&ndev);
@@ -441,6 +549,25 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
         h->store_dev = owner->store_dev;
         h->owns_store = false;
         h->loaded_host = owner->loaded_host;
+    } else if (ext) {
+        ce = register_external(ext->ptr, store_bytes);
+        if (ce) {
+            cudaGetLastError();
+            delete h;
+            return fail(nullptr, PE_ERR_HOST_ALLOC,
+                        std::string("could not register the external host store: ") + cudaGetErrorString(ce));
+        }
+        void* dp = nullptr;
+        ce = cudaHostGetDevicePointer(&dp, ext->ptr, 0);
+        if (ce) {
+            unregister_external(ext->ptr);
+            delete h;
+            return fail(nullptr, PE_ERR_CUDA, std::string("cudaHostGetDevicePointer: ") + cudaGetErrorString(ce));
+        }
+        h->store_host = static_cast<uint8_t*>(ext->ptr);
+        h->store_dev = static_cast<uint8_t*>(dp);
+        h->external_store = true;
+        h->loaded_host.assign((size_t)cfg->num_layers * cfg->num_experts, ext->filled ? 1 : 0);
     } else {
         void* p = nullptr;
         ce = cudaHostAlloc(&p, store_bytes, cudaHostAllocMapped | cudaHostAllocPortable);
@@ -474,6 +601,7 @@ pe_status create_impl(const pe_config* cfg, void* arena, size_t arena_bytes, pe_
     if (st != PE_OK) {
         const std::string msg = "device state init failed: " + h->last_error;
         if (h->owns_store) cudaFreeHost(h->store_host);
+        if (h->external_store) unregister_external(h->store_host);
         delete h;
         return fail(nullptr, PE_ERR_CUDA, msg);
     }
@@ -571,19 +699,29 @@ int32_t pe_max_waves(const pe_config* cfg, int32_t num_tokens) {
 }
 
 pe_status pe_create(const pe_config* cfg, void* dev_arena, size_t arena_bytes, pe_handle** out) {
-    return create_impl(cfg, dev_arena, arena_bytes, nullptr, out);
+    return create_impl(cfg, dev_arena, arena_bytes, nullptr, nullptr, out);
+}
+
+pe_status pe_create_external(const pe_config* cfg, void* dev_arena, size_t arena_bytes, void* host_store,
+                             size_t host_store_bytes, int32_t filled, pe_handle** out) {
+    ExternalStore ext;
+    ext.ptr = host_store;
+    ext.bytes = host_store_bytes;
+    ext.filled = filled != 0;
+    return create_impl(cfg, dev_arena, arena_bytes, nullptr, &ext, out);
 }
 
 pe_status pe_create_shared(const pe_config* cfg, void* dev_arena, size_t arena_bytes,
                            pe_handle* store_owner, pe_handle** out) {
     if (!store_owner) return fail(nullptr, PE_ERR_INVALID, "store_owner is NULL");
-    return create_impl(cfg, dev_arena, arena_bytes, store_owner, out);
+    return create_impl(cfg, dev_arena, arena_bytes, store_owner, nullptr, out);
 }
 
 pe_status pe_load_host_expert(pe_handle* h, int32_t layer, int32_t expert, const void* w13,
                               const void* w2, const void* s13, const void* s2) {
     if (!h) return PE_ERR_INVALID;
-    if (!h->owns_store) return fail(h, PE_ERR_INVALID, "load experts through the handle that owns the host store");
+    if (!h->owns_store && !h->external_store)
+        return fail(h, PE_ERR_INVALID, "load experts through the handle that owns or registered the host store");
     if (layer < 0 || layer >= h->cfg.num_layers || expert < 0 || expert >= h->cfg.num_experts)
         return fail(h, PE_ERR_RANGE, "layer or expert out of range");
     if (!w13 || !w2) return fail(h, PE_ERR_INVALID, "w13 and w2 must not be NULL");
@@ -592,11 +730,16 @@ pe_status pe_load_host_expert(pe_handle* h, int32_t layer, int32_t expert, const
     if (!scaled && (s13 || s2)) return fail(h, PE_ERR_INVALID, "bf16 experts take no scales");
     const pe_row_layout& r = h->row;
     uint8_t* row = h->store_host + ((size_t)layer * h->cfg.num_experts + expert) * r.row_stride;
-    std::memcpy(row + r.w13_offset, w13, r.w13_bytes);
-    std::memcpy(row + r.w2_offset, w2, r.w2_bytes);
-    if (scaled) {
-        std::memcpy(row + r.s13_offset, s13, r.s13_bytes);
-        std::memcpy(row + r.s2_offset, s2, r.s2_bytes);
+    if (is_fp4(h->cfg.dtype)) {
+        load_fp4_row(h->cfg, r, row, static_cast<const uint8_t*>(w13), static_cast<const uint8_t*>(w2),
+                     static_cast<const uint8_t*>(s13), static_cast<const uint8_t*>(s2));
+    } else {
+        std::memcpy(row + r.w13_offset, w13, r.w13_bytes);
+        std::memcpy(row + r.w2_offset, w2, r.w2_bytes);
+        if (scaled) {
+            std::memcpy(row + r.s13_offset, s13, r.s13_bytes);
+            std::memcpy(row + r.s2_offset, s2, r.s2_bytes);
+        }
     }
     const size_t idx = (size_t)layer * h->cfg.num_experts + expert;
     if (!h->loaded_host[idx]) {
@@ -662,7 +805,7 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
     // decode sizes page in inside the gate/up kernel; the choice depends on T
     // only, and both routes compute every h with the same code
     const bool pagein_fused = (long long)T * c.top_k <= kFusedMaxEntries;
-    const int fmt = c.dtype;  // PE_BF16, PE_FP8_BLOCK128 or PE_INT4_GPTQ
+    const int fmt = c.dtype;  // a pe_dtype
     if (!pagein_fused && h->tc_ok) {
         // prefill sizes: every wave's page-in and tensor-core GEMMs pipelined
         // in one kernel; every entry lands in the merged buffer, summed after
@@ -687,8 +830,8 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             ProfScope p(h, P_GATEUP_PAGEIN, st);
             e = fmt == PE_FP8_BLOCK128
                     ? launch_gateup_pagein_fp8(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
-                : fmt == PE_INT4_GPTQ
-                    ? launch_gateup_pagein_int4(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                : is_4bit(fmt)
+                    ? launch_gateup_pagein_q4(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st)
                     : launch_gateup_pagein(L, s, x, host_layer, slots_layer, w, T, h->hbuf, h->num_sms, st);
             if (e) return cuda_fail(h, e, "gate/up + page-in kernel");
         } else {
@@ -700,7 +843,7 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             {
                 ProfScope p(h, P_GATEUP, st);
                 e = fmt == PE_FP8_BLOCK128 ? launch_gateup_fp8(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
-                    : fmt == PE_INT4_GPTQ  ? launch_gateup_int4(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
+                    : is_4bit(fmt)         ? launch_gateup_q4(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st)
                                            : launch_gateup(L, s, x, slots_layer, w, T, h->hbuf, h->num_sms, st);
                 if (e) return cuda_fail(h, e, "gate/up kernel");
             }
@@ -709,8 +852,8 @@ pe_status pe_forward(pe_handle* h, int32_t layer, const void* hidden, const floa
             ProfScope p(h, P_DOWN, st);
             e = fmt == PE_FP8_BLOCK128
                     ? launch_down_fp8(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
-                : fmt == PE_INT4_GPTQ
-                    ? launch_down_int4(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
+                : is_4bit(fmt)
+                    ? launch_down_q4(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st)
                     : launch_down(L, s, slots_layer, w, T, h->hbuf, h->merged, y, fused, h->num_sms, st);
             if (e) return cuda_fail(h, e, "down kernel");
         }
@@ -894,6 +1037,7 @@ void pe_destroy(pe_handle* h) {
     cudaDeviceSynchronize();
     for (auto ev : h->pool) cudaEventDestroy(ev);
     if (h->owns_store && h->store_host) cudaFreeHost(h->store_host);
+    if (h->external_store && h->store_host) unregister_external(h->store_host);
     delete h;
 }
 

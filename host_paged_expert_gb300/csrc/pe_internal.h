@@ -17,6 +17,13 @@ constexpr int kPlanMaxThreads = 1024;
 constexpr int kFusedMaxEntries = 64;  // decode: one warp scans a wave's entries per weight row
 constexpr int kFp8Block = 128;
 constexpr int kInt4Group = 128;  // GPTQ int4: inputs per scale
+constexpr int kMxfp4Block = 32;  // MXFP4: inputs per E8M0 scale
+constexpr int kNvfp4Block = 16;  // NVFP4: inputs per E4M3 scale
+// The 4-bit formats (GPTQ int4, MXFP4, NVFP4) share one code layout: two
+// codes per byte, rows of K/2 bytes.
+__host__ __device__ constexpr bool is_4bit(int dtype) {
+    return dtype == PE_INT4_GPTQ || dtype == PE_MXFP4 || dtype == PE_NVFP4;
+}
 // Output columns of one prefill GEMM tile: a gate/up tile reads BN/2 gate and
 // BN/2 up rows of w13, a down tile BN rows of w2 (the weight tensor maps'
 // box heights).
@@ -83,13 +90,14 @@ struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
     CUtensorMap w13;     // 3-D [L*K slots][2I][H], boxes of BN/2 rows: bf16 64 x 64 x 1 (swizzled),
-                         //   FP8 codes 64 x 64 x 1, int4 [..][2I][H/2 bytes] 32 x 64 x 1
+                         //   FP8 codes 64 x 64 x 1, 4-bit codes [..][2I][H/2 bytes] 32 x 64 x 1
     CUtensorMap w2;      // 3-D [L*K slots][H][I], boxes of BN rows: bf16 64 x 128 x 1 (swizzled),
                          //   FP8 codes 64 x 128 x 1, int4 [..][H][I/2 bytes] 32 x 128 x 1
 };
 
 bool prefill_tc_supported(const Shape& s);
 size_t prefill_max_rows(int max_entries, int E);
+size_t prefill_max_tiles(int max_entries, int E);
 size_t prefill_max_items(const Shape& s, size_t max_tiles);
 cudaError_t prefill_setup_kernels();
 // CTAs of the prefill step kernel for this format that fit on one SM (its
@@ -172,16 +180,17 @@ cudaError_t launch_gateup_fp8(const LayerDev& L, const Shape& s, const __nv_bflo
 cudaError_t launch_down_fp8(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
                             int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
                             int num_sms, cudaStream_t st);
-// GPTQ int4 counterparts of the three decode kernels above.
-cudaError_t launch_gateup_pagein_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
-                                      const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
-                                      float* hbuf, int num_sms, cudaStream_t st);
-cudaError_t launch_gateup_int4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
-                               const uint8_t* slots_layer, int wave, int T, float* hbuf, int num_sms,
-                               cudaStream_t st);
-cudaError_t launch_down_int4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
-                             int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
-                             int num_sms, cudaStream_t st);
+// 4-bit (GPTQ int4, MXFP4, NVFP4; chosen by s.dtype) counterparts of the
+// three decode kernels above.
+cudaError_t launch_gateup_pagein_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                                    const uint8_t* host_layer, uint8_t* slots_layer, int wave, int T,
+                                    float* hbuf, int num_sms, cudaStream_t st);
+cudaError_t launch_gateup_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
+                             const uint8_t* slots_layer, int wave, int T, float* hbuf, int num_sms,
+                             cudaStream_t st);
+cudaError_t launch_down_q4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave,
+                           int T, const float* hbuf, float* merged, __nv_bfloat16* out, int fused,
+                           int num_sms, cudaStream_t st);
 // out[t] = sum_j merged[t, j] in entry order, rounded to bf16.
 cudaError_t launch_topk_sum(const Shape& s, const float* merged, __nv_bfloat16* out, int T,
                             cudaStream_t st);

@@ -53,9 +53,19 @@ class MoEShape:
     num_slots: int
     hidden: int
     intermediate: int
-    dtype: str = "bf16"  # "bf16", "fp8" (E4M3, 128x128 blocks, fp32 scales) or
-    # "int4" (GPTQ: 4-bit codes, zero point 8, fp16 scale per output row and 128 inputs)
+    dtype: str = "bf16"  # "bf16", "fp8" (E4M3, 128x128 blocks, fp32 scales),
+    # "int4" (GPTQ: 4-bit codes, zero point 8, fp16 scale per output row and 128 inputs),
+    # "mxfp4" (E2M1 codes, E8M0 scale per row and 32 inputs) or
+    # "nvfp4" (E2M1 codes, E4M3 scale per row and 16 inputs, fp32 scale per tensor)
     block: int = 128
+
+    @property
+    def is_fp4(self) -> bool:
+        return self.dtype in ("mxfp4", "nvfp4")
+
+    @property
+    def fp4_block(self) -> int:
+        return 32 if self.dtype == "mxfp4" else 16
 
     def with_slots(self, k: int) -> "MoEShape":
         return dataclasses.replace(self, num_slots=k)
@@ -72,6 +82,8 @@ class MoEShape:
     @property
     def s13_shape(self) -> tuple[int, int]:
         b = self.block
+        if self.is_fp4:
+            return (2 * self.intermediate, self.hidden // self.fp4_block)
         if self.dtype == "int4":
             return (2 * self.intermediate, -(-self.hidden // b))
         return (-(-2 * self.intermediate // b), -(-self.hidden // b))
@@ -79,6 +91,8 @@ class MoEShape:
     @property
     def s2_shape(self) -> tuple[int, int]:
         b = self.block
+        if self.is_fp4:
+            return (self.hidden, self.intermediate // self.fp4_block)
         if self.dtype == "int4":
             return (self.hidden, -(-self.intermediate // b))
         return (-(-self.hidden // b), -(-self.intermediate // b))
@@ -90,6 +104,8 @@ class MoEShape:
             return 2 * (self.w13_elems + self.w2_elems)
         s13 = self.s13_shape[0] * self.s13_shape[1]
         s2 = self.s2_shape[0] * self.s2_shape[1]
+        if self.is_fp4:  # codes, one byte per block scale, NVFP4 also two fp32 tensor scales
+            return (self.w13_elems + self.w2_elems) // 2 + s13 + s2 + (8 if self.dtype == "nvfp4" else 0)
         if self.dtype == "int4":
             return (self.w13_elems + self.w2_elems) // 2 + 2 * (s13 + s2)
         return self.w13_elems + self.w2_elems + 4 * (s13 + s2)
@@ -99,6 +115,8 @@ TINY = MoEShape(1, 16, 2, 6, 256, 128, "bf16")
 STACK48 = MoEShape(48, 128, 8, 32, 2048, 768, "bf16")
 STACK48_FP8 = MoEShape(48, 128, 8, 40, 2048, 768, "fp8")
 STACK48_INT4 = MoEShape(48, 128, 8, 92, 2048, 768, "int4")
+STACK48_MXFP4 = MoEShape(48, 128, 8, 92, 2048, 768, "mxfp4")
+STACK48_NVFP4 = MoEShape(48, 128, 8, 92, 2048, 768, "nvfp4")
 
 
 # ----------------------------------------------------------------------------
@@ -148,14 +166,17 @@ class ExpertWeights:
     ``s13`` ([ceil(2I/128), ceil(H/128)]) and ``s2`` ([ceil(H/128), ceil(I/128)]);
     GPTQ int4 experts give packed 4-bit codes (uint8, [2I, H/2] and [H, I/2],
     input 2j in the low nibble of byte j) plus fp16 scales ``s13`` ([2I, H/128])
-    and ``s2`` ([H, I/128]).
+    and ``s2`` ([H, I/128]).  MXFP4 / NVFP4 experts give packed E2M1 codes in
+    the same layout plus byte scale grids ``s13`` ([2I, H/32] E8M0 or
+    [2I, H/16] E4M3) and ``s2``; NVFP4 also the fp32 tensor scales ``g13`` and
+    ``g2``.
     """
 
     def __init__(self, shape: MoEShape, seed: int = 0, std: float = 0.02):
         self.shape = shape
         self.seed = seed
         n = shape.w13_elems + shape.w2_elems
-        if shape.dtype == "int4":
+        if shape.dtype == "int4" or shape.is_fp4:
             n //= 2  # two codes per byte
         n_experts = shape.num_layers * shape.num_experts
         pool = max(1 << 25, n + 64 * n_experts)
@@ -165,6 +186,14 @@ class ExpertWeights:
             # the weights are of the 0.02 scale of the bf16 experts
             z = rng.standard_normal(2 * pool, dtype=np.float32)
             q = np.clip(np.rint(z * np.float32(2.5)) + 8, 0, 15).astype(np.uint8)
+            self._pool = q[0::2] | (q[1::2] << 4)
+            z = None
+        elif shape.is_fp4:
+            # E2M1 codes of N(0, 1.5): the nearest of the magnitudes
+            # 0, .5, 1, 1.5, 2, 3, 4, 6 (ties away from zero) and the sign bit
+            z = rng.standard_normal(2 * pool, dtype=np.float32) * np.float32(1.5)
+            mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], dtype=np.float32)
+            q = np.searchsorted(mids, np.abs(z), side="right").astype(np.uint8) | ((z < 0).astype(np.uint8) << 3)
             self._pool = q[0::2] | (q[1::2] << 4)
             z = None
         else:
@@ -186,7 +215,7 @@ class ExpertWeights:
         s = self.shape
         o = self.offset(layer, expert)
         win = self._pool[o : o + self._n]
-        if s.dtype == "int4":
+        if s.dtype == "int4" or s.is_fp4:
             n13 = s.w13_elems // 2
             w13 = win[:n13].reshape(2 * s.intermediate, s.hidden // 2)
             w2 = win[n13:].reshape(s.hidden, s.intermediate // 2)
@@ -202,6 +231,18 @@ class ExpertWeights:
             rng = np.random.default_rng([self.seed, 0x5CA1E, layer, expert])
             out["s13"] = (np.abs(rng.standard_normal(s.s13_shape)) * 0.008).astype(np.float16)
             out["s2"] = (np.abs(rng.standard_normal(s.s2_shape)) * 0.008).astype(np.float16)
+        elif s.dtype == "mxfp4":
+            # E8M0 exponents 2^-8 .. 2^-6 per block: weights of the 0.02 scale
+            rng = np.random.default_rng([self.seed, 0x5CA1E, layer, expert])
+            out["s13"] = rng.integers(119, 122, size=s.s13_shape).astype(np.uint8)
+            out["s2"] = rng.integers(119, 122, size=s.s2_shape).astype(np.uint8)
+        elif s.dtype == "nvfp4":
+            # E4M3 block scales |N(1, 0.25)| and a tensor scale near 0.015
+            rng = np.random.default_rng([self.seed, 0x5CA1E, layer, expert])
+            out["s13"] = _encode_e4m3(np.abs(rng.normal(1.0, 0.25, s.s13_shape)).astype(np.float32))
+            out["s2"] = _encode_e4m3(np.abs(rng.normal(1.0, 0.25, s.s2_shape)).astype(np.float32))
+            out["g13"] = np.float32(0.015 * (1.0 + 0.1 * rng.standard_normal()))
+            out["g2"] = np.float32(0.015 * (1.0 + 0.1 * rng.standard_normal()))
         return out
 
 

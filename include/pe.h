@@ -51,12 +51,17 @@ typedef enum pe_status {
 
 /* Expert storage formats ("Paged Experts", "Supported Configurations and
  * Limitations": unquantised, block-quantised FP8 with 128x128 blocks, and
- * GPTQ int4; other formats are rejected at creation). */
+ * GPTQ int4; "SGLang Paged Experts: corré MoE más grandes que tu VRAM",
+ * "¿Qué es la paginación de expertos…?": MXFP4 and NVFP4 as well; other
+ * formats are rejected at creation).  Activations stay bf16 in every format. */
 typedef enum pe_dtype {
     PE_BF16 = 0,          /* bf16 weights                                    */
     PE_FP8_BLOCK128 = 1,  /* E4M3 weights, one fp32 scale per 128x128 block  */
-    PE_INT4_GPTQ = 2      /* GPTQ int4: 4-bit codes, zero point 8, one fp16
+    PE_INT4_GPTQ = 2,     /* GPTQ int4: 4-bit codes, zero point 8, one fp16
                              scale per output row and group of 128 inputs    */
+    PE_MXFP4 = 3,         /* E2M1 codes, one E8M0 scale per row and 32 inputs*/
+    PE_NVFP4 = 4          /* E2M1 codes, one E4M3 scale per row and 16
+                             inputs, times one fp32 scale per tensor         */
 } pe_dtype;
 
 /* Device error word bits (read through pe_stats). */
@@ -175,16 +180,42 @@ int32_t pe_max_waves(const pe_config* cfg, int32_t num_tokens);
 pe_status pe_create(const pe_config* cfg, void* dev_arena, size_t arena_bytes, pe_handle** out);
 
 /* Like pe_create, but the new handle reads the host store of `store_owner`
- * (same L, E, H, I and dtype required; K and max_tokens may differ).  The
- * owner must outlive the new handle.  Used to run the same experts with
- * another K, e.g. K=E as the unpaged reference. */
+ * (a handle from pe_create or pe_create_external; same L, E, H, I and dtype
+ * required; K and max_tokens may differ).  The owner must outlive the new
+ * handle.  Used to run the same experts with another K, e.g. K=E as the
+ * unpaged reference. */
 pe_status pe_create_shared(const pe_config* cfg, void* dev_arena, size_t arena_bytes,
                            pe_handle* store_owner, pe_handle** out);
 
-/* Copy one expert into its host-store row (a synchronous host memcpy).
+/* Like pe_create, but the host store is caller-owned memory: host_store must
+ * be 4096-byte aligned, hold at least L*E*row_stride bytes (row_stride from
+ * pe_get_row_layout) and stay valid until pe_destroy.  It is how several
+ * replica processes on one host read ONE copy of the experts ("Paged
+ * Experts", "Supported Configurations and Limitations": every expert of every
+ * layer has to be page-locked in host memory, so N private copies would need
+ * N times the host memory): one process maps a shared region (a file under
+ * /dev/shm, say), fills it through a handle created with filled = 0 and
+ * pe_load_host_expert, and every replica, that one included, creates its
+ * handle on the same mapping with filled = 1, which marks every expert loaded.
+ * The library registers the memory (cudaHostRegister, mapped and portable)
+ * while any handle of this process uses it (handles on the same store share
+ * one registration, released with the last of them in pe_destroy); it never
+ * frees it.  A handle with filled = 1 only reads the store.
+ * Errors: as pe_create; PE_ERR_INVALID for a NULL, misaligned or too small
+ *   store (checked before any CUDA call); PE_ERR_HOST_ALLOC if the
+ *   registration fails. */
+pe_status pe_create_external(const pe_config* cfg, void* dev_arena, size_t arena_bytes, void* host_store,
+                             size_t host_store_bytes, int32_t filled, pe_handle** out);
+
+/* Copy one expert into its host-store row (a synchronous host memcpy),
+ * through the handle that created or registered the store.
  *   w13, w2: host pointers in the row layout's formats (bf16 bits, E4M3
- *   codes or packed int4 codes); s13, s2: the scales, fp32 for FP8 and fp16
- *   for int4, NULL for bf16.
+ *   codes or packed 4-bit codes); s13, s2: the scales, fp32 for FP8 and fp16
+ *   for int4, NULL for bf16.  MXFP4 / NVFP4 take their logical shapes
+ *   (w13 [2I, H/2], w2 [H, I/2] bytes; scales [2I, H/B] and [H, I/B] bytes,
+ *   B = 32 or 16), and for NVFP4 each scale pointer starts with a 16-byte
+ *   header holding the tensor's fp32 scale (then 12 ignored bytes); the
+ *   library writes them into the padded row layout, zeros included.
  *   Marks the expert loaded; a later forward that routes to an expert that
  *   was never loaded sets PE_DEVERR_NOT_LOADED.  Loading an expert that is
  *   currently resident does not refresh its slot: load before forwarding, or

@@ -27,6 +27,7 @@ from typing import Callable
 
 import numpy as np
 
+from . import fp4 as _fp4
 from . import fp8 as _fp8
 from . import int4 as _int4
 from .lru import ResidencySim, StepPlan
@@ -52,6 +53,13 @@ def expert_weights(row: dict, dtype: str, block: int = 128) -> tuple[np.ndarray,
         return (
             _int4.dequant_rows(row["w13"], row["s13"], block),
             _int4.dequant_rows(row["w2"], row["s2"], block),
+        )
+    if dtype == "mxfp4":
+        return _fp4.dequant_mx(row["w13"], row["s13"]), _fp4.dequant_mx(row["w2"], row["s2"])
+    if dtype == "nvfp4":
+        return (
+            _fp4.dequant_nv(row["w13"], row["s13"], row["g13"]),
+            _fp4.dequant_nv(row["w2"], row["s2"], row["g2"]),
         )
     raise ValueError(f"unsupported expert dtype {dtype!r}")
 

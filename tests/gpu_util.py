@@ -9,10 +9,10 @@ from host_paged_expert_gb300 import synth
 from oracle import mlp as omlp
 
 # rel-L2 tolerances against the oracle: bf16 and block-FP8 as stated for the
-# layer; GPTQ int4 takes the block-FP8 budget, its error sources being the
-# same (exactly dequantised weights, bf16 rounding of h, of the output and,
-# on the tensor cores, of each scaled weight)
-REL_L2 = {"bf16": 1e-2, "fp8": 3e-2, "int4": 3e-2}
+# layer; GPTQ int4, MXFP4 and NVFP4 take the block-FP8 budget, their error
+# sources being the same (exactly dequantised weights, bf16 rounding of h, of
+# the output and, on the tensor cores, of each scaled weight)
+REL_L2 = {"bf16": 1e-2, "fp8": 3e-2, "int4": 3e-2, "fp4": 3e-2, "mxfp4": 3e-2, "nvfp4": 3e-2}
 
 
 def torch_mod():

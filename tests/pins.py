@@ -328,3 +328,72 @@ def check_int4_gptq_layout(dequant_gptq, seed=1):
     for r in range(n):
         for c in range(k):
             assert w[r, c] == (q[r, c] - 8) * float(s[r, c // 128]), (r, c)
+
+
+# ---------------------------------------------------------------- fp4 (MXFP4, NVFP4)
+
+# The sixteen E2M1 values, typed from the format's published value list
+# (positive codes 0..7, then the same magnitudes negated).
+E2M1_BY_HAND = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def check_e2m1_table(decode_e2m1):
+    got = decode_e2m1(np.arange(16))
+    assert got.tolist() == E2M1_BY_HAND
+    assert np.signbit(got[8]) and not np.signbit(got[0])
+
+
+def check_e8m0_table(decode_e8m0):
+    """Every E8M0 code against torch's float8_e8m0fnu decoding."""
+    import torch
+
+    want = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+    got = decode_e8m0(np.arange(256, dtype=np.uint8))
+    assert np.isnan(got[255]) and np.isnan(want[255])
+    assert np.array_equal(got[:255], want[:255])
+    assert got[127] == 1.0 and got[0] == 2.0 ** -127
+
+
+def _pack_fp4_by_hand(q):
+    """4-bit codes [N, K] -> row bytes [N, K/2], input 2j in the low nibble."""
+    n, k = len(q), len(q[0])
+    out = np.zeros((n, k // 2), dtype=np.uint8)
+    for r in range(n):
+        for j in range(k // 2):
+            out[r, j] = int(q[r][2 * j]) | (int(q[r][2 * j + 1]) << 4)
+    return out
+
+
+def check_fp4_hand_values(dequant_mx, dequant_nv):
+    """A byte 0x9F holds code 15 (-6) in its low nibble and code 9 (-0.5) in
+    its high one.  MX scale code 126 halves; NV: an E4M3 block scale of 2.0
+    (code 0x40) times a global scale of 0.25."""
+    codes = np.array([[0x9F] + [0x00] * 15], dtype=np.uint8)  # one row, K = 32
+    w = dequant_mx(codes, np.array([[126]], dtype=np.uint8))
+    assert w.shape == (1, 32)
+    assert w[0, 0] == -3.0 and w[0, 1] == -0.25 and not w[0, 2:].any()
+    w = dequant_nv(codes, np.array([[0x40, 0x38]], dtype=np.uint8), 0.25)  # 2.0 and 1.0
+    assert w[0, 0] == -3.0 and w[0, 1] == -0.25 and not w[0, 2:16].any()
+
+
+def check_fp4_brute_force(dequant_mx, dequant_nv, seed=3):
+    """Plain loops over (n, k) with each block index written out, on
+    non-square shapes with several blocks per row; the NV global scale is an
+    fp32 value."""
+    from oracle.fp8 import e4m3_value
+
+    rng = np.random.default_rng(seed)
+    for n, k in ((3, 64), (5, 96)):
+        q = rng.integers(0, 16, size=(n, k))
+        packed = _pack_fp4_by_hand(q)
+        smx = rng.integers(118, 134, size=(n, k // 32)).astype(np.uint8)
+        w = dequant_mx(packed, smx)
+        for r in range(n):
+            for c in range(k):
+                assert w[r, c] == E2M1_BY_HAND[q[r, c]] * 2.0 ** (int(smx[r, c // 32]) - 127), (r, c)
+        snv = rng.integers(0x20, 0x58, size=(n, k // 16)).astype(np.uint8)
+        g = float(np.float32(0.0123))
+        w = dequant_nv(packed, snv, g)
+        for r in range(n):
+            for c in range(k):
+                assert w[r, c] == E2M1_BY_HAND[q[r, c]] * e4m3_value(snv[r, c // 16]) * g, (r, c)

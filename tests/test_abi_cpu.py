@@ -64,6 +64,49 @@ def test_row_layout_matches_expert_sizes(L):
         assert i4[k] % 128 == 0
 
 
+def test_fp4_row_layouts(L):
+    """MXFP4: codes plus one E8M0 byte per 32 inputs; NVFP4: one E4M3 byte
+    per 16 inputs plus a 16-byte tensor-scale header per grid.  An
+    intermediate width that is not a multiple of 128 is carried padded to the
+    next multiple (2880 -> 2944), in codes and scales alike."""
+    H, I = 2048, 768
+    mx = _lib.row_layout(synth.STACK48_MXFP4)
+    assert mx["w13_bytes"] == 2 * I * H // 2 and mx["w2_bytes"] == H * I // 2
+    assert mx["s13_bytes"] == 2 * I * H // 32 and mx["s2_bytes"] == H * I // 32
+    assert mx["payload_bytes"] == synth.STACK48_MXFP4.expert_bytes == 2_506_752
+    nv = _lib.row_layout(synth.STACK48_NVFP4)
+    assert nv["s13_bytes"] == 16 + 2 * I * H // 16 and nv["s2_bytes"] == 16 + H * I // 16
+    assert nv["payload_bytes"] == synth.STACK48_NVFP4.expert_bytes + 2 * 12  # headers pad the two fp32 scales
+    for k in ("w13_offset", "s13_offset", "w2_offset", "s2_offset"):
+        assert mx[k] % 128 == 0 and nv[k] % 128 == 0
+    pad = _lib.row_layout(synth.MoEShape(1, 8, 2, 3, 256, 2880, "mxfp4"))
+    assert pad["w13_bytes"] == 2 * 2944 * 256 // 2 and pad["w2_bytes"] == 256 * 2944 // 2
+    assert pad["s13_bytes"] == 2 * 2944 * 256 // 32 and pad["s2_bytes"] == 256 * 2944 // 32
+
+
+@pytest.mark.parametrize("dtype,H,I", [("mxfp4", 200, 256), ("mxfp4", 256, 48), ("nvfp4", 256, 40)])
+def test_fp4_shape_rules(L, dtype, H, I):
+    """H must be a multiple of 128; I a multiple of the format's block."""
+    cfg = _lib.make_config(synth.MoEShape(1, 8, 2, 4, H, I, dtype), 4, 0)
+    assert L.pe_required_device_bytes(ctypes.byref(cfg)) == 0
+
+
+def test_external_store_argument_checks(L):
+    """pe_create_external refuses a NULL, misaligned or too small host store
+    before it touches the device."""
+    import numpy as np
+
+    cfg = _lib.make_config(synth.TINY, 4)
+    need = _lib.host_store_bytes(synth.TINY)
+    buf = np.zeros(need + 8192, np.uint8)
+    base = (buf.ctypes.data + 4095) // 4096 * 4096
+    h = ctypes.c_void_p()
+    for ptr, n in ((None, need), (base + 8, need), (base, need - 1)):
+        st = L.pe_create_external(ctypes.byref(cfg), None, 0, ptr, n, 1, ctypes.byref(h))
+        assert st == _lib.PE_ERR_INVALID, (ptr, n)
+        assert b"external host store" in L.pe_last_error(None)
+
+
 def test_max_waves_from_shapes(L):
     s = synth.STACK48
     assert _lib.max_waves(s, 1) == 1

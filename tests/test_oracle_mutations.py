@@ -51,6 +51,25 @@ MUTANTS = [
      lambda m: pins.check_int4_brute_force(m.dequant_rows)),
     ("oracle.int4", "q[i::8] = (w >> (4 * i)) & 0xF", "q[i::8] = (w >> (4 * (7 - i))) & 0xF",
      lambda m: pins.check_int4_gptq_layout(m.dequant_gptq)),
+    # fp4 (MXFP4, NVFP4)
+    ("oracle.fp4", "q[:, 0::2] = c & 0xF", "q[:, 0::2] = c >> 4",
+     lambda m: pins.check_fp4_hand_values(m.dequant_mx, m.dequant_nv)),
+    ("oracle.fp4", "return sign * (1.0 + man / 2.0) * 2.0 ** (exp - 1)", "return sign * (1.0 + man / 2.0) * 2.0 ** exp",
+     lambda m: pins.check_e2m1_table(m.decode_e2m1)),
+    ("oracle.fp4", "return sign * (man / 2.0)", "return sign * man",
+     lambda m: pins.check_e2m1_table(m.decode_e2m1)),
+    ("oracle.fp4", "sign = -1.0 if code & 0x8 else 1.0", "sign = -1.0 if code & 0x1 else 1.0",
+     lambda m: pins.check_e2m1_table(m.decode_e2m1)),
+    ("oracle.fp4", "else 2.0 ** (code - 127)", "else 2.0 ** (code - 128)",
+     lambda m: pins.check_e8m0_table(m.decode_e8m0)),
+    ("oracle.fp4", "return _block_scaled(codes, decode_e8m0(scales), MX_BLOCK)",
+     "return _block_scaled(codes, decode_e8m0(scales), NV_BLOCK)",
+     lambda m: pins.check_fp4_brute_force(m.dequant_mx, m.dequant_nv)),
+    ("oracle.fp4", "_fp8.decode_e4m3(scales) * g", "_fp8.decode_e4m3(scales)",
+     lambda m: pins.check_fp4_hand_values(m.dequant_mx, m.dequant_nv)),
+    ("oracle.fp4", "return w * block_scale_values[:, np.arange(k) // block]",
+     "return w * block_scale_values[:, np.arange(k) % block_scale_values.shape[1]]",
+     lambda m: pins.check_fp4_brute_force(m.dequant_mx, m.dequant_nv)),
     # mlp
     ("oracle.mlp", "return (silu(gate) * up) @ w2.T", "return (silu(up) * gate) @ w2.T",
      lambda m: pins.check_mlp_hand(m.expert_mlp)),

@@ -249,3 +249,38 @@ def test_gptq_checkpoint_repack_matches_the_oracle():
     assert np.array_equal(int4.dequant_rows(codes, srow), int4.dequant_gptq(qweight, scales))
     w13, s13 = formats.gate_up_rows((codes, srow), (codes[::-1], srow[::-1]))
     assert w13.shape == (2 * n, k // 2) and np.array_equal(w13[n:], codes[::-1]) and np.array_equal(s13[:n], srow)
+
+
+def test_e2m1_table_by_hand():
+    from oracle import fp4
+
+    pins.check_e2m1_table(fp4.decode_e2m1)
+    # the same values from the bit fields, one code at a time
+    assert [fp4.e2m1_value(c) for c in range(16)] == pins.E2M1_BY_HAND
+
+
+def test_e8m0_table_matches_torch():
+    from oracle import fp4
+
+    pins.check_e8m0_table(fp4.decode_e8m0)
+
+
+def test_fp4_hand_values():
+    from oracle import fp4
+
+    pins.check_fp4_hand_values(fp4.dequant_mx, fp4.dequant_nv)
+
+
+def test_fp4_brute_force():
+    from oracle import fp4
+
+    pins.check_fp4_brute_force(fp4.dequant_mx, fp4.dequant_nv)
+
+
+def test_fp4_rejects_bad_grid():
+    from oracle import fp4
+
+    with pytest.raises(ValueError):
+        fp4.dequant_mx(np.zeros((2, 32), np.uint8), np.zeros((2, 1), np.uint8))  # K = 64 needs 2 blocks
+    with pytest.raises(ValueError):
+        fp4.dequant_nv(np.zeros((2, 16), np.uint8), np.zeros((2, 1), np.uint8), 1.0)  # K = 32 needs 2 blocks

@@ -1,7 +1,8 @@
 """Multi-replica bookkeeping on the CPU with two gloo ranks: rank discovery,
 distinct per-replica request streams, the max-over-replicas time and the
-whole-job rate, the reference arm running on rank 0 only, and a replica that
-dies between steps ending the survivor's next collective with an error."""
+whole-job rate, the reference arm running on rank 0 only, a replica that
+dies between steps ending the survivor's next collective with an error, and
+one host store shared by the replicas (filled once, mapped by both)."""
 
 import json
 import os
@@ -60,6 +61,42 @@ def _dying_worker(rank, world, port, out):
     os._exit(0)
 
 
+def _shared_store_worker(rank, world, port, out):
+    import numpy as np
+
+    from host_paged_expert_gb300 import shared_store
+
+    _env(rank, world, port)
+    rep = replicas.from_env()
+    replicas.init(rep, "gloo", timeout_s=60)
+    path = os.path.join(out, "store.bin")
+    nbytes = 3 * 65536 + 4096
+    fills = []
+
+    def fill(store):  # the creator writes every "expert row" once
+        fills.append(rank)
+        a = np.frombuffer(store.view(), dtype=np.uint8)
+        a[:] = (np.arange(nbytes) * 7 % 251).astype(np.uint8)
+
+    store = shared_store.open_for_replicas(rep, path, nbytes, fill)
+    a = np.frombuffer(store.view(), dtype=np.uint8)
+    same = bool(np.array_equal(a, (np.arange(nbytes) * 7 % 251).astype(np.uint8)))
+    aligned = store.ptr % 4096 == 0
+    replicas.barrier(rep)
+    if rank == 0:  # a write after both mapped it: the other replica sees the same pages, not a copy
+        a[12345] = 99
+    replicas.barrier(rep)
+    seen = int(a[12345])
+    replicas.barrier(rep)
+    del a
+    store.close()
+    replicas.barrier(rep)
+    replicas.finish(rep)
+    with open(os.path.join(out, f"r{rank}.json"), "w") as f:
+        json.dump({"filled": fills, "same": same, "aligned": aligned, "seen": seen,
+                   "exists": os.path.exists(path)}, f)
+
+
 def _run(fn, world, tmp_path, limit=120):
     import multiprocessing as mp
 
@@ -116,6 +153,20 @@ def test_lost_replica_ends_next_collective(tmp_path):
     r0 = json.load(open(tmp_path / "r0.json"))
     assert r0["result"] != "no error"
     assert r0["seconds"] < 30
+
+
+def test_shared_host_store_two_replicas(tmp_path):
+    """Replica 0 creates and fills the store; replica 1 maps the filled
+    store; both see the same bytes and the same pages; the creator removes
+    the file when it closes."""
+    pytest.importorskip("torch")
+    codes = _run(_shared_store_worker, 2, tmp_path)
+    assert codes == [0, 0]
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(2)]
+    assert res[0]["filled"] == [0] and res[1]["filled"] == []
+    assert all(r["same"] and r["aligned"] for r in res)
+    assert res[1]["seen"] == 99
+    assert not (tmp_path / "store.bin").exists()
 
 
 def test_reference_arm_only_on_root(capsys):

@@ -60,3 +60,22 @@ def test_zipf_prior_and_prefill():
     assert p.shape == (3, 64, 128)
     h = synth.hidden_states((2, 3), 16)
     assert h.shape == (2, 3, 16) and h.dtype == np.uint16
+
+
+def test_fp4_expert_rows():
+    """MXFP4 / NVFP4 rows: packed E2M1 codes in the int4 layout covering all
+    sixteen codes, byte scale grids of the format's block, NVFP4 tensor
+    scales, and distinct experts."""
+    for dt, blk in (("mxfp4", 32), ("nvfp4", 16)):
+        s = synth.MoEShape(2, 4, 2, 2, 256, 384, dt)
+        w = synth.ExpertWeights(s, seed=1)
+        r = w.row(1, 2)
+        assert r["w13"].shape == (2 * 384, 128) and r["w2"].shape == (256, 192)
+        assert r["s13"].shape == (2 * 384, 256 // blk) and r["s2"].shape == (256, 384 // blk)
+        assert r["w13"].dtype == np.uint8 and r["s13"].dtype == np.uint8
+        codes = np.concatenate([r["w13"].ravel() & 0xF, r["w13"].ravel() >> 4])
+        assert set(np.unique(codes).tolist()) == set(range(16))
+        if dt == "nvfp4":
+            assert r["g13"].dtype == np.float32 and 0.005 < float(r["g13"]) < 0.03
+        assert not np.array_equal(r["w13"], w.row(1, 3)["w13"])
+        assert s.expert_bytes == 3 * 256 * 384 // 2 + (2 * 384 * 256 + 256 * 384) // blk + (8 if dt == "nvfp4" else 0)
