@@ -724,19 +724,20 @@ def oracle_leg(args):
     shape, B, _ = workload(args.workload)
     weights = synth.ExpertWeights(shape, seed=0)
     L = shape.num_layers
-    lg_h, hs_h = make_inputs(shape, B, 1 + int(args.cpu_seconds * 4 / L) + 8)
-    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=args.cpu_seconds, warm=L)
+    warm = max(1, args.warmup)
+    lg_h, hs_h = make_inputs(shape, B, warm + int(args.cpu_seconds * 4 / L) + 8)
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=args.cpu_seconds, warm=warm * L)
     print(json.dumps({"steps": steps, "seconds": sec, "tok_s": steps / L * B / sec,
                       "blas_threads": blas_threads(), "cores": len(os.sched_getaffinity(0))}), flush=True)
 
 
-def oracle_one_core(workload_name: str, seconds: float):
+def oracle_one_core(workload_name: str, seconds: float, warm_tokens: int = 1):
     """The same oracle leg in a fresh interpreter confined to one core, with
     one BLAS thread (a new process, never a fork of this CUDA process)."""
     env = dict(os.environ, **ONE_CORE_ENV)
     cpu = sorted(os.sched_getaffinity(0))[0]
     cmd = [sys.executable, os.path.abspath(__file__), "--oracle-leg", "--workload", workload_name,
-           "--cpu-seconds", str(seconds)]
+           "--cpu-seconds", str(seconds), "--warmup", str(warm_tokens)]
     try:
         r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=seconds * 6 + 120,
                            preexec_fn=lambda: os.sched_setaffinity(0, {cpu}))
@@ -745,15 +746,17 @@ def oracle_one_core(workload_name: str, seconds: float):
         return {"error": f"{type(exc).__name__}: {exc}"}
 
 
-def cpu_baseline_entry(shape, B, weights, lg_h, hs_h, seconds, workload_name):
-    """cpu_baseline: the oracle at all cores and at one core, steady state."""
+def cpu_baseline_entry(shape, B, weights, lg_h, hs_h, seconds, workload_name, warm_tokens):
+    """cpu_baseline: the oracle at all cores and at one core, steady state:
+    from the token the GPU arm's timed passes start at (after its warm-up)."""
     L = shape.num_layers
-    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=seconds, warm=L)
-    one = oracle_one_core(workload_name, seconds)
+    warm_tokens = max(1, warm_tokens)
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, budget_s=seconds, warm=warm_tokens * L)
+    one = oracle_one_core(workload_name, seconds, warm_tokens)
     out = {"value": round(steps / L * B / sec, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
            "blas_threads": blas_threads(), "kind": "oracle",
-           "sample": f"{steps} layer-steps (token-major) after one whole token of warm-up, {sec:.1f} s, "
-                     "fp64 numpy"}
+           "sample": f"{steps} layer-steps (token-major) from token {warm_tokens} on, after {warm_tokens} "
+                     f"warm-up tokens, {sec:.1f} s, fp64 numpy"}
     if "tok_s" in one:
         out["one_core"] = {"value": round(one["tok_s"], 4), "unit": "tok/s", "cores": one["cores"],
                            "blas_threads": one["blas_threads"],
@@ -770,22 +773,20 @@ def run_reference(args, rep):
     shape, B, desc = workload(args.workload)
     weights = synth.ExpertWeights(shape, seed=0)
     L = shape.num_layers
-    # steady state: one whole token (L layer-steps) of warm-up fills the
-    # slots the way a running decode has them, then W more untimed steps
-    warm = L + args.warmup
-    n_tok = -(-(warm + args.steps) // L) + 1
-    lg_h, hs_h = make_inputs(shape, B, n_tok)
-    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, n_steps=args.steps, warm=warm)
+    # a step is what a step of our arm is: one token (all L layer-steps) of
+    # the same workload, after W tokens of warm-up (steady state)
+    lg_h, hs_h = make_inputs(shape, B, args.warmup + args.steps)
+    steps, sec = oracle_layer_steps(shape, weights, lg_h, hs_h, n_steps=args.steps * L, warm=args.warmup * L)
     tok_s = steps / L * B / sec
     line = {"impl": "reference", "metric": METRIC, "value": round(tok_s, 4), "unit": "tok/s", "n_gpus": 1,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / steps * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / (steps / L) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": f"{args.workload}: {desc}",
-                                            "step": "one layer-step of the CPU oracle; tok/s = layer-steps / 48 / s"},
+                                            "step": f"one token through the {L} layers of the CPU oracle"},
             "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": len(os.sched_getaffinity(0)),
                              "blas_threads": blas_threads(), "kind": "oracle",
-                             "sample": f"{steps} layer-steps after {warm} warm-up layer-steps (one whole token, "
-                                       f"then {args.warmup}), token-major over the {L} layers"},
+                             "sample": f"tokens {args.warmup}..{args.warmup + args.steps - 1} of the workload "
+                                       f"({steps} layer-steps) after {args.warmup} warm-up tokens"},
             "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -912,7 +913,7 @@ def main():
             "hbm_gbs": peaks["hbm_gbs"], "link_gbs": link}
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_entry(shape, B, r["weights"], r["lg_h"], r["hs_h"], args.cpu_seconds,
-                                                  args.workload)
+                                                  args.workload, args.warmup)
     print(json.dumps(line), flush=True)
     replicas.finish(rep)
 

@@ -99,8 +99,8 @@ __device__ __forceinline__ void dot32x2_fp4_bf16(int4 wg, int4 wu, const int4 (&
     const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
     const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
     float g[2], u[2];
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {  // kept rolled: fewer decoded pairs live at once
         float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
 #pragma unroll
         for (int q = 2 * hf; q < 2 * hf + 2; ++q) {  // word q: codes 8q..8q+7 against x[q]

@@ -28,6 +28,9 @@ constexpr int kWarps4 = kThreads4 / 32;
 constexpr int kCopyLoads4 = 8;
 constexpr size_t kWarpCopy4 = (size_t)32 * 16 * kCopyLoads4;
 constexpr int kDownRows4 = 8;
+// rows of a down item: FP4's two scales per chunk take registers int4 does not need
+template <int FMT>
+constexpr int down_rows4() { return FMT == PE_INT4_GPTQ ? kDownRows4 : 4; }
 constexpr int kSmemBudget4 = 48 * 1024;
 
 // Gate/up of one wave fused with its page-in; same work split as the bf16
@@ -158,37 +161,37 @@ __global__ void __launch_bounds__(kThreads4) gateup_q4_kernel(LayerDev L, Shape 
 
 // Down projection of one wave (same structure as the bf16 kernel): a CTA owns
 // token t and kDownRows4 rows, warp w the entries j = w, w + 8, ...
-template <int FMT, int CPL>
+template <int FMT, int CPL, int ROWS = down_rows4<FMT>()>
 __global__ void __launch_bounds__(kThreads4) down_q4_kernel(LayerDev L, Shape s, const uint8_t* __restrict__ slots,
                                                              int wave, int T, const float* __restrict__ hbuf,
                                                              float* __restrict__ merged, __nv_bfloat16* __restrict__ out,
                                                              int fused) {
-    __shared__ float sh_p[kMaxTopK][kDownRows4];
+    __shared__ float sh_p[kMaxTopK][ROWS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int blocks_per_t = (s.H + kDownRows4 - 1) / kDownRows4;
+    const int blocks_per_t = (s.H + ROWS - 1) / ROWS;
     const int t = blockIdx.x / blocks_per_t;
-    const int m0 = (blockIdx.x - t * blocks_per_t) * kDownRows4;
+    const int m0 = (blockIdx.x - t * blocks_per_t) * ROWS;
     pdl_wait();
     pdl_trigger();
     if (t >= T) return;
     for (int j = warp; j < s.k; j += kWarps4) {
         const int i = t * s.k + j;
         if (L.entry_wave[i] != wave) {
-            if (fused && lane < kDownRows4) sh_p[j][lane] = 0.f;
+            if (fused && lane < ROWS) sh_p[j][lane] = 0.f;
             continue;
         }
         const uint8_t* base = slots + (size_t)L.entry_slot[i] * s.stride;
-        float p[kDownRows4];
-        Q4Ops<FMT>::template down<CPL, kDownRows4>(base, s, hbuf + (size_t)i * s.I, L.topk_w[i], m0, false,
+        float p[ROWS];
+        Q4Ops<FMT>::template down<CPL, ROWS>(base, s, hbuf + (size_t)i * s.I, L.topk_w[i], m0, false,
                                                    fused ? nullptr : merged + (size_t)i * s.H, p, lane);
         if (fused && lane == 0) {
 #pragma unroll
-            for (int r = 0; r < kDownRows4; ++r) sh_p[j][r] = p[r];
+            for (int r = 0; r < ROWS; ++r) sh_p[j][r] = p[r];
         }
     }
     if (!fused) return;
     __syncthreads();
-    if ((int)threadIdx.x < kDownRows4 && m0 + (int)threadIdx.x < s.H) {
+    if ((int)threadIdx.x < ROWS && m0 + (int)threadIdx.x < s.H) {
         const int r = threadIdx.x;
         float acc = 0.f;
         for (int j = 0; j < s.k; ++j) acc = __fadd_rn(acc, sh_p[j][r]);
@@ -235,7 +238,7 @@ cudaError_t gateup_q4(const LayerDev& L, const Shape& s, const __nv_bfloat16* x,
 template <int FMT>
 cudaError_t down_q4(const LayerDev& L, const Shape& s, const uint8_t* slots_layer, int wave, int T, const float* hbuf,
                     float* merged, __nv_bfloat16* out, int fused, cudaStream_t st) {
-    const long long blocks = (long long)T * ((s.H + kDownRows4 - 1) / kDownRows4);
+    const long long blocks = (long long)T * ((s.H + down_rows4<FMT>() - 1) / down_rows4<FMT>());
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     const int cpl = (s.I / 32 + 31) / 32;

@@ -197,7 +197,7 @@ constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
 // int4 rows are short (H/2 and I/2 bytes), so an int4 down item takes
 // kRowsD4 rows to keep enough bytes in flight (a gate/up item stays one row
 // pair: two spill registers); the per-row arithmetic is unchanged.
-constexpr int kRowsG4 = 2, kRowsD4 = 8;
+constexpr int kRowsG4 = 2, kRowsD4 = 8, kRowsDFp4 = 4;
 // FMT: the expert format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4 or
 // PE_NVFP4; the three 4-bit formats share the int4 tiling).
 template <int EPL, int FMT>
@@ -278,8 +278,10 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     const size_t row_bytes = (size_t)s.H * 2;
     // gate/up row pairs per resident-expert item (a page-in item takes one:
     // the link wants many warps with host reads in flight)
-    constexpr int RPI = is_4bit(FMT) ? kRowsG4 : 1;
-    constexpr int RD = is_4bit(FMT) ? kRowsD4 : kRowsD;  // down rows per item
+    // FP4 rows take fewer per item than int4: their two scales per chunk and
+    // longer decoding would not fit the register budget of two CTAs per SM
+    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;
+    constexpr int RD = FMT == PE_INT4_GPTQ ? kRowsD4 : is_4bit(FMT) ? kRowsDFp4 : kRowsD;  // down rows per item
     const int ipe = s.I / RPI;  // gate/up items per resident expert
     const long long miss_rows = (long long)count * s.I;
     const size_t tail_bytes = s.copy_bytes - s.tail_off;

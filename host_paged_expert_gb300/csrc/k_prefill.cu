@@ -91,32 +91,37 @@ namespace pe {
 namespace {
 
 constexpr int BM = 128, BK = 64, STAGES = 4;
-constexpr int BN = kPrefillBN;        // output columns of a tile (MMA N)
-constexpr int MT = 2 * BM;            // rows of one tile: two M=128 MMAs
-constexpr int A_BYTES = BM * BK * 2;  // one 128-row half of the A tile
-constexpr int B_BYTES = BN * BK * 2;  // the bf16 B tile
+constexpr int kQBN = 128;             // weight rows of a quantised tile (prefill_bn)
+constexpr int A_BYTES = BM * BK * 2;  // one 128-row part of the token (A) tile
+constexpr int kAccCols = 256;         // TMEM columns of one accumulator buffer
 constexpr int kConvWarps = 10;        // warps 2..11: decode quantised weight tiles (idle for bf16)
 constexpr int kEpiWarps = 4;          // warps 12..15: the epilogue (one per TMEM lane quarter)
 constexpr int kStepThreads = (2 + kConvWarps + kEpiWarps) * 32;
 constexpr int kInfoDepth = 4;         // tiles the scheduler may publish ahead
-constexpr uint32_t kTmemCols = 4 * BN;  // two accumulator buffers x two 128-row halves
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // two accumulator buffers
 constexpr int kLinkEvery = 4;         // the CTAs on SMs 0, 4, 8, ... stream the host link
 constexpr int kLinkUnroll = 8;
 constexpr size_t kLinkChunk = (size_t)kStepThreads * 16 * kLinkUnroll;  // 64 KiB per item
 constexpr int kMaxScaleCols = 64;     // FP8 / int4: K / 128 of either GEMM (H, I <= 8192)
-constexpr int kScaleStageBytes = BN * kMaxScaleCols * 2;  // a 4-bit tile's staged scales: 16 KiB
+constexpr int kScaleStageBytes = kQBN * kMaxScaleCols * 2;  // a 4-bit tile's staged scales: 16 KiB
 constexpr uint32_t kSpin = 1u << 22;  // polls, >= 128 ns apart
 
 // Stage layout per weight format (PE_BF16, PE_FP8_BLOCK128, the 4-bit formats):
-// [A half 0][A half 1][B tile, bf16, swizzled][quantised formats only: code
-// staging], every part 1024-aligned.
+// [A part 0 (token rows 0-127)][A part 1 (rows 128-255; quantised formats)]
+// [B tile, bf16, swizzled][quantised formats only: code staging], every part
+// 1024-aligned.
 template <int FMT>
 struct Tile {
-    static constexpr int C_BYTES = FMT == PE_FP8_BLOCK128 ? BN * BK          // E4M3 codes of the B tile
-                                   : is_4bit(FMT)         ? BN * BK / 2      // 4-bit codes of the B tile
+    static constexpr int BN = prefill_bn(FMT);       // weight rows (MMA N)
+    static constexpr int MT = prefill_mt(FMT);       // token rows (one or two M=128 MMAs)
+    static constexpr int A_PARTS = MT / BM;          // 128-row token boxes per k-step
+    static constexpr int B_BYTES = BN * BK * 2;      // the bf16 weight tile
+    static constexpr int C_BYTES = FMT == PE_FP8_BLOCK128 ? BN * BK          // E4M3 codes of the weight tile
+                                   : is_4bit(FMT)         ? BN * BK / 2      // 4-bit codes of the weight tile
                                                           : 0;
-    static constexpr int STAGE_BYTES = 2 * A_BYTES + B_BYTES + C_BYTES;
+    static constexpr int STAGE_BYTES = A_PARTS * A_BYTES + B_BYTES + C_BYTES;
     static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + slack to align the ring
+    static_assert(A_PARTS * BN <= kAccCols, "an accumulator buffer holds the tile");
 };
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -199,7 +204,7 @@ __device__ __forceinline__ void load_entries(const LayerDev& L, int i0, int stri
 }
 
 __global__ void __launch_bounds__(1024) prefill_align_kernel(LayerDev L, Shape s, PrefillDev P, int slot_base, int T,
-                                                             int n1, int n2, unsigned nchunk, int lag) {
+                                                             int n1, int n2, unsigned nchunk, int lag, int MT) {
     __shared__ int sh_g_of_e[kMaxExperts];  // expert -> member
     __shared__ int sh_me[kMaxExperts], sh_ms[kMaxExperts], sh_wp[kMaxExperts];  // expert, slot, wave*2 + paged
     __shared__ int sh_cnt[kMaxExperts], sh_off[kMaxExperts], sh_fill[kMaxExperts];
@@ -599,11 +604,12 @@ struct StepShared {
     uint32_t tmem_base;
 };
 
-// The tile's rows of the B operand for column tile n: gate rows n*BN/2.. and
-// up rows I + n*BN/2.. (gate/up), or rows n*BN.. (down).
+// A quantised tile's rows of the B operand for column tile n: gate rows
+// n*BN/2.. and up rows I + n*BN/2.. (gate/up), or rows n*BN.. (down).
 template <int EPI>
 __device__ __forceinline__ int b_row(const Shape& s, int n_tile, int r) {
-    return EPI == 0 ? (r < BN / 2 ? n_tile * (BN / 2) + r : s.I + n_tile * (BN / 2) + r - BN / 2) : n_tile * BN + r;
+    return EPI == 0 ? (r < kQBN / 2 ? n_tile * (kQBN / 2) + r : s.I + n_tile * (kQBN / 2) + r - kQBN / 2)
+                    : n_tile * kQBN + r;
 }
 
 // Producer: TMA loads of one tile's k-steps into the ring.
@@ -612,15 +618,16 @@ __device__ __forceinline__ void produce_tile(const CUtensorMap* tmA, const CUten
                                              uint8_t* ring, const TileInfo& I, int kblocks, uint32_t kb0,
                                              const Shape& s, uint32_t* err) {
     constexpr bool QUANT = FMT != PE_BF16;
-    const bool two = I.ti.z > BM;
-    const int b_tx = QUANT ? Tile<FMT>::C_BYTES : B_BYTES;
+    constexpr int BN = Tile<FMT>::BN, AP = Tile<FMT>::A_PARTS;
+    const bool two = I.ti.z > BM;  // only tiles of two A parts have more than 128 rows
+    const int b_tx = QUANT ? Tile<FMT>::C_BYTES : Tile<FMT>::B_BYTES;
     for (int kb = 0; kb < kblocks; ++kb) {
         const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
         if (use > 0 && !tc::mbar_wait(&S.empty[st], (use - 1) & 1, err, PE_DEVERR_TIMEOUT)) return;
         tc::mbar_arrive_expect_tx(&S.full[st], (two ? 2 * A_BYTES : A_BYTES) + b_tx);
         uint8_t* a = ring + st * Tile<FMT>::STAGE_BYTES;
         // bf16: the B tile itself; quantised: its codes, into the staging buffer
-        uint8_t* b = QUANT ? a + 2 * A_BYTES + B_BYTES : a + 2 * A_BYTES;
+        uint8_t* b = QUANT ? a + AP * A_BYTES + Tile<FMT>::B_BYTES : a + AP * A_BYTES;
         // the weight map's inner coordinate counts bytes for int4 (two codes each)
         const int kx = is_4bit(FMT) ? kb * (BK / 2) : kb * BK;
         tc::tma_load_2d(a, tmA, &S.full[st], kb * BK, I.ti.x);
@@ -650,7 +657,7 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
     asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");
     if (FMT == PE_FP8_BLOCK128) {
         // the tile's rows lie in one 128-row block per range (gate and up, or down)
-        const int rb0 = b_row<EPI>(s, I.n, 0) / kFp8Block, rb1 = b_row<EPI>(s, I.n, BN - 1) / kFp8Block;
+        const int rb0 = b_row<EPI>(s, I.n, 0) / kFp8Block, rb1 = b_row<EPI>(s, I.n, kQBN - 1) / kFp8Block;
         for (int i = ct; i < 2 * ng; i += NCT) {
             const int h = i / ng, c = i - h * ng;
             scale[h * kMaxScaleCols + c] = __ldcg(reinterpret_cast<const float*>(sc) + (size_t)(h ? rb1 : rb0) * ng + c);
@@ -662,9 +669,9 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
         // as vectors
         const int row_bytes = FMT == PE_INT4_GPTQ ? ng * 2 : Kdim / fp4_block(FMT);
         const uint8_t* grid = sc + fp4_scale_header(FMT);
-        const int half_vecs = (BN / 2) * row_bytes / 16;
+        const int half_vecs = (kQBN / 2) * row_bytes / 16;
         const uint8_t* src0 = grid + (size_t)b_row<EPI>(s, I.n, 0) * row_bytes;
-        const uint8_t* src1 = grid + (size_t)b_row<EPI>(s, I.n, BN / 2) * row_bytes;
+        const uint8_t* src1 = grid + (size_t)b_row<EPI>(s, I.n, kQBN / 2) * row_bytes;
         int4* dst = reinterpret_cast<int4*>(scale4);
         for (int i = ct; i < 2 * half_vecs; i += NCT) {
             const uint8_t* src = i < half_vecs ? src0 + 16 * (size_t)i : src1 + 16 * (size_t)(i - half_vecs);
@@ -678,13 +685,13 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
     for (int kb = 0; kb < kblocks; ++kb) {
         const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
         if (!tc::mbar_wait(&S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) return;
-        uint8_t* bt = ring + st * Tile<FMT>::STAGE_BYTES + 2 * A_BYTES;
-        const uint8_t* codes = bt + B_BYTES;
-        for (int q = ct; q < BN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
+        uint8_t* bt = ring + st * Tile<FMT>::STAGE_BYTES + Tile<FMT>::A_PARTS * A_BYTES;
+        const uint8_t* codes = bt + Tile<FMT>::B_BYTES;
+        for (int q = ct; q < kQBN * (BK / 16); q += NCT) {  // 16-code chunks: row r, chunk j
             const int r = q >> 2, j = q & 3;
             uint32_t packed[8];
             if (FMT == PE_FP8_BLOCK128) {
-                const float scl = scale[((EPI == 0 && r >= BN / 2) ? kMaxScaleCols : 0) + (kb * BK) / kFp8Block];
+                const float scl = scale[((EPI == 0 && r >= kQBN / 2) ? kMaxScaleCols : 0) + (kb * BK) / kFp8Block];
                 const int4 cv = *reinterpret_cast<const int4*>(codes + r * BK + j * 16);
                 const uint32_t w4[4] = {(uint32_t)cv.x, (uint32_t)cv.y, (uint32_t)cv.z, (uint32_t)cv.w};
 #pragma unroll
@@ -745,12 +752,13 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
     }
 }
 
-// MMA issuer: one tile into TMEM accumulator buffer acc (256 columns: two
-// 128-row halves x BN).
+// MMA issuer: one tile into TMEM accumulator buffer acc (256 columns: one
+// or two 128-row parts x BN).
 template <int FMT>
 __device__ __forceinline__ void mma_tile(StepShared& S, uint8_t* ring, const TileInfo& I, int kblocks, uint32_t kb0,
                                          uint32_t dst, uint32_t* err) {
     constexpr bool QUANT = FMT != PE_BF16;
+    constexpr int BN = Tile<FMT>::BN;
     constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
     const bool two = I.ti.z > BM;
     for (int kb = 0; kb < kblocks; ++kb) {
@@ -758,7 +766,7 @@ __device__ __forceinline__ void mma_tile(StepShared& S, uint8_t* ring, const Til
         if (!tc::mbar_wait(QUANT ? &S.conv[st] : &S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) break;
         tc::fence_after_sync();
         const uint32_t a = tc::smem_u32(ring + st * Tile<FMT>::STAGE_BYTES);
-        const uint32_t b = a + 2 * A_BYTES;
+        const uint32_t b = a + Tile<FMT>::A_PARTS * A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bd = tc::smem_desc_sw128(b + kk * 32);
@@ -776,7 +784,7 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f +
 
 // Epilogue (warps 12..15): warp w reads TMEM lanes 32*(w%4).. of the
 // accumulator buffer; in row half hf, lane l owns tile row hf*128 + 32*(w%4) + l.
-template <int EPI>
+template <int EPI, int BN>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, const PrefillDev& P, const LayerDev& L,
                                               const Shape& s, float* __restrict__ merged) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
@@ -965,7 +973,7 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                     if (lane == 0) {
                         if (buse > 0) tc::mbar_wait(&S.acc_empty[buf], (buse - 1) & 1, err, PE_DEVERR_TIMEOUT);
                         tc::fence_after_sync();
-                        mma_tile<FMT>(S, ring, I, kblocks, kb_ring, tmem + buf * (2 * BN), err);
+                        mma_tile<FMT>(S, ring, I, kblocks, kb_ring, tmem + buf * kAccCols, err);
                         tc::mma_commit(&S.acc_full[buf]);
                     }
                     __syncwarp();
@@ -978,9 +986,9 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                     tc::mbar_wait(&S.acc_full[buf], buse & 1, err, PE_DEVERR_TIMEOUT);
                     tc::fence_after_sync();
                     if (I.kind == 0)
-                        epilogue_tile<0>(I, tmem + buf * (2 * BN), P, L, s, merged);
+                        epilogue_tile<0, Tile<FMT>::BN>(I, tmem + buf * kAccCols, P, L, s, merged);
                     else
-                        epilogue_tile<1>(I, tmem + buf * (2 * BN), P, L, s, merged);
+                        epilogue_tile<1, Tile<FMT>::BN>(I, tmem + buf * kAccCols, P, L, s, merged);
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&S.acc_empty[buf]);  // the buffer may be overwritten
@@ -1026,8 +1034,8 @@ __global__ void prefill_wait_selftest_kernel(const unsigned* never, unsigned* ab
     }
 }
 
-int step_n1(const Shape& s) { return s.I / (BN / 2); }
-int step_n2(const Shape& s) { return s.H / BN; }
+int step_n1(const Shape& s) { return s.I / (prefill_bn(s.dtype) / 2); }
+int step_n2(const Shape& s) { return s.H / prefill_bn(s.dtype); }
 unsigned step_nchunk(const Shape& s) { return (unsigned)((s.copy_bytes + kLinkChunk - 1) / kLinkChunk); }
 size_t align_smem(const Shape& s) { return sizeof(int) * ((size_t)2 * s.Wmax + (size_t)3 * s.Wmax * s.K); }
 constexpr size_t kAlignMaxSmem = 160 * 1024;  // dynamic shared memory the align kernel may use
@@ -1040,9 +1048,10 @@ bool prefill_tc_supported(const Shape& s) {
     if (s.dtype != PE_BF16 && (s.H > kMaxScaleCols * 128 || s.I > kMaxScaleCols * 128)) return false;
     // MXFP4 / NVFP4: a tile's scale rows (K / block bytes each) fit the staging buffer
     if ((s.dtype == PE_MXFP4 || s.dtype == PE_NVFP4) &&
-        BN * (s.H > s.I ? s.H : s.I) / fp4_block(s.dtype) > kScaleStageBytes)
+        kQBN * (s.H > s.I ? s.H : s.I) / fp4_block(s.dtype) > kScaleStageBytes)
         return false;
-    return s.H % BN == 0 && s.I % (BN / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
+    const int bn = prefill_bn(s.dtype);
+    return s.H % bn == 0 && s.I % (bn / 2) == 0 && s.H % BK == 0 && s.I % BK == 0;
 }
 
 size_t prefill_max_rows(int max_entries, int E) {
@@ -1107,7 +1116,8 @@ cudaError_t launch_prefill_align(const LayerDev& L, const Shape& s, const Prefil
     // down tiles trail their gate/up tiles by two rounds of the GEMM CTAs
     const int gemm_ctas = num_sms - (num_sms + kLinkEvery - 1) / kLinkEvery;
     cudaError_t e = launch_pdl(prefill_align_kernel, 1, 1024, align_smem(s), st, L, s, P, slot_base, T, step_n1(s),
-                               step_n2(s), step_nchunk(s), 2 * (gemm_ctas > 1 ? gemm_ctas : 1));
+                               step_n2(s), step_nchunk(s), 2 * (gemm_ctas > 1 ? gemm_ctas : 1),
+                               prefill_mt(s.dtype));
     if (e) return e;
     return launch_pdl(prefill_gather_kernel, num_sms * 4, 256, 0, st, x, P, s.H, s.k);
 }

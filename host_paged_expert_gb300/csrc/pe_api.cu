@@ -372,7 +372,7 @@ pe_status setup_prefill(pe_handle* h) {
         ok = ok && encode_bf16(&h->maps.h_perm, P.h_perm, 2, d, st, b);
     }
     // weight boxes: BN/2 rows of w13 (the gate or the up half of a tile), BN rows of w2
-    const cuuint32_t r13 = kPrefillBN / 2, r2 = kPrefillBN;
+    const cuuint32_t r13 = prefill_bn(c.dtype) / 2, r2 = prefill_bn(c.dtype);
     if (is_4bit(c.dtype)) {  // packed 4-bit code tiles (two codes per byte), decoded in shared memory
         {
             const cuuint64_t d[3] = {H / 2, 2 * I, nslots}, st[2] = {H / 2, stride};

@@ -24,10 +24,15 @@ constexpr int kNvfp4Block = 16;  // NVFP4: inputs per E4M3 scale
 __host__ __device__ constexpr bool is_4bit(int dtype) {
     return dtype == PE_INT4_GPTQ || dtype == PE_MXFP4 || dtype == PE_NVFP4;
 }
-// Output columns of one prefill GEMM tile: a gate/up tile reads BN/2 gate and
-// BN/2 up rows of w13, a down tile BN rows of w2 (the weight tensor maps'
-// box heights).
-constexpr int kPrefillBN = 128;
+// Shape of one prefill GEMM tile.  Token rows sit on the MMA's M (TMEM
+// lanes), weight rows on its N: a gate/up tile reads BN/2 gate and BN/2 up
+// rows of w13, a down tile BN rows of w2 (the weight tensor maps' box
+// heights).  bf16 tiles are 128 token rows x 256 weight rows, one M=128,
+// N=256 MMA per 16-deep slice; the quantised formats, whose code staging
+// takes shared memory, 256 token rows x 128 weight rows, two M=128, N=128
+// MMAs sharing the weight tile.
+__host__ __device__ constexpr int prefill_bn(int dtype) { return dtype == PE_BF16 ? 256 : 128; }
+__host__ __device__ constexpr int prefill_mt(int dtype) { return dtype == PE_BF16 ? 128 : 256; }
 
 enum Counter { C_STEPS = 0, C_WAVES, C_ENTRIES, C_DISTINCT, C_HITS, C_PAGE_INS, C_COLD, C_NUM };
 
@@ -89,10 +94,10 @@ struct PrefillDev {
 struct PrefillMaps {
     CUtensorMap x_perm;  // 2-D bf16 [max_rows][H], 64 x 128 boxes
     CUtensorMap h_perm;  // 2-D bf16 [max_rows][I], 64 x 128 boxes
-    CUtensorMap w13;     // 3-D [L*K slots][2I][H], boxes of BN/2 rows: bf16 64 x 64 x 1 (swizzled),
+    CUtensorMap w13;     // 3-D [L*K slots][2I][H], boxes of BN/2 rows: bf16 64 x 128 x 1 (swizzled),
                          //   FP8 codes 64 x 64 x 1, 4-bit codes [..][2I][H/2 bytes] 32 x 64 x 1
-    CUtensorMap w2;      // 3-D [L*K slots][H][I], boxes of BN rows: bf16 64 x 128 x 1 (swizzled),
-                         //   FP8 codes 64 x 128 x 1, int4 [..][H][I/2 bytes] 32 x 128 x 1
+    CUtensorMap w2;      // 3-D [L*K slots][H][I], boxes of BN rows: bf16 64 x 256 x 1 (swizzled),
+                         //   FP8 codes 64 x 128 x 1, 4-bit codes [..][H][I/2 bytes] 32 x 128 x 1
 };
 
 bool prefill_tc_supported(const Shape& s);

@@ -23,8 +23,8 @@ def test_reference_arm_prints_one_contract_line():
     assert d["unit"] == "tok/s" and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 1 and d["n_gpus"] == 1
     assert d["value"] > 0
-    # one layer-step per step, 48 layers per token
-    assert abs(d["value"] - 1.0 / (d["ms_per_step"] * 1e-3) / 48) <= 0.01 * d["value"]
+    # a step is one token through the 48 layers (batch 1): tok/s = 1 / seconds per step
+    assert abs(d["value"] - 1.0 / (d["ms_per_step"] * 1e-3)) <= 0.01 * d["value"]
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert d["e2e"] == {"value": d["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
