@@ -228,9 +228,9 @@ def measured_peaks():
 # reported only while these still hash to the value it was captured on.
 KERNEL_SOURCES = {
     "decode_step": ("k_decode.cu", "plan_block.cuh", "pe_device.cuh", "fp8_device.cuh", "int4_device.cuh",
-                    "pe_internal.h"),
+                    "fp4_device.cuh", "pe_internal.h"),
     "prefill_step": ("k_prefill.cu", "tc_sm100.cuh", "pe_device.cuh", "fp8_device.cuh", "int4_device.cuh",
-                     "pe_internal.h"),
+                     "fp4_device.cuh", "pe_internal.h"),
 }
 
 

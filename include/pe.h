@@ -75,8 +75,9 @@ typedef struct pe_config {
     int32_t num_experts;  /* E, routed experts per layer (1..1024)        */
     int32_t top_k;        /* experts per token (1..min(E, 32))            */
     int32_t num_slots;    /* K, resident experts per layer (top_k..E)     */
-    int32_t hidden;       /* H, model width (multiple of 8; of 128 for FP8, int4)*/
-    int32_t intermediate; /* I, expert width (multiple of 8; of 128 for FP8, int4)*/
+    int32_t hidden;       /* H, model width (multiple of 8; of 128 for FP8, int4, FP4)*/
+    int32_t intermediate; /* I, expert width (multiple of 8; of 128 for FP8, int4;
+                             of the 32- or 16-input block for MXFP4, NVFP4)    */
     int32_t dtype;        /* pe_dtype                                     */
     int32_t max_tokens;   /* largest num_tokens a forward call may pass   */
     int32_t device;       /* CUDA device ordinal                          */
@@ -94,6 +95,13 @@ typedef struct pe_config {
  *       row-major fp16 scales (one per output row and 128 inputs).  A GPTQ
  *       checkpoint (8 codes per int32 along the input, scales [K/128, N])
  *       maps to this by a transpose of both.
+ * MXFP4 / NVFP4: E2M1 codes packed as for int4, with I padded to Ip, the
+ *       next multiple of 128 (zero codes and scales): w13 = [2Ip, H/2]
+ *       (gate rows 0.., up rows Ip..), w2 = [H, Ip/2]; s13 = [2Ip, H/B] and
+ *       s2 = [H, Ip/B] one-byte block scales, B = 32 (MXFP4, E8M0) or 16
+ *       (NVFP4, E4M3); for NVFP4 each grid follows a 16-byte header whose
+ *       first 4 bytes are the tensor's fp32 scale.  pe_load_host_expert takes
+ *       the logical (unpadded) tensors and writes this layout.
  * Offsets are 128-byte aligned. */
 typedef struct pe_row_layout {
     uint64_t w13_offset, w13_bytes;
