@@ -679,9 +679,6 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
         }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory");  // converter warps only
-    // NVFP4: the tensor scale (times 1/2) from the scale grid's header
-    const float g_half = FMT == PE_NVFP4 ? 0.5f * __ldcg(reinterpret_cast<const float*>(sc)) : 1.f;
-    (void)g_half;
     for (int kb = 0; kb < kblocks; ++kb) {
         const uint32_t pos = kb0 + kb, st = pos % STAGES, use = pos / STAGES;
         if (!tc::mbar_wait(&S.full[st], use & 1, err, PE_DEVERR_TIMEOUT)) return;
@@ -703,11 +700,16 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
                     packed[2 * t + 1] = *reinterpret_cast<const uint32_t*>(&p1);
                 }
             } else if (FMT == PE_MXFP4 || FMT == PE_NVFP4) {
-                // 2*e2m1(q) times half the block scale (exact for MXFP4), rounded to bf16
+                // 2*e2m1(q) (exact bf16 pairs) times half the block scale, one
+                // packed bf16 multiply.  Every product is exact: an E8M0 half is
+                // a power of two, and 2*e2m1 (two significant bits) times an
+                // E4M3 half (four) fits bf16's eight.  NVFP4's tensor scale is
+                // applied to the fp32 accumulators in the epilogue.
                 const int k0 = kb * BK + j * 16;
                 const uint8_t* srow = reinterpret_cast<const uint8_t*>(scale4) + r * (Kdim / fp4_block(FMT));
-                const float scl = FMT == PE_NVFP4 ? e4m3x2(srow[k0 / kNvfp4Block]).x * g_half
+                const float scl = FMT == PE_NVFP4 ? e4m3x2(srow[k0 / kNvfp4Block]).x * 0.5f
                                                   : e8m0_half(srow[k0 / kMxfp4Block]);
+                const __nv_bfloat162 s2 = __float2bfloat162_rn(scl);
                 const uint2 cv = *reinterpret_cast<const uint2*>(codes + r * (BK / 2) + j * 8);
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // codes 8h .. 8h+7 of the chunk: one word
@@ -715,7 +717,7 @@ __device__ __forceinline__ void convert_tile(StepShared& S, uint8_t* ring, float
                     e2m1x8_bf16x2(h ? cv.y : cv.x, p);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        const __nv_bfloat162 c2 = __floats2bfloat162_rn(bf_lo(p[i]) * scl, bf_hi(p[i]) * scl);
+                        const __nv_bfloat162 c2 = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&p[i]), s2);
                         packed[4 * h + i] = *reinterpret_cast<const uint32_t*>(&c2);
                     }
                 }
@@ -784,9 +786,11 @@ __device__ __forceinline__ float silu_fast(float g) { return __fdividef(g, 1.f +
 
 // Epilogue (warps 12..15): warp w reads TMEM lanes 32*(w%4).. of the
 // accumulator buffer; in row half hf, lane l owns tile row hf*128 + 32*(w%4) + l.
-template <int EPI, int BN>
+// TS: the accumulators are first multiplied by the weight tensor's scale ts
+// (NVFP4, whose converters leave it out).
+template <int EPI, int BN, bool TS>
 __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, const PrefillDev& P, const LayerDev& L,
-                                              const Shape& s, float* __restrict__ merged) {
+                                              const Shape& s, float ts, float* __restrict__ merged) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3;
     for (int hf = 0; hf < (I.ti.z > BM ? 2 : 1); ++hf) {
         const int r = hf * BM + quarter * 32 + lane;
@@ -801,9 +805,14 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, c
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float h0 = __fmul_rn(silu_fast(__uint_as_float(g[2 * c])), __uint_as_float(u[2 * c]));
-                        const float h1 =
-                            __fmul_rn(silu_fast(__uint_as_float(g[2 * c + 1])), __uint_as_float(u[2 * c + 1]));
+                        float g0 = __uint_as_float(g[2 * c]), g1 = __uint_as_float(g[2 * c + 1]);
+                        float u0 = __uint_as_float(u[2 * c]), u1 = __uint_as_float(u[2 * c + 1]);
+                        if (TS) {
+                            g0 = __fmul_rn(ts, g0), g1 = __fmul_rn(ts, g1);
+                            u0 = __fmul_rn(ts, u0), u1 = __fmul_rn(ts, u1);
+                        }
+                        const float h0 = __fmul_rn(silu_fast(g0), u0);
+                        const float h1 = __fmul_rn(silu_fast(g1), u1);
                         const __nv_bfloat162 hv = __floats2bfloat162_rn(h0, h1);
                         packed[c] = *reinterpret_cast<const uint32_t*>(&hv);
                     }
@@ -816,7 +825,7 @@ __device__ __forceinline__ void epilogue_tile(const TileInfo& I, uint32_t acc, c
             }
         } else {
             const int entry = r < I.ti.z ? P.perm[I.ti.x + r] : -1;
-            const float w = entry >= 0 ? L.topk_w[entry] : 0.f;
+            const float w = entry >= 0 ? (TS ? __fmul_rn(L.topk_w[entry], ts) : L.topk_w[entry]) : 0.f;
             for (int c4 = 0; c4 < BN / 32; ++c4) {
                 uint32_t v[32];
                 tc::tmem_ld32(trow + c4 * 32, v);
@@ -985,10 +994,17 @@ __global__ void __launch_bounds__(kStepThreads, 1)
                 } else {  // epilogue
                     tc::mbar_wait(&S.acc_full[buf], buse & 1, err, PE_DEVERR_TIMEOUT);
                     tc::fence_after_sync();
+                    constexpr bool TS = FMT == PE_NVFP4;
+                    // NVFP4: the tensor scale from the head of the slot's scale grid
+                    // (written with the codes, so present once they were converted)
+                    const float ts =
+                        TS ? __ldcg(reinterpret_cast<const float*>(slots_all + (size_t)I.ti.y * s.stride +
+                                                                   (I.kind == 0 ? s.s13_off : s.s2_off)))
+                           : 1.f;
                     if (I.kind == 0)
-                        epilogue_tile<0, Tile<FMT>::BN>(I, tmem + buf * kAccCols, P, L, s, merged);
+                        epilogue_tile<0, Tile<FMT>::BN, TS>(I, tmem + buf * kAccCols, P, L, s, ts, merged);
                     else
-                        epilogue_tile<1, Tile<FMT>::BN>(I, tmem + buf * kAccCols, P, L, s, merged);
+                        epilogue_tile<1, Tile<FMT>::BN, TS>(I, tmem + buf * kAccCols, P, L, s, ts, merged);
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(&S.acc_empty[buf]);  // the buffer may be overwritten
