@@ -91,23 +91,26 @@ __device__ __forceinline__ float fp4_global_half(const uint8_t* scale_region, bo
     }
 }
 
-// Gate and up dot products of one 32-code chunk against the same 32 bf16
-// values, each as the sums over codes 0..15 and 16..31 (2*v units): every
-// half as an even-input and an odd-input chain in input order, added at the
-// end.  Products are exact and each step rounds once.
-__device__ __forceinline__ void dot32x2_fp4_bf16(int4 wg, int4 wu, const int4 (&x)[4], float2& pg, float2& pu) {
-    const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
-    const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
-    float g[2], u[2];
+// Gate and up dot products of one 32-code chunk against its 32 bf16 values
+// (64 bytes at xc), each as the sums over codes 0..15 and 16..31 (2*v units):
+// every half as an even-input and an odd-input chain in input order, added at
+// the end.  Products are exact and each step rounds once.  The loop over the
+// halves stays rolled (fewer decoded pairs live) and takes its words by
+// selects: words indexed at run time would be placed in local memory.
+__device__ __forceinline__ void dot32x2_fp4_bf16(int4 wg, int4 wu, const uint8_t* xc, float2& pg, float2& pu) {
+    float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
 #pragma unroll 1
-    for (int hf = 0; hf < 2; ++hf) {  // kept rolled: fewer decoded pairs live at once
+    for (int hf = 0; hf < 2; ++hf) {  // words 2hf and 2hf + 1 against x at xc + 32hf
         float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
+        const uint32_t gw[2] = {hf ? (uint32_t)wg.z : (uint32_t)wg.x, hf ? (uint32_t)wg.w : (uint32_t)wg.y};
+        const uint32_t uw[2] = {hf ? (uint32_t)wu.z : (uint32_t)wu.x, hf ? (uint32_t)wu.w : (uint32_t)wu.y};
 #pragma unroll
-        for (int q = 2 * hf; q < 2 * hf + 2; ++q) {  // word q: codes 8q..8q+7 against x[q]
-            const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
+        for (int q = 0; q < 2; ++q) {  // word 2hf + q: codes 8(2hf + q) .. +7
+            const int4 xq = *reinterpret_cast<const int4*>(xc + 32 * hf + 16 * q);
+            const uint32_t xv[4] = {(uint32_t)xq.x, (uint32_t)xq.y, (uint32_t)xq.z, (uint32_t)xq.w};
             uint32_t pgv[4], puv[4];
-            e2m1x8_bf16x2(gv[q], pgv);
-            e2m1x8_bf16x2(uv[q], puv);
+            e2m1x8_bf16x2(gw[q], pgv);
+            e2m1x8_bf16x2(uw[q], puv);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 ge = fma_bf16_lo(pgv[i], xv[i], ge);
@@ -116,11 +119,17 @@ __device__ __forceinline__ void dot32x2_fp4_bf16(int4 wg, int4 wu, const int4 (&
                 uo = fma_bf16_hh(puv[i], xv[i], uo);
             }
         }
-        g[hf] = __fadd_rn(ge, go);
-        u[hf] = __fadd_rn(ue, uo);
+        const float gs = __fadd_rn(ge, go), us = __fadd_rn(ue, uo);
+        if (hf) {
+            g1 = gs;
+            u1 = us;
+        } else {
+            g0 = gs;
+            u0 = us;
+        }
     }
-    pg = make_float2(g[0], g[1]);
-    pu = make_float2(u[0], u[1]);
+    pg = make_float2(g0, g1);
+    pu = make_float2(u0, u1);
 }
 
 // The two 16-code halves of sum_{e<32} 2*v_e * h_e (input order within each):
@@ -157,11 +166,8 @@ __device__ __forceinline__ float row_pair_h_fp4(const int4 (&gv)[CPL], const int
     for (int c = 0; c < CPL; ++c) {
         const int idx = lane + 32 * c;
         if (idx < nchunk) {
-            int4 x[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) x[v] = *reinterpret_cast<const int4*>(xr + 64 * (size_t)idx + 16 * v);
             float2 pg, pu;
-            dot32x2_fp4_bf16(gv[c], uv[c], x, pg, pu);
+            dot32x2_fp4_bf16(gv[c], uv[c], xr + 64 * (size_t)idx, pg, pu);
             ag = fmaf(sg[c].y, pg.y, fmaf(sg[c].x, pg.x, ag));
             au = fmaf(su[c].y, pu.y, fmaf(su[c].x, pu.x, au));
         }

@@ -78,20 +78,28 @@ __device__ __forceinline__ void dot8_int4_bf16(uint32_t w, const uint32_t (&xv)[
     od = fma_bf16_hh(p37, xv[3], od);  // input 7
 }
 
-// Gate and up dot products of one 32-code chunk against the same 32 bf16
-// values: pg = sum_e (g_e - 8) x_e and pu likewise.  Each is accumulated as
-// an even-input and an odd-input partial sum (in input order within each)
-// added at the end, so the four chains run side by side.  The products are
-// exact and each step rounds once, as fmaf on the values widened to fp32.
-__device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const int4 (&x)[4], float& pg, float& pu) {
-    const uint32_t gv[4] = {(uint32_t)wg.x, (uint32_t)wg.y, (uint32_t)wg.z, (uint32_t)wg.w};
-    const uint32_t uv[4] = {(uint32_t)wu.x, (uint32_t)wu.y, (uint32_t)wu.z, (uint32_t)wu.w};
+// Gate and up dot products of one 32-code chunk against its 32 bf16 values
+// (64 bytes at xc): pg = sum_e (g_e - 8) x_e and pu likewise.  Each is
+// accumulated as an even-input and an odd-input partial sum (in input order
+// within each) added at the end, so the four chains run side by side.  The
+// products are exact and each step rounds once, as fmaf on the values widened
+// to fp32.  The loop over the chunk's two 16-code halves stays rolled (a
+// smaller body, fewer values live) and takes its words by selects: words
+// indexed at run time would be placed in local memory.
+__device__ __forceinline__ void dot32x2_int4_bf16(int4 wg, int4 wu, const uint8_t* xc, float& pg, float& pu) {
     float ge = 0.f, go = 0.f, ue = 0.f, uo = 0.f;
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {  // kept rolled: a smaller loop body stays in the instruction cache
-        const uint32_t xv[4] = {(uint32_t)x[q].x, (uint32_t)x[q].y, (uint32_t)x[q].z, (uint32_t)x[q].w};
-        dot8_int4_bf16(gv[q], xv, ge, go);
-        dot8_int4_bf16(uv[q], xv, ue, uo);
+    for (int hf = 0; hf < 2; ++hf) {  // words 2hf and 2hf + 1: codes 16hf .. 16hf + 15
+        const uint32_t g0 = hf ? (uint32_t)wg.z : (uint32_t)wg.x, g1 = hf ? (uint32_t)wg.w : (uint32_t)wg.y;
+        const uint32_t u0 = hf ? (uint32_t)wu.z : (uint32_t)wu.x, u1 = hf ? (uint32_t)wu.w : (uint32_t)wu.y;
+        const int4 xa = *reinterpret_cast<const int4*>(xc + 32 * hf);
+        const int4 xb = *reinterpret_cast<const int4*>(xc + 32 * hf + 16);
+        const uint32_t xva[4] = {(uint32_t)xa.x, (uint32_t)xa.y, (uint32_t)xa.z, (uint32_t)xa.w};
+        const uint32_t xvb[4] = {(uint32_t)xb.x, (uint32_t)xb.y, (uint32_t)xb.z, (uint32_t)xb.w};
+        dot8_int4_bf16(g0, xva, ge, go);
+        dot8_int4_bf16(u0, xva, ue, uo);
+        dot8_int4_bf16(g1, xvb, ge, go);
+        dot8_int4_bf16(u1, xvb, ue, uo);
     }
     pg = __fadd_rn(ge, go);
     pu = __fadd_rn(ue, uo);
@@ -166,11 +174,8 @@ __device__ __forceinline__ float row_pair_h_int4(const int4 (&gv)[CPL], const in
     for (int c = 0; c < CPL; ++c) {
         const int idx = lane + 32 * c;
         if (idx < nchunk) {
-            int4 x[4];
-#pragma unroll
-            for (int v = 0; v < 4; ++v) x[v] = *reinterpret_cast<const int4*>(xr + 64 * (size_t)idx + 16 * v);
             float pg, pu;
-            dot32x2_int4_bf16(gv[c], uv[c], x, pg, pu);
+            dot32x2_int4_bf16(gv[c], uv[c], xr + 64 * (size_t)idx, pg, pu);
             ag = fmaf(sg[c], pg, ag);
             au = fmaf(su[c], pu, au);
         }
