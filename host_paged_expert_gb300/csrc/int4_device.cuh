@@ -227,11 +227,18 @@ __device__ __forceinline__ void load_row_pair_int4(const uint8_t* base, const Sh
     }
 }
 
+// Position of float4 v (inputs 32 idx + 4v .. +3) of an h vector staged in
+// shared memory: the eight float4 of chunk idx are stored XOR-swizzled by idx,
+// so the lanes of a warp (one chunk each) read eight different bank groups.
+__device__ __forceinline__ int hs_index(int idx, int v) { return idx * 8 + (v ^ (idx & 7)); }
+
 // p = w * (down_m . h) for ROWS rows m0.. of one entry, written to out_row
 // (or returned in p_out when it is not null).  The down rows' codes are
 // [H, I/2] bytes, their scales [H, I/128] fp16.  CPL = 16-byte chunks (32
-// codes) of an I-long row per lane.  l2_only reads past L1.
-template <int CPL, int ROWS>
+// codes) of an I-long row per lane.  l2_only reads past L1.  HS: h is the
+// entry's h staged in shared memory in the hs_index layout (else read
+// through L2).
+template <int CPL, int ROWS, bool HS = false>
 __device__ __forceinline__ void down_rows_int4(const uint8_t* w2, const __half* s2, const float* h, float wj, int m0,
                                                int H, int I, bool l2_only, float* out_row, float* p_out, int lane) {
     const int nchunk = I >> 5;
@@ -256,8 +263,9 @@ __device__ __forceinline__ void down_rows_int4(const uint8_t* w2, const __half* 
         const int idx = lane + 32 * c;
 #pragma unroll
         for (int v = 0; v < 8; ++v)
-            hv[c][v] = idx < nchunk ? __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v))
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[c][v] = idx >= nchunk ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : HS ? reinterpret_cast<const float4*>(h)[hs_index(idx, v)]
+                            : __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v));
     }
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {

@@ -67,6 +67,10 @@ constexpr int kLinkSmEvery = 3, kLinkSmEveryInt4Batch = 6;
 __host__ __device__ __forceinline__ int decode_meta_words(const Shape& s) {
     return (2 * s.K + 3 * kFusedMaxEntries + 3) & ~3;
 }
+// 32-bit words after the plan that hold one entry's h during the down
+// projections of the 4-bit formats (I floats, I a multiple of 128); staged x
+// follows.
+__host__ __device__ __forceinline__ int decode_hstage_words(const Shape& s) { return is_4bit(s.dtype) ? s.I : 0; }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
@@ -235,7 +239,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     // x is copied to shared memory asynchronously, underneath the planning
     const uint8_t* xbase = reinterpret_cast<const uint8_t*>(x);
     if (stage_x) {
-        int4* sx = reinterpret_cast<int4*>(sh_mexp + decode_meta_words(s));
+        int4* sx = reinterpret_cast<int4*>(sh_mexp + decode_meta_words(s) + decode_hstage_words(s));
         const int nvec = T * s.H / 8;
         for (int i = threadIdx.x; i < nvec; i += blockDim.x) {
             const unsigned dst = (unsigned)__cvta_generic_to_shared(sx + i);
@@ -509,17 +513,28 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         cta_arrive(&sync[D_HITS]);
     }
 
+    // The 4-bit formats' down items read the entry's h from shared memory:
+    // the eight warps of a CTA take eight consecutive down items of one
+    // entry, and the CTA stages that entry's h once for all of them (in the
+    // hs_index layout) rather than every warp reading it through L2.
+    float* sh_h = reinterpret_cast<float*>(sh_mexp + decode_meta_words(s));
+    auto stage_h = [&](int e) {
+        if constexpr (is_4bit(FMT)) {
+            const float4* src = reinterpret_cast<const float4*>(hbuf + (size_t)e * s.I);
+            float4* dst = reinterpret_cast<float4*>(sh_h);
+            for (int i = threadIdx.x; i < s.I / 4; i += kThr) dst[hs_index(i >> 3, i & 7)] = __ldcg(src + i);
+        }
+    };
     // down projection rows m0.. of entry e into the merged buffer
     auto down_entry = [&](int e, int m0) {
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
         const float we = sh_ew[e];
         if constexpr (FMT == PE_MXFP4 || FMT == PE_NVFP4)
-            down_rows_fp4<FMT, CPLI4, RD>(sb + s.w2_off, sb + s.s2_off, hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true,
-                                          merged + (size_t)e * s.H, nullptr, lane);
+            down_rows_fp4<FMT, CPLI4, RD, true>(sb + s.w2_off, sb + s.s2_off, sh_h, we, m0, s.H, s.I, true,
+                                                merged + (size_t)e * s.H, nullptr, lane);
         else if constexpr (FMT == PE_INT4_GPTQ)
-            down_rows_int4<CPLI4, RD>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off),
-                                          hbuf + (size_t)e * s.I, we, m0, s.H, s.I, true, merged + (size_t)e * s.H,
-                                          nullptr, lane);
+            down_rows_int4<CPLI4, RD, true>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off), sh_h, we,
+                                            m0, s.H, s.I, true, merged + (size_t)e * s.H, nullptr, lane);
         else if constexpr (FMT == PE_FP8_BLOCK128)
             down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), hbuf + (size_t)e * s.I,
                                  we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
@@ -528,35 +543,41 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     };
 
     // ---- phase 2: down projections ----
+    // Down items are numbered per entry in blocks of kWp (row blocks padded to
+    // a multiple of kWp), so the kWp items a CTA takes at once, one per warp,
+    // belong to one entry.
+    const long long rbp = (row_blocks + kWp - 1) / kWp * kWp;
     // Resident experts: as soon as every resident expert's h is done.  Items
     // go out eight at a time (one per warp) from a per-step ticket, so link
     // CTAs that finish their page-ins early (small or few page-ins) help.
     if (hbm_cta || hbm_items > 0) {
         cta_wait(&sync[D_HITS], (unsigned)hbm_ctas, err, &sh_flag);
-        const long long items = (long long)sh_nhit * row_blocks;
+        const long long items = (long long)sh_nhit * rbp;
         __shared__ unsigned sh_ticket;
         for (;;) {
+            // every warp is done with the previous items (and their staged h)
             if (threadIdx.x == 0) sh_ticket = atomicAdd(&sync[H_TICKET], (unsigned)kWp);
             __syncthreads();
             const long long base = sh_ticket;
-            __syncthreads();  // every warp has read it before thread 0 takes the next
+            if (base < items) stage_h(sh_hit_list[base / rbp]);
+            __syncthreads();  // h staged, and every warp has read the ticket before thread 0 takes the next
             if (base >= items) break;
             const long long it = base + warp;
-            if (it < items) {
-                const int e = sh_hit_list[it / row_blocks];
-                const int m0 = (int)(it % row_blocks) * RD;
-                down_entry(e, m0);
-            }
+            const int blk = (int)(it % rbp);
+            if (blk < row_blocks) down_entry(sh_hit_list[it / rbp], blk * RD);
         }
     }
     // paged experts: once the link is drained (their h and their w2 rows)
     cta_wait(&sync[D_LINK], (unsigned)link_ctas, err, &sh_flag);
     {
-        const long long items = (long long)sh_nmiss * row_blocks;
-        for (long long it = (long long)blockIdx.x * kWp + warp; it < items; it += (long long)G * kWp) {
-            const int e = sh_miss_list[it / row_blocks];
-            const int m0 = (int)(it % row_blocks) * RD;
-            down_entry(e, m0);
+        const long long items = (long long)sh_nmiss * rbp;
+        for (long long base = (long long)blockIdx.x * kWp; base < items; base += (long long)G * kWp) {
+            __syncthreads();  // every warp is done with the previous items' staged h
+            stage_h(sh_miss_list[base / rbp]);
+            __syncthreads();
+            const long long it = base + warp;
+            const int blk = (int)(it % rbp);
+            if (blk < row_blocks) down_entry(sh_miss_list[it / rbp], blk * RD);
         }
     }
     cta_arrive(&sync[S_DOWN]);
@@ -605,7 +626,8 @@ bool decode_fused_supported(const Shape& s, int T) {
                       : is_4bit(s.dtype) ? (s.H <= 32 * 32 * CPLH4 && s.I <= 32 * 32 * CPLI4)
                                                 : (s.H <= 32 * 8 * CPLH && s.I <= 32 * 8 * CPLI);
     return (long long)T * s.k <= kFusedMaxEntries && (long long)T * s.k <= s.K && s.E <= kPlanCap &&
-           s.K <= kPlanCap && dims && (size_t)4 * decode_meta_words(s) <= (size_t)kDynBudget;
+           s.K <= kPlanCap && dims &&
+           (size_t)4 * (decode_meta_words(s) + decode_hstage_words(s)) <= (size_t)kDynBudget;
 }
 
 cudaError_t decode_setup_kernels() {
@@ -657,7 +679,7 @@ cudaError_t launch_decode_fused(const LayerDev& L, const Shape& s, const float* 
                                 __nv_bfloat16* out, unsigned* sync, uint32_t* err, int num_sms, int ctas_per_sm,
                                 cudaStream_t st) {
     const int grid = num_sms * ctas_per_sm;  // every CTA is resident at once (decode_ctas_per_sm)
-    const size_t meta = (size_t)4 * decode_meta_words(s);
+    const size_t meta = (size_t)4 * (decode_meta_words(s) + decode_hstage_words(s));
     const size_t xbytes = (size_t)T * s.H * 2;
     const int stage = meta + xbytes <= (size_t)kDynBudget;
     const size_t smem = meta + (stage ? xbytes : 0);
