@@ -219,7 +219,7 @@ __device__ __forceinline__ void load_row_pair_fp4(const uint8_t* base, const Sha
 // (or returned in p_out when it is not null).  The down rows' codes are
 // [H, I/2] bytes, their scale grid [H, I/block] after the header.  CPL =
 // 16-byte chunks (32 codes) of an I-long row per lane.  l2_only reads past L1.
-// HS: h staged in shared memory in the hs_index layout (else read through L2).
+// HS: h staged in shared memory in the hs_pos<8> layout (else read through L2).
 template <int FMT, int CPL, int ROWS, bool HS = false>
 __device__ __forceinline__ void down_rows_fp4(const uint8_t* w2, const uint8_t* s2_region, const float* h, float wj,
                                               int m0, int H, int I, bool l2_only, float* out_row, float* p_out,
@@ -249,7 +249,7 @@ __device__ __forceinline__ void down_rows_fp4(const uint8_t* w2, const uint8_t* 
 #pragma unroll
         for (int v = 0; v < 8; ++v)
             hv[c][v] = idx >= nchunk ? make_float4(0.f, 0.f, 0.f, 0.f)
-                       : HS ? reinterpret_cast<const float4*>(h)[hs_index(idx, v)]
+                       : HS ? reinterpret_cast<const float4*>(h)[hs_pos<8>(idx, v)]
                             : __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v));
     }
 #pragma unroll

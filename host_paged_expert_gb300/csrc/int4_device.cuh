@@ -25,42 +25,6 @@ __device__ __forceinline__ uint32_t i4_pair_bf16(uint32_t w) {
     return *reinterpret_cast<const uint32_t*>(&d);
 }
 
-// c + a * b for bf16 a, b (the low or high halves of two 32-bit registers)
-// with one rounding to fp32: the mixed-precision fma of sm_100 and later,
-// equal to fmaf(float(a), float(b), c).
-__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
-    float d;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
-        : "=f"(d)
-        : "r"(a), "r"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float fma_bf16_hl(uint32_t a, uint32_t b, float c) {  // a high, b low
-    float d;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bl, %3;\n\t}"
-        : "=f"(d)
-        : "r"(a), "r"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float fma_bf16_lh(uint32_t a, uint32_t b, float c) {  // a low, b high
-    float d;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bh, %3;\n\t}"
-        : "=f"(d)
-        : "r"(a), "r"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float fma_bf16_hh(uint32_t a, uint32_t b, float c) {
-    float d;
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
-        : "=f"(d)
-        : "r"(a), "r"(b), "f"(c));
-    return d;
-}
-
 // One row's even-input and odd-input partial sums over the 8 codes of word w
 // against the 8 bf16 inputs in xv[0..3] (xv[i] holds inputs 2i, 2i+1): each
 // chain takes its inputs in ascending order.  The codes are decoded two at a
@@ -227,16 +191,11 @@ __device__ __forceinline__ void load_row_pair_int4(const uint8_t* base, const Sh
     }
 }
 
-// Position of float4 v (inputs 32 idx + 4v .. +3) of an h vector staged in
-// shared memory: the eight float4 of chunk idx are stored XOR-swizzled by idx,
-// so the lanes of a warp (one chunk each) read eight different bank groups.
-__device__ __forceinline__ int hs_index(int idx, int v) { return idx * 8 + (v ^ (idx & 7)); }
-
 // p = w * (down_m . h) for ROWS rows m0.. of one entry, written to out_row
 // (or returned in p_out when it is not null).  The down rows' codes are
 // [H, I/2] bytes, their scales [H, I/128] fp16.  CPL = 16-byte chunks (32
 // codes) of an I-long row per lane.  l2_only reads past L1.  HS: h is the
-// entry's h staged in shared memory in the hs_index layout (else read
+// entry's h staged in shared memory in the hs_pos<8> layout (else read
 // through L2).
 template <int CPL, int ROWS, bool HS = false>
 __device__ __forceinline__ void down_rows_int4(const uint8_t* w2, const __half* s2, const float* h, float wj, int m0,
@@ -264,7 +223,7 @@ __device__ __forceinline__ void down_rows_int4(const uint8_t* w2, const __half* 
 #pragma unroll
         for (int v = 0; v < 8; ++v)
             hv[c][v] = idx >= nchunk ? make_float4(0.f, 0.f, 0.f, 0.f)
-                       : HS ? reinterpret_cast<const float4*>(h)[hs_index(idx, v)]
+                       : HS ? reinterpret_cast<const float4*>(h)[hs_pos<8>(idx, v)]
                             : __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v));
     }
 #pragma unroll

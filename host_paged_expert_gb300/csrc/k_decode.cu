@@ -68,9 +68,8 @@ __host__ __device__ __forceinline__ int decode_meta_words(const Shape& s) {
     return (2 * s.K + 3 * kFusedMaxEntries + 3) & ~3;
 }
 // 32-bit words after the plan that hold one entry's h during the down
-// projections of the 4-bit formats (I floats, I a multiple of 128); staged x
-// follows.
-__host__ __device__ __forceinline__ int decode_hstage_words(const Shape& s) { return is_4bit(s.dtype) ? s.I : 0; }
+// projections (I floats, I a multiple of 8); staged x follows.
+__host__ __device__ __forceinline__ int decode_hstage_words(const Shape& s) { return s.I; }
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
     unsigned v;
@@ -111,7 +110,8 @@ __device__ __forceinline__ bool cta_wait(const unsigned* ctr, unsigned target, u
 }
 
 // p = w * (down_m . h) for kRowsD rows m0.. of one entry, written to merged.
-// CPL = 16-byte chunks of an I-long row per lane.
+// CPL = 16-byte chunks of an I-long row per lane.  h: the entry's h staged in
+// shared memory (hs_pos<2> layout).
 template <int CPL>
 __device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, float wj, int m0, int H, int I,
                                           float* merged_row, int lane) {
@@ -131,8 +131,8 @@ __device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, flo
     for (int c = 0; c < CPL; ++c) {
         const int idx = lane + 32 * c;
         if (idx < nchunk) {
-            hv[c][0] = __ldcg(reinterpret_cast<const float4*>(h + 8 * idx));
-            hv[c][1] = __ldcg(reinterpret_cast<const float4*>(h + 8 * idx + 4));
+            hv[c][0] = reinterpret_cast<const float4*>(h)[hs_pos<2>(idx, 0)];
+            hv[c][1] = reinterpret_cast<const float4*>(h)[hs_pos<2>(idx, 1)];
         } else {
             hv[c][0] = hv[c][1] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -149,7 +149,8 @@ __device__ __forceinline__ void down_rows(const uint8_t* w2, const float* h, flo
 }
 
 // FP8 version: E4M3 codes with the 128x128 block scales of w2 (all kRowsD rows
-// lie in one 128-row block), the same arithmetic as the FP8 down kernel.
+// lie in one 128-row block), the same arithmetic as the FP8 down kernel; h
+// staged in shared memory (hs_pos<4> layout).
 template <int CPL>
 __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2, const float* h, float wj, int m0,
                                               int H, int I, float* merged_row, int lane) {
@@ -173,7 +174,7 @@ __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2
         if (idx < nchunk) {
             sc[c] = __ldcg(srow + (idx * 16) / kFp8Block);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) hv[c][v] = __ldcg(reinterpret_cast<const float4*>(h + 16 * idx + 4 * v));
+            for (int v = 0; v < 4; ++v) hv[c][v] = reinterpret_cast<const float4*>(h)[hs_pos<4>(idx, v)];
         } else {
             sc[c] = 0.f;
 #pragma unroll
@@ -192,15 +193,16 @@ __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2
 }
 
 // Dynamic shared memory: [member experts K][member slots K][entry keys nent]
-// [entry member nent] padded to 4 ints, then the tokens' x when it fits.
+// [entry member nent] padded to 4 ints, then one entry's h (I floats) for the
+// down items, then the tokens' x when it fits.
 // Chunks per lane cover H <= 2048 and I <= 1024 (bf16: 8 and 4 chunks of 8
 // values, FP8: 4 and 2 chunks of 16 codes, int4: 2 and 1 chunks of 32 codes);
-// chunks past the row are skipped,
-// so the arithmetic is that of the exact chunk counts.
+// chunks past the row are skipped, so the arithmetic is that of the exact
+// chunk counts.
 constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
-// int4 rows are short (H/2 and I/2 bytes), so an int4 down item takes
-// kRowsD4 rows to keep enough bytes in flight (a gate/up item stays one row
-// pair: two spill registers); the per-row arithmetic is unchanged.
+// int4 rows are short (H/2 and I/2 bytes), so an int4 gate/up item takes
+// kRowsG4 row pairs and a down item kRowsD4 rows to keep enough bytes in
+// flight; the per-row arithmetic is unchanged.
 constexpr int kRowsG4 = 2, kRowsD4 = 8, kRowsDFp4 = 4;
 // FMT: the expert format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4 or
 // PE_NVFP4; the three 4-bit formats share the int4 tiling).
@@ -513,17 +515,16 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         cta_arrive(&sync[D_HITS]);
     }
 
-    // The 4-bit formats' down items read the entry's h from shared memory:
-    // the eight warps of a CTA take eight consecutive down items of one
-    // entry, and the CTA stages that entry's h once for all of them (in the
-    // hs_index layout) rather than every warp reading it through L2.
+    // Down items read the entry's h from shared memory: the eight warps of a
+    // CTA take eight consecutive down items of one entry, and the CTA stages
+    // that entry's h once for all of them (hs_pos layout, F4 float4s per
+    // lane chunk) rather than every warp reading it through L2.
+    constexpr int F4 = is_4bit(FMT) ? 8 : FMT == PE_FP8_BLOCK128 ? 4 : 2;
     float* sh_h = reinterpret_cast<float*>(sh_mexp + decode_meta_words(s));
     auto stage_h = [&](int e) {
-        if constexpr (is_4bit(FMT)) {
-            const float4* src = reinterpret_cast<const float4*>(hbuf + (size_t)e * s.I);
-            float4* dst = reinterpret_cast<float4*>(sh_h);
-            for (int i = threadIdx.x; i < s.I / 4; i += kThr) dst[hs_index(i >> 3, i & 7)] = __ldcg(src + i);
-        }
+        const float4* src = reinterpret_cast<const float4*>(hbuf + (size_t)e * s.I);
+        float4* dst = reinterpret_cast<float4*>(sh_h);
+        for (int i = threadIdx.x; i < s.I / 4; i += kThr) dst[hs_pos<F4>(i / F4, i % F4)] = __ldcg(src + i);
     };
     // down projection rows m0.. of entry e into the merged buffer
     auto down_entry = [&](int e, int m0) {
@@ -536,10 +537,10 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
             down_rows_int4<CPLI4, RD, true>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off), sh_h, we,
                                             m0, s.H, s.I, true, merged + (size_t)e * s.H, nullptr, lane);
         else if constexpr (FMT == PE_FP8_BLOCK128)
-            down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), hbuf + (size_t)e * s.I,
-                                 we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+            down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), sh_h, we, m0, s.H,
+                                 s.I, merged + (size_t)e * s.H, lane);
         else
-            down_rows<CPLI>(sb + s.w2_off, hbuf + (size_t)e * s.I, we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
+            down_rows<CPLI>(sb + s.w2_off, sh_h, we, m0, s.H, s.I, merged + (size_t)e * s.H, lane);
     };
 
     // ---- phase 2: down projections ----

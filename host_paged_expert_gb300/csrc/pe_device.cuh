@@ -24,14 +24,52 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// acc += sum of the 8 bf16 products of w and x, in element order.
+// c + a * b for bf16 a, b (the low or high halves of two 32-bit registers)
+// with one rounding to fp32: the mixed-precision fma of sm_100 and later,
+// equal to fmaf(float(a), float(b), c).
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hl(uint32_t a, uint32_t b, float c) {  // a high, b low
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bl, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_lh(uint32_t a, uint32_t b, float c) {  // a low, b high
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bh, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fma_bf16_hh(uint32_t a, uint32_t b, float c) {
+    float d;
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+        : "=f"(d)
+        : "r"(a), "r"(b), "f"(c));
+    return d;
+}
+
+// acc += sum of the 8 bf16 products of w and x, in element order, each
+// through the mixed-precision fma (the same value as fmaf on the operands
+// widened to fp32).
 __device__ __forceinline__ float dot8_bf16(int4 w, int4 x, float acc) {
     const uint32_t wv[4] = {(uint32_t)w.x, (uint32_t)w.y, (uint32_t)w.z, (uint32_t)w.w};
     const uint32_t xv[4] = {(uint32_t)x.x, (uint32_t)x.y, (uint32_t)x.z, (uint32_t)x.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        acc = fmaf(__uint_as_float(wv[q] << 16), __uint_as_float(xv[q] << 16), acc);
-        acc = fmaf(__uint_as_float(wv[q] & 0xffff0000u), __uint_as_float(xv[q] & 0xffff0000u), acc);
+        acc = fma_bf16_lo(wv[q], xv[q], acc);
+        acc = fma_bf16_hh(wv[q], xv[q], acc);
     }
     return acc;
 }
@@ -81,6 +119,19 @@ namespace pe {
 // (it returns once that kernel has completed and its writes are visible),
 // and pdl_trigger() to let the next kernel start early.  Without the launch
 // attribute both are no-ops.
+// Position of float4 v of chunk idx (F4 float4s per chunk, one chunk per
+// lane) in an h vector staged in shared memory: the float4s of each chunk are
+// XOR-swizzled by the chunk index so that the eight lanes of a quarter warp,
+// reading the same v of eight consecutive chunks, hit eight different 16-byte
+// bank groups.
+template <int F4>
+__device__ __forceinline__ int hs_pos(int idx, int v) {
+    static_assert(F4 == 2 || F4 == 4 || F4 == 8, "chunks of 8, 16 or 32 h values");
+    if constexpr (F4 == 8) return idx * 8 + (v ^ (idx & 7));
+    else if constexpr (F4 == 4) return idx * 4 + (v ^ ((idx >> 1) & 3));
+    else return idx * 2 + (v ^ ((idx >> 2) & 1));
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
