@@ -200,9 +200,9 @@ __device__ __forceinline__ void down_rows_fp8(const uint8_t* w2, const float* s2
 // chunks past the row are skipped, so the arithmetic is that of the exact
 // chunk counts.
 constexpr int CPLH = 8, CPLI = 4, CPLH8 = 4, CPLI8 = 2, CPLH4 = 2, CPLI4 = 1;
-// int4 rows are short (H/2 and I/2 bytes), so an int4 gate/up item takes
-// kRowsG4 row pairs and a down item kRowsD4 rows to keep enough bytes in
-// flight; the per-row arithmetic is unchanged.
+// 4-bit rows are short (H/2 and I/2 bytes), so a resident 4-bit gate/up item
+// takes kRowsG4 row pairs and an int4 down item kRowsD4 rows to keep enough
+// bytes in flight; the per-row arithmetic is unchanged.
 constexpr int kRowsG4 = 2, kRowsD4 = 8, kRowsDFp4 = 4;
 // FMT: the expert format (PE_BF16, PE_FP8_BLOCK128, PE_INT4_GPTQ, PE_MXFP4 or
 // PE_NVFP4; the three 4-bit formats share the int4 tiling).
@@ -284,9 +284,7 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
     const size_t row_bytes = (size_t)s.H * 2;
     // gate/up row pairs per resident-expert item (a page-in item takes one:
     // the link wants many warps with host reads in flight)
-    // FP4 rows take fewer per item than int4: their two scales per chunk and
-    // longer decoding would not fit the register budget of two CTAs per SM
-    constexpr int RPI = FMT == PE_INT4_GPTQ ? kRowsG4 : 1;
+    constexpr int RPI = is_4bit(FMT) ? kRowsG4 : 1;
     constexpr int RD = FMT == PE_INT4_GPTQ ? kRowsD4 : is_4bit(FMT) ? kRowsDFp4 : kRowsD;  // down rows per item
     const int ipe = s.I / RPI;  // gate/up items per resident expert
     const long long miss_rows = (long long)count * s.I;
