@@ -220,7 +220,7 @@ __device__ __forceinline__ void load_row_pair_fp4(const uint8_t* base, const Sha
 // [H, I/2] bytes, their scale grid [H, I/block] after the header.  CPL =
 // 16-byte chunks (32 codes) of an I-long row per lane.  l2_only reads past L1.
 // HS: h staged in shared memory in the hs_pos<8> layout (else read through L2).
-template <int FMT, int CPL, int ROWS, bool HS = false>
+template <int FMT, int CPL, int ROWS, bool HS = false, bool TR = false>
 __device__ __forceinline__ void down_rows_fp4(const uint8_t* w2, const uint8_t* s2_region, const float* h, float wj,
                                               int m0, int H, int I, bool l2_only, float* out_row, float* p_out,
                                               int lane) {
@@ -252,19 +252,29 @@ __device__ __forceinline__ void down_rows_fp4(const uint8_t* w2, const uint8_t* 
                        : HS ? reinterpret_cast<const float4*>(h)[hs_pos<8>(idx, v)]
                             : __ldcg(reinterpret_cast<const float4*>(h + 32 * idx + 4 * v));
     }
+    float d[ROWS];
 #pragma unroll
     for (int r = 0; r < ROWS; ++r) {
-        float d = 0.f;
+        d[r] = 0.f;
 #pragma unroll
         for (int c = 0; c < CPL; ++c)
             if (lane + 32 * c < nchunk) {
                 const float2 hh = dot32_fp4_f32(wv[r][c], hv[c]);
-                d = fmaf(sc[r][c].y, hh.y, fmaf(sc[r][c].x, hh.x, d));
+                d[r] = fmaf(sc[r][c].y, hh.y, fmaf(sc[r][c].x, hh.x, d[r]));
             }
-        d = warp_sum(d);
-        const float p = __fmul_rn(wj, d);
-        if (p_out) p_out[r] = p;
-        if (lane == 0 && out_row && m0 + r < H) out_row[m0 + r] = p;
+    }
+    if constexpr (TR) {  // row totals by the transposed butterfly, written by one lane each
+        constexpr int SH = ROWS == 8 ? 2 : ROWS == 4 ? 3 : ROWS == 2 ? 4 : 5;
+        const float t = warp_sum_rows<ROWS>(d, lane);
+        const int r = lane >> SH;
+        if ((lane & ((1 << SH) - 1)) == 0 && m0 + r < H) out_row[m0 + r] = __fmul_rn(wj, t);
+    } else {
+#pragma unroll
+        for (int r = 0; r < ROWS; ++r) {
+            const float p = __fmul_rn(wj, warp_sum(d[r]));
+            if (p_out) p_out[r] = p;
+            if (lane == 0 && out_row && m0 + r < H) out_row[m0 + r] = p;
+        }
     }
 }
 

@@ -529,10 +529,10 @@ __global__ void __launch_bounds__(kThr, 2) decode_step_kernel(LayerDev L, Shape 
         const uint8_t* sb = slots + (size_t)sh_ekey[e] * s.stride;
         const float we = sh_ew[e];
         if constexpr (FMT == PE_MXFP4 || FMT == PE_NVFP4)
-            down_rows_fp4<FMT, CPLI4, RD, true>(sb + s.w2_off, sb + s.s2_off, sh_h, we, m0, s.H, s.I, true,
+            down_rows_fp4<FMT, CPLI4, RD, true, true>(sb + s.w2_off, sb + s.s2_off, sh_h, we, m0, s.H, s.I, true,
                                                 merged + (size_t)e * s.H, nullptr, lane);
         else if constexpr (FMT == PE_INT4_GPTQ)
-            down_rows_int4<CPLI4, RD, true>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off), sh_h, we,
+            down_rows_int4<CPLI4, RD, true, true>(sb + s.w2_off, reinterpret_cast<const __half*>(sb + s.s2_off), sh_h, we,
                                             m0, s.H, s.I, true, merged + (size_t)e * s.H, nullptr, lane);
         else if constexpr (FMT == PE_FP8_BLOCK128)
             down_rows_fp8<CPLI8>(sb + s.w2_off, reinterpret_cast<const float*>(sb + s.s2_off), sh_h, we, m0, s.H,

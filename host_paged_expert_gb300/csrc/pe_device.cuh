@@ -60,6 +60,34 @@ __device__ __forceinline__ float fma_bf16_hh(uint32_t a, uint32_t b, float c) {
     return d;
 }
 
+// Totals over the warp of R per-lane values (R rows), by a transposed
+// butterfly: at each of the first log2(R) steps (lane distance 16, 8, ...) a
+// lane keeps half of the rows it holds, adds its partner's copy of them and
+// hands the other half to the partner, then the usual butterfly finishes.
+// Every row's total is formed by the same tree of additions as warp_sum (so
+// the same value, bit for bit) with R - 1 + 5 - log2(R) shuffles instead of
+// 5R.  Lane l returns the total of row (l >> (5 - log2 R)) & (R - 1).
+template <int R>
+__device__ __forceinline__ float warp_sum_rows(float (&v)[R], int lane) {
+    static_assert(R == 1 || R == 2 || R == 4 || R == 8, "1, 2, 4 or 8 rows");
+    constexpr int LOGR = R == 8 ? 3 : R == 4 ? 2 : R == 2 ? 1 : 0;
+#pragma unroll
+    for (int step = 0; step < LOGR; ++step) {
+        const int o = 16 >> step, n = R >> step;  // rows held before this step
+        const bool hi = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < n / 2; ++i) {
+            const float keep = hi ? v[i + n / 2] : v[i];
+            const float send = hi ? v[i] : v[i + n / 2];
+            v[i] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, o));
+        }
+    }
+    float t = v[0];
+#pragma unroll
+    for (int o = 16 >> LOGR; o; o >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, o));
+    return t;
+}
+
 // acc += sum of the 8 bf16 products of w and x, in element order, each
 // through the mixed-precision fma (the same value as fmaf on the operands
 // widened to fp32).
