@@ -29,8 +29,11 @@
 //
 // Every value is computed by the same device code, in the same order, as in
 // the multi-kernel path (row_pair_h for h, the lane-chunked dot product and
-// warp sum for a down row, p = w * d, the sum over j = 0..k-1 from zero), so
-// the two paths give the same bits and the output still equals K = E.
+// the same tree of additions over the warp for a down row - warp_sum, or
+// warp_sum_rows for the 4-bit rows - p = w * d, the sum over j = 0..k-1 from
+// zero), so the two paths give the same bits and the output still equals
+// K = E.  The down items read the entry's h from a copy in shared memory
+// (stage_h), with the same values.
 
 #include "fp4_device.cuh"
 #include "fp8_device.cuh"
