@@ -112,7 +112,7 @@ def parse():
     p.add_argument("--probe-bytes", type=int, default=2 << 30)
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: run a shorter stack of the same layer shape")
-    p.add_argument("--repeats", type=int, default=3,
+    p.add_argument("--repeats", type=int, default=5,
                    help="timed passes of the value and e2e measurements (median reported)")
     p.add_argument("--oracle-leg", action="store_true", help=argparse.SUPPRESS)
     return p.parse_args()
